@@ -1,0 +1,452 @@
+#!/usr/bin/env python3
+"""FAVOR+ attention benchmark: one JSON line with tokens/s, roofline fraction, e2e and CPU baseline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one full FAVOR+ attention call (every kernel of the path: features, state, readout for
+the non-causal form; the chunked scan for the causal form) over one batch of seeded synthetic input
+already resident in HBM. The default workload is the (B, H, n, d) = (1, 8, 1024, 64) shape of the
+linear-attention lesson's exercise with m = 256 random features, bf16 in / fp32 accumulate.
+
+Timing: W untimed warm-up steps; K timed steps bracketed by a barrier and device synchronisation;
+each step timed by CUDA events on the launching stream; L2 flushed (a 512 MB write) before every
+timed step when the step's inputs are smaller than 2x L2; SM clocks sampled through NVML during the
+timed region. Multi-GPU (torchrun): every rank runs an independent replica of the workload (the
+path has no exchange step), `value` is the tokens of all ranks over the slowest rank's time.
+
+--impl reference times the fp64 CPU oracle (the only reference implementation: the pages ship no
+code) on the host cores, on a bounded sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import seeded_inputs as si  # noqa: E402
+
+METRIC = "FAVOR+ attention tokens/s (B*H*n per s) and % of HBM/tensor roofline"
+DEFAULT_WORKLOAD = "noncausal_bf16_B1H8n1024d64m256"
+L2_BYTES = 126 * 1024 * 1024
+FLUSH_BYTES = 512 * 1024 * 1024
+
+# Nominal unit counts used where a kernel is bound by plain CUDA-core arithmetic:
+# 148 SMs x 128 fp32 FMA lanes x 2 flop x 2.032 GHz.
+FP32_SIMT_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
+
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the committed ncu
+# captures, valid only while the kernel sources hash to `src`.
+NCU_TRAFFIC: dict[str, dict] = {}
+
+
+def load_peaks() -> tuple[dict, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "kernelized_linear_attention_04_b300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+# ------------------------------------------------------------------------------------------------
+# Algorithmic work per kernel (per launch). Per token per head the whole path does
+# 8 m d flops (two projections, the state contraction and the readout contraction) and moves
+# 4 d s bytes (read Q, K, V, write Y; s = element size). Omega is counted once per launch.
+# ------------------------------------------------------------------------------------------------
+
+def kernel_work(w, kernel: str) -> tuple[float, float]:
+    """(algorithmic flops, algorithmic HBM bytes) of one launch of `kernel` on workload w."""
+    T, s, md = w.tokens, w.elem_bytes, w.m * w.d
+    om = w.m * w.d * s
+    if kernel == "state":        # project K, accumulate S and z; reads K, V
+        return 4.0 * md * T, 2.0 * w.d * s * T + om
+    if kernel == "readout":      # project Q, contract with S, divide; reads Q, writes Y
+        return 4.0 * md * T, 2.0 * w.d * s * T + om
+    if kernel == "causal":       # the whole causal path in one kernel
+        return 8.0 * md * T, 4.0 * w.d * s * T + om
+    if kernel == "combine":      # partial states -> one state per head
+        return 0.0, 0.0
+    if kernel.startswith("features"):
+        return 2.0 * md * T, (w.d * s + w.m * 4) * T + om
+    return 0.0, 0.0
+
+
+def path_work(w) -> tuple[float, float]:
+    return 8.0 * w.m * w.d * w.tokens, 4.0 * w.d * w.elem_bytes * w.tokens + w.m * w.d * w.elem_bytes
+
+
+# ------------------------------------------------------------------------------------------------
+# Clock sampling (NVML) during the timed region
+# ------------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    REASONS = {
+        "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
+        "hw_power_brake_slowdown": 0x80, "sw_power_cap": 0x4,
+    }
+
+    def __init__(self, device_index: int, period_s: float = 0.01):
+        self.samples: list[tuple[int, int]] = []
+        self.max_mhz = None
+        self.period = period_s
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            import pynvml
+
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self.max_mhz = int(pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM))
+        except Exception as e:  # pragma: no cover - reported in the JSON line
+            self.nv = None
+            self.err = str(e)
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                mhz = int(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
+                rs = int(self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h))
+                self.samples.append((mhz, rs))
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.nv is not None:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join()
+
+    def summary(self) -> dict:
+        if self.nv is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "error": getattr(self, "err", "")}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
+        mhz = statistics.median(s[0] for s in self.samples)
+        reasons = sorted({name for _, rs in self.samples for name, bit in self.REASONS.items() if rs & bit})
+        return {"sm_mhz": mhz, "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------------------------------------------
+# Distributed plumbing (replicas; barrier + max over ranks only)
+# ------------------------------------------------------------------------------------------------
+
+def dist_setup(backend: str):
+    import torch.distributed as dist
+
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    rank = dist.get_rank() if dist.is_initialized() else 0
+    return rank, ws
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float, device) -> float:
+    import torch
+    import torch.distributed as dist
+
+    if not dist.is_initialized():
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle timing (the cpu_baseline object, and the whole --impl reference arm)
+# ------------------------------------------------------------------------------------------------
+
+def oracle_sample_heads(w, budget_s: float) -> list[tuple[int, int]]:
+    """Heads for one oracle timing sample: as many as fit `budget_s` at a rough 1 GFLOP/s/core."""
+    import oracle
+
+    cores = oracle.get_threads()
+    per_head_flops = 10.0 * w.m * w.d * w.n  # includes the key pre-pass for the head stabiliser
+    k = int(max(1, min(w.heads, budget_s * cores * 1e9 / per_head_flops)))
+    k = max(1, (k // cores) * cores) if k >= cores else k
+    return [(i // w.H, i % w.H) for i in range(min(k, w.heads))]
+
+
+def oracle_inputs(w, heads):
+    import oracle  # noqa: F401
+
+    Q, K, V = [], [], []
+    for b, h in heads:
+        hi = si.head_inputs(w, b, h)
+        Q.append(si.to_f64(hi["Q"]))
+        K.append(si.to_f64(hi["K"]))
+        V.append(si.to_f64(hi["V"]))
+    return np.stack(Q), np.stack(K), np.stack(V), si.omega_for(w)[1]
+
+
+def oracle_step(w, inputs):
+    import oracle
+
+    Q, K, V, om = inputs
+    fn = oracle.attn_causal if w.causal else oracle.attn_noncausal
+    return fn(Q, K, V, om, kind=w.kind, relu_eps=w.relu_eps)
+
+
+def cpu_baseline(w, target_s: float = 12.0) -> dict:
+    import oracle
+
+    heads = oracle_sample_heads(w, budget_s=min(4.0, target_s / 3))
+    inputs = oracle_inputs(w, heads)
+    oracle_step(w, inputs)  # load / first-touch
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle_step(w, inputs)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= target_s or reps >= 1000:
+            break
+    tokens = reps * len(heads) * w.n
+    return {"value": tokens / el, "unit": "tokens/s", "cores": oracle.get_threads(), "kind": "oracle",
+            "sample": f"{len(heads)} of {w.heads} heads (all {w.n} tokens each) x {reps} repetitions, "
+                      f"{el:.1f} s wall, fp64 C loops, OpenMP over heads"}
+
+
+def run_reference(args, w):
+    rank, ws = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return 0
+    import oracle
+
+    heads = oracle_sample_heads(w, budget_s=0.5)
+    inputs = oracle_inputs(w, heads)
+    for _ in range(args.warmup):
+        oracle_step(w, inputs)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(w, inputs)
+        times.append(time.perf_counter() - t0)
+    tok = len(heads) * w.n
+    value = tok * len(times) / sum(times)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.get_threads(), "kind": "oracle",
+                         "sample": f"{len(heads)} of {w.heads} heads (all {w.n} tokens each) per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(w, l2_note: str | None = None) -> dict:
+    c = {"workload": w.name, "form": "causal" if w.causal else "non-causal", "features": w.kind,
+         "B": w.B, "H": w.H, "n": w.n, "d": w.d, "m": w.m, "inputs": f"iid N(0, {w.sigma}^2)"}
+    if w.causal:
+        c["chunk"] = w.chunk
+    if l2_note:
+        c["l2"] = l2_note
+    return c
+
+
+# ------------------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------------------
+
+def run_ours(args, w):
+    import torch
+
+    rank, world = dist_setup("nccl")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import kernelized_linear_attention_04_b300 as favor
+
+    dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    full = si.full_inputs(w)
+    om_store, _ = si.omega_for(w)
+
+    def pinned(a):
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if a.dtype == np.uint16 else torch.from_numpy(a)
+        return t.pin_memory()
+
+    hQ, hK, hV, hOm = pinned(full["Q"]), pinned(full["K"]), pinned(full["V"]), pinned(om_store)
+    del full
+    Q, K, V, Om = (t.to(dev) for t in (hQ, hK, hV, hOm))
+    Y = torch.empty_like(Q)
+    hY = torch.empty(Y.shape, dtype=dt).pin_memory()
+    op = "causal" if w.causal else "noncausal"
+    wsb = favor.workspace_bytes(op, w.B, w.H, w.n, w.d, w.m, dt, kind=w.kind, chunk=w.chunk if w.causal else 0)
+    wsp = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        if w.causal:
+            favor.favor_attn_causal(Q, K, V, Om, chunk=w.chunk, kind=w.kind, relu_eps=w.relu_eps, out=Y,
+                                    workspace=wsp, stream=stream)
+        else:
+            favor.favor_attn_noncausal(Q, K, V, Om, kind=w.kind, relu_eps=w.relu_eps, out=Y, workspace=wsp,
+                                       stream=stream)
+
+    step_bytes = path_work(w)[1]
+    flush = step_bytes < 2 * L2_BYTES
+    fbuf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
+    l2_note = "flushed before every timed step (512 MB write)" if flush else "inputs larger than L2"
+
+    def timed_loop(n_steps, body):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_steps)]
+        for a, b in evs:
+            if fbuf is not None:
+                fbuf.zero_()
+            a.record(stream)
+            body()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    assert favor.last_device_error() == 0
+
+    # -- device-resident throughput ---------------------------------------------------------
+    sampler = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    with sampler:
+        ms = timed_loop(args.steps, call)
+    barrier()
+    torch.cuda.synchronize()
+    ms_per_step = max_over_ranks(sum(ms) / len(ms), dev)
+    value = world * w.tokens / (ms_per_step * 1e-3)
+
+    # -- per-kernel durations (same loop, launches bracketed by events inside the library) -----
+    favor.trace_enable(True)
+    timed_loop(args.steps, call)
+    tr = favor.trace_read()
+    favor.trace_enable(False)
+    launched = {k: v for k, v in tr.items() if v[0] > 0}
+    launches_per_step = sum(v[0] for v in launched.values()) / args.steps
+    dom = max(launched, key=lambda k: launched[k][1])
+    dom_ms = launched[dom][1] / launched[dom][0]
+    flops, nbytes = kernel_work(w, dom)
+    peaks, peak_kind = load_peaks()
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    simt = w.dtype == "f32" or not getattr(favor, "TENSOR_CORE_PATH", False)
+    if simt:
+        t_cmp, cmp_unit, cmp_peak, cmp_bound = flops / (FP32_SIMT_PEAK_TFLOPS * 1e12), "TFLOP/s", FP32_SIMT_PEAK_TFLOPS, "alu"
+        cmp_note = "nominal fp32 FFMA: 148 SMs x 128 lanes x 2 flop x 2.032 GHz"
+    else:
+        t_cmp, cmp_unit, cmp_peak, cmp_bound = flops / (peaks["bf16_tflops"] * 1e12), "TFLOP/s", peaks["bf16_tflops"], "tensor"
+        cmp_note = f"bf16 dense, {peak_kind} burst"
+    if t_hbm >= t_cmp:
+        ach, peak, unit, bound, note = nbytes / (dom_ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s", "hbm", f"HBM copy, {peak_kind}"
+    else:
+        ach, peak, unit, bound, note = flops / (dom_ms * 1e-3) / 1e12, cmp_peak, cmp_unit, cmp_bound, cmp_note
+    src = kernel_source_hash()
+    tr_entry = NCU_TRAFFIC.get(f"{w.name}:{dom}")
+    traffic = tr_entry["bytes"] if tr_entry and tr_entry.get("src") == src else None
+    roofline = {"bound": bound, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
+                "traffic": traffic, "kernel": dom, "kernel_ms": dom_ms, "peak_source": note,
+                "algorithmic_flops": flops, "algorithmic_bytes": nbytes,
+                "kernels_ms": {k: v[1] / v[0] for k, v in launched.items()}}
+    # whole-path roofline fraction (the slower of flops at the tensor peak and bytes at HBM)
+    pf, pb = path_work(w)
+    t_roof = max(pf / (peaks["bf16_tflops"] * 1e12), pb / (peaks["hbm_gbs"] * 1e9))
+
+    # -- end to end through the public API with host buffers ----------------------------------
+    def e2e_body():
+        Q.copy_(hQ, non_blocking=True)
+        K.copy_(hK, non_blocking=True)
+        V.copy_(hV, non_blocking=True)
+        Om.copy_(hOm, non_blocking=True)
+        call()
+        hY.copy_(Y, non_blocking=True)
+
+    for _ in range(2):
+        e2e_body()
+    barrier()
+    torch.cuda.synchronize()
+    ms_e2e = timed_loop(args.steps, e2e_body)
+    barrier()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(sum(ms_e2e) / len(ms_e2e), dev)
+    h2d = sum(t.numel() * t.element_size() for t in (hQ, hK, hV, hOm))
+    d2h = hY.numel() * hY.element_size()
+    assert favor.last_device_error() == 0
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": workload_config(w, l2_note),
+            "path_roofline_frac": (t_roof * 1e3) / ms_per_step,
+            "roofline": roofline,
+            "e2e": {"value": world * w.tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": int(round(launches_per_step * args.steps)),
+            "clocks": sampler.summary(),
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w)
+        print(json.dumps(line))
+    import torch.distributed as dist
+
+    if dist.is_initialized():
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=si.workloads.WORKLOAD_ORDER)
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the host-core oracle timing")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus > 1 and ws != args.gpus:
+        ap.error("--gpus N > 1 runs under torchrun with N processes")
+    w = si.get_workload(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,148 @@
+/*
+ * favor.h — C ABI of libfavor.so: FAVOR+ (Performer) attention forward pass on one B300 (sm_103a).
+ *
+ * What is computed (sources are the pages' titles and sections):
+ *   x^ = d^(-1/4) x for every query and key row ("Performer" paper note, *Standard Attention Cost*:
+ *   the 1/sqrt(d) of softmax(QK^T/sqrt(d)), split evenly between q and k);
+ *   positive random features ("Performer" paper note, *FAVOR+*)
+ *       phi_r(x) = exp(w_r^T x^ - |x^|^2/2 - stab) / sqrt(m),     r = 1..m, w_r = row r of Omega,
+ *   or the generalized-ReLU family ("Performer for vision", *What Is Performer?*, Key Feature 4)
+ *       phi_r(x) = max(0, w_r^T x^) / sqrt(m) + relu_eps;
+ *   the state S = Phi(K)^T V (m x d) and normaliser z = Phi(K)^T 1 ("Performer" paper note,
+ *   *Kernel Attention View* and *Normalization*);
+ *   y_i = phi(q_i)^T S / phi(q_i)^T z, with sums over all keys (non-causal) or over keys j <= i
+ *   (causal: prefix sums, "Performer for vision", *How It Works*, Step 2).
+ * No n x n matrix is formed on the attention path.
+ *
+ * Conventions for every entry point:
+ *   - Q, K, V, X and Y are contiguous row-major [B, H, n, d] device arrays of the dtype `dt`; Omega is a
+ *     contiguous row-major [m, d] device array of the same dtype, shared by queries, keys and all heads.
+ *     Callers pass RAW q and k: the d^(-1/4) scaling is applied inside.
+ *   - All device pointers must be 16-byte aligned; workspace must be 256-byte aligned.
+ *   - Supported shapes: d in {64, 128}; m a multiple of 64 with 64 <= m <= 512; n >= 0; B, H >= 0.
+ *     B*H*n == 0 is a valid empty call that returns FAVOR_OK and touches no memory.
+ *   - Arithmetic: fp32 inputs are computed in fp32 on CUDA cores; bf16 inputs run on the tensor
+ *     cores with fp32 accumulation (features rounded to bf16 between the two contractions).
+ *   - Ownership: the caller owns every buffer. The library allocates no device memory; it keeps only
+ *     small host-side caches. `workspace` is scratch owned by the caller for the duration of the
+ *     call (size from favor_workspace_bytes; it may be NULL when that size is 0).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream). Every call is
+ *     asynchronous on that stream. Argument errors are reported by the return value before anything
+ *     is launched; launch failures return FAVOR_ERR_CUDA; device-side failures (a bounded wait that
+ *     ran out) are recorded in a device error word read by favor_last_device_error.
+ *   - Calls are deterministic: the same inputs give bit-identical outputs.
+ *   - Thread safety: calls from several host threads are safe; tracing state is global.
+ */
+#ifndef FAVOR_H
+#define FAVOR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FAVOR_ABI_VERSION 1
+
+typedef enum {
+    FAVOR_OK = 0,
+    FAVOR_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad enum value                    */
+    FAVOR_ERR_UNSUPPORTED = 2,  /* d, m or chunk outside the supported set                        */
+    FAVOR_ERR_MISALIGNED = 3,   /* a pointer is not 16-byte aligned (workspace: 256-byte)          */
+    FAVOR_ERR_WORKSPACE = 4,    /* ws_bytes smaller than favor_workspace_bytes(...)                */
+    FAVOR_ERR_CUDA = 5,         /* a CUDA runtime/driver call or kernel launch failed              */
+    FAVOR_ERR_TIMEOUT = 6       /* a device-side bounded wait gave up (reported after the fact)    */
+} favor_status_t;
+
+typedef enum { FAVOR_F32 = 0, FAVOR_BF16 = 1 } favor_dtype_t;
+typedef enum { FAVOR_EXP = 0, FAVOR_RELU = 1 } favor_kind_t;
+
+/* Stabiliser of favor_features (exp family only; ignored for ReLU):
+ *   NONE: stab = 0;  ROW: per token, stab = max_r u_r(x);  HEAD: per (b, h), stab = max over the
+ *   head's tokens j and features r of u_r(x_j), with u_r(x) = w_r^T x^ - |x^|^2/2.
+ * With ROW/HEAD the largest feature of a row/head is exactly 1/sqrt(m) (up to rounding). */
+typedef enum { FAVOR_STAB_NONE = 0, FAVOR_STAB_ROW = 1, FAVOR_STAB_HEAD = 2 } favor_stab_t;
+
+typedef enum { FAVOR_OP_FEATURES = 0, FAVOR_OP_NONCAUSAL = 1, FAVOR_OP_CAUSAL = 2 } favor_op_t;
+
+/* Bytes of workspace the given call needs (0 if none). Same arguments as the call itself; `stab`
+ * and `chunk` are read only for the ops that take them. Returns (size_t)-1 for unsupported shapes. */
+size_t favor_workspace_bytes(favor_op_t op, int B, int H, int n, int d, int m, favor_dtype_t dt,
+                             favor_kind_t kind, favor_stab_t stab, int chunk);
+
+/*
+ * Feature map phi(X) ("Performer" paper note, *FAVOR+*; "Performer for vision", *Kernel Choices*).
+ *   X     [B, H, n, d] dtype dt (raw, unscaled), Omega [m, d] dtype dt;
+ *   Phi   [B, H, n, m] fp32 output;
+ *   stab  see favor_stab_t (exp family); relu_eps the additive floor of the ReLU family.
+ * Exists to check phi itself and for callers that compose their own contractions; the attention
+ * entry points never write phi to memory.
+ */
+favor_status_t favor_features(const void* X, const void* Omega, float* Phi, int B, int H, int n, int d, int m,
+                              favor_dtype_t dt, favor_kind_t kind, float relu_eps, favor_stab_t stab,
+                              void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Non-causal FAVOR+ attention ("Performer" paper note, *Normalization*, second equation;
+ * "Performer for vision", *How It Works*, Step 1):
+ *   S = Phi(K)^T V, z = Phi(K)^T 1 per (b, h); Y = Phi(Q) S / Phi(Q) z (row-wise divide).
+ *   Q, K, V, Y [B, H, n, d] dtype dt; Omega [m, d] dtype dt. Y may not alias Q, K or V.
+ * Stabilisers: queries use one constant per row, keys one constant per head (after rescaling of
+ * partial sums); both cancel in the ratio, so Y does not depend on them.
+ */
+favor_status_t favor_attn_noncausal(const void* Q, const void* K, const void* V, const void* Omega, void* Y,
+                                    int B, int H, int n, int d, int m, favor_dtype_t dt, favor_kind_t kind,
+                                    float relu_eps, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Causal FAVOR+ attention ("Performer for vision", *How It Works*, Step 2: prefix sums so that
+ * each token attends only to itself and earlier tokens; "Performer" paper note, *Normalization*):
+ *   y_i = phi(q_i)^T S_i / phi(q_i)^T z_i,  S_i = sum_{j<=i} phi(k_j) v_j^T,  z_i = sum_{j<=i} phi(k_j).
+ * Computed as a chunked scan: per chunk of `chunk` tokens, an intra-chunk lower-triangular block
+ * plus the carried prefix state. chunk: 0 (default, 64) or 64. Shapes and dtypes as above.
+ */
+favor_status_t favor_attn_causal(const void* Q, const void* K, const void* V, const void* Omega, void* Y,
+                                 int B, int H, int n, int d, int m, int chunk, favor_dtype_t dt,
+                                 favor_kind_t kind, float relu_eps, void* workspace, size_t ws_bytes,
+                                 void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* favor_status_string(favor_status_t status);
+
+/* Synchronises `stream`, then reads and clears the device error word of the current device.
+ * Returns FAVOR_OK, FAVOR_ERR_TIMEOUT (a bounded device wait gave up) or FAVOR_ERR_CUDA. */
+favor_status_t favor_last_device_error(void* stream);
+
+/* FAVOR_ABI_VERSION of the loaded library. */
+int favor_abi_version(void);
+
+/* ---- tracing: per-kernel device time, recorded with CUDA events around every launch ---------- */
+
+typedef enum {
+    FAVOR_KERNEL_FEATURES = 0,      /* feature map (favor_features)                          */
+    FAVOR_KERNEL_FEATURES_HEAD = 1, /* per-head stabiliser pass of favor_features            */
+    FAVOR_KERNEL_STATE = 2,         /* non-causal key-side state reduction (S, z partials)   */
+    FAVOR_KERNEL_COMBINE = 3,       /* non-causal combine of the partial states              */
+    FAVOR_KERNEL_READOUT = 4,       /* non-causal query-side readout and divide              */
+    FAVOR_KERNEL_CAUSAL = 5,        /* causal chunked scan                                    */
+    FAVOR_KERNEL_COUNT = 6
+} favor_kernel_id_t;
+
+/* Starts (on != 0) or stops recording. Starting clears previous records. While recording, every
+ * launch is bracketed by two events on its stream, which adds a little host overhead. */
+favor_status_t favor_trace_enable(int on);
+
+/* Waits for the recorded events and writes, per favor_kernel_id_t, the number of launches and the
+ * summed device milliseconds (arrays of FAVOR_KERNEL_COUNT entries). Records stay until the next
+ * favor_trace_enable(1). */
+favor_status_t favor_trace_read(int* launches, double* total_ms);
+
+/* Name of a kernel id (static storage). */
+const char* favor_kernel_name(int kernel_id);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FAVOR_H */

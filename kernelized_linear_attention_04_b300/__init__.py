@@ -1,0 +1,194 @@
+"""FAVOR+ (Performer) attention forward pass on B300: thin Python binding over libfavor.so.
+
+Every step of the computation runs in the library's CUDA kernels; this module only marshals torch
+tensors (device memory, streams) into the C ABI declared in ``include/favor.h``. There is no CPU
+path: if the library cannot be loaded, importing this package raises.
+
+    import kernelized_linear_attention_04_b300 as favor
+    Y = favor.favor_attn_noncausal(Q, K, V, Omega)            # [B, H, n, d] bf16/fp32 CUDA tensors
+    Y = favor.favor_attn_causal(Q, K, V, Omega, chunk=64)
+    Phi = favor.favor_features(X, Omega, stab="head")
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "FavorError", "favor_features", "favor_attn_noncausal", "favor_attn_causal", "workspace_bytes",
+    "last_device_error", "trace_enable", "trace_read", "abi_version", "lib", "LIB_PATH",
+    "KERNEL_NAMES", "EXPORTED_SYMBOLS",
+]
+
+LIB_PATH = _build.LIB
+
+_DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+_KINDS = {"exp": 0, "relu": 1}
+_STABS = {"none": 0, "row": 1, "head": 2}
+_OPS = {"features": 0, "noncausal": 1, "causal": 2}
+_STATUS = {0: "FAVOR_OK", 1: "FAVOR_ERR_INVALID_ARG", 2: "FAVOR_ERR_UNSUPPORTED", 3: "FAVOR_ERR_MISALIGNED",
+           4: "FAVOR_ERR_WORKSPACE", 5: "FAVOR_ERR_CUDA", 6: "FAVOR_ERR_TIMEOUT"}
+KERNEL_COUNT = 6
+
+# Every function include/favor.h declares.
+EXPORTED_SYMBOLS = (
+    "favor_workspace_bytes", "favor_features", "favor_attn_noncausal", "favor_attn_causal",
+    "favor_status_string", "favor_last_device_error", "favor_abi_version", "favor_trace_enable",
+    "favor_trace_read", "favor_kernel_name",
+)
+
+
+class FavorError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = lib.favor_status_string(status).decode() if lib is not None else _STATUS.get(status, str(status))
+        super().__init__(f"{where}: {msg}")
+
+
+def _load() -> ctypes.CDLL:
+    path = _build.build() if _build.is_stale() else LIB_PATH  # fails loudly if it cannot build
+    L = ctypes.CDLL(path)
+    vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.favor_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, i32]
+    L.favor_workspace_bytes.restype = sz
+    L.favor_features.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp]
+    L.favor_features.restype = i32
+    L.favor_attn_noncausal.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, vp, sz, vp]
+    L.favor_attn_noncausal.restype = i32
+    L.favor_attn_causal.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, f32, vp, sz, vp]
+    L.favor_attn_causal.restype = i32
+    L.favor_status_string.argtypes = [i32]
+    L.favor_status_string.restype = ctypes.c_char_p
+    L.favor_last_device_error.argtypes = [vp]
+    L.favor_last_device_error.restype = i32
+    L.favor_abi_version.restype = i32
+    L.favor_trace_enable.argtypes = [i32]
+    L.favor_trace_enable.restype = i32
+    L.favor_trace_read.argtypes = [vp, vp]
+    L.favor_trace_read.restype = i32
+    L.favor_kernel_name.argtypes = [i32]
+    L.favor_kernel_name.restype = ctypes.c_char_p
+    return L
+
+
+lib: ctypes.CDLL = _load()
+KERNEL_NAMES = tuple(lib.favor_kernel_name(i).decode() for i in range(KERNEL_COUNT))
+
+
+def abi_version() -> int:
+    return int(lib.favor_abi_version())
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise FavorError(status, where)
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream))
+
+
+def _ptr(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _dims(X: torch.Tensor, name: str) -> tuple[int, int, int, int]:
+    if X.dim() != 4:
+        raise ValueError(f"{name} must be [B, H, n, d], got shape {tuple(X.shape)}")
+    if not X.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if X.dtype not in _DTYPES:
+        raise TypeError(f"{name} must be float32 or bfloat16, got {X.dtype}")
+    return tuple(int(s) for s in X.shape)  # type: ignore[return-value]
+
+
+def workspace_bytes(op: str, B: int, H: int, n: int, d: int, m: int, dtype: torch.dtype, *, kind: str = "exp",
+                    stab: str = "row", chunk: int = 0) -> int:
+    """Workspace bytes a call needs (raises FavorError(UNSUPPORTED) for shapes the library rejects)."""
+    v = lib.favor_workspace_bytes(_OPS[op], B, H, n, d, m, _DTYPES[dtype], _KINDS[kind], _STABS[stab], chunk)
+    if v == ctypes.c_size_t(-1).value:
+        raise FavorError(2, "favor_workspace_bytes")
+    return int(v)
+
+
+def _workspace(nbytes: int, like: torch.Tensor, workspace):
+    if nbytes == 0:
+        return workspace, 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=like.device)
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def favor_features(X: torch.Tensor, Omega: torch.Tensor, *, kind: str = "exp", relu_eps: float = 1e-3,
+                   stab: str = "row", out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    """phi(X) as fp32 [B, H, n, m] for raw X [B, H, n, d] and Omega [m, d] (same dtype)."""
+    B, H, n, d = _dims(X, "X")
+    m = int(Omega.shape[0])
+    if out is None:
+        out = torch.empty((B, H, n, m), dtype=torch.float32, device=X.device)
+    ws, wsb = _workspace(workspace_bytes("features", B, H, n, d, m, X.dtype, kind=kind, stab=stab), X, workspace)
+    _check(lib.favor_features(_ptr(X), _ptr(Omega), _ptr(out), B, H, n, d, m, _DTYPES[X.dtype], _KINDS[kind],
+                              relu_eps, _STABS[stab], _ptr(ws), wsb, _stream_handle(stream)), "favor_features")
+    return out
+
+
+def _attn_prep(Q, K, V, Omega, out):
+    B, H, n, d = _dims(Q, "Q")
+    if K.shape != Q.shape or V.shape != Q.shape:
+        raise ValueError("Q, K, V must have the same shape")
+    if not (Q.dtype == K.dtype == V.dtype == Omega.dtype):
+        raise TypeError("Q, K, V and Omega must share one dtype")
+    if Omega.dim() != 2 or Omega.shape[1] != d or not Omega.is_contiguous():
+        raise ValueError("Omega must be a contiguous [m, d] tensor")
+    if out is None:
+        out = torch.empty_like(Q)
+    return B, H, n, d, int(Omega.shape[0]), out
+
+
+def favor_attn_noncausal(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, Omega: torch.Tensor, *,
+                         kind: str = "exp", relu_eps: float = 1e-3, out: torch.Tensor | None = None,
+                         workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Y = Phi(Q)(Phi(K)^T V) / Phi(Q)(Phi(K)^T 1), all keys."""
+    B, H, n, d, m, out = _attn_prep(Q, K, V, Omega, out)
+    ws, wsb = _workspace(workspace_bytes("noncausal", B, H, n, d, m, Q.dtype, kind=kind), Q, workspace)
+    _check(lib.favor_attn_noncausal(_ptr(Q), _ptr(K), _ptr(V), _ptr(Omega), _ptr(out), B, H, n, d, m,
+                                    _DTYPES[Q.dtype], _KINDS[kind], relu_eps, _ptr(ws), wsb, _stream_handle(stream)),
+           "favor_attn_noncausal")
+    return out
+
+
+def favor_attn_causal(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, Omega: torch.Tensor, *, chunk: int = 64,
+                      kind: str = "exp", relu_eps: float = 1e-3, out: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Causal FAVOR+ attention (keys j <= i) as a chunked prefix-sum scan."""
+    B, H, n, d, m, out = _attn_prep(Q, K, V, Omega, out)
+    ws, wsb = _workspace(workspace_bytes("causal", B, H, n, d, m, Q.dtype, kind=kind, chunk=chunk), Q, workspace)
+    _check(lib.favor_attn_causal(_ptr(Q), _ptr(K), _ptr(V), _ptr(Omega), _ptr(out), B, H, n, d, m, chunk,
+                                 _DTYPES[Q.dtype], _KINDS[kind], relu_eps, _ptr(ws), wsb, _stream_handle(stream)),
+           "favor_attn_causal")
+    return out
+
+
+def last_device_error(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device error status (0 = none)."""
+    return int(lib.favor_last_device_error(_stream_handle(stream)))
+
+
+def trace_enable(on: bool = True) -> None:
+    _check(lib.favor_trace_enable(1 if on else 0), "favor_trace_enable")
+
+
+def trace_read() -> dict[str, tuple[int, float]]:
+    """{kernel name: (launches, total device ms)} of the launches recorded since trace_enable(True)."""
+    launches = (ctypes.c_int * KERNEL_COUNT)()
+    total = (ctypes.c_double * KERNEL_COUNT)()
+    _check(lib.favor_trace_read(ctypes.cast(launches, ctypes.c_void_p), ctypes.cast(total, ctypes.c_void_p)),
+           "favor_trace_read")
+    return {KERNEL_NAMES[i]: (int(launches[i]), float(total[i])) for i in range(KERNEL_COUNT)}

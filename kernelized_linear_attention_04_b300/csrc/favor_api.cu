@@ -1,0 +1,376 @@
+// C ABI of libfavor.so (declared in include/favor.h): argument checks, workspace layout, kernel
+// dispatch, launch tracing and the device error word. One translation unit holds every kernel.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/favor.h"
+#include "common.cuh"
+#include "simt_kernels.cuh"
+
+namespace favor {
+namespace {
+
+// ------------------------------------------------------------------------------------------------
+// Tracing: two events around every launch while enabled.
+// ------------------------------------------------------------------------------------------------
+struct TraceRec {
+    int kid;
+    cudaEvent_t a, b;
+};
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+std::vector<TraceRec> g_recs;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t pool_event() {
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+void release_records() {
+    for (auto& r : g_recs) {
+        g_event_pool.push_back(r.a);
+        g_event_pool.push_back(r.b);
+    }
+    g_recs.clear();
+}
+
+// Runs `launch` (which enqueues one kernel on `s`) and reports launch errors.
+template <class F>
+favor_status_t traced(int kid, cudaStream_t s, F&& launch) {
+    bool on;
+    {
+        std::lock_guard<std::mutex> g(g_trace_mu);
+        on = g_trace_on;
+    }
+    cudaEvent_t a = nullptr, b = nullptr;
+    if (on) {
+        std::lock_guard<std::mutex> g(g_trace_mu);
+        a = pool_event();
+        b = pool_event();
+        if (a) cudaEventRecord(a, s);
+    }
+    launch();
+    cudaError_t err = cudaGetLastError();
+    if (on && a && b) {
+        cudaEventRecord(b, s);
+        std::lock_guard<std::mutex> g(g_trace_mu);
+        g_recs.push_back({kid, a, b});
+    }
+    return err == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;
+}
+
+#define FAVOR_TRY(expr)                       \
+    do {                                      \
+        favor_status_t _st = (expr);          \
+        if (_st != FAVOR_OK) return _st;      \
+    } while (0)
+
+// ------------------------------------------------------------------------------------------------
+// Argument checks and workspace layout
+// ------------------------------------------------------------------------------------------------
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+favor_status_t check_shape(int B, int H, int n, int d, int m, favor_dtype_t dt, favor_kind_t kind) {
+    if (B < 0 || H < 0 || n < 0) return FAVOR_ERR_INVALID_ARG;
+    if (dt != FAVOR_F32 && dt != FAVOR_BF16) return FAVOR_ERR_INVALID_ARG;
+    if (kind != FAVOR_EXP && kind != FAVOR_RELU) return FAVOR_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FAVOR_ERR_UNSUPPORTED;
+    if (m < 64 || m > 512 || m % 64 != 0) return FAVOR_ERR_UNSUPPORTED;
+    return FAVOR_OK;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+constexpr int kMaxSplits = 64;
+
+// Token splits of the non-causal state pass: enough CTAs to fill the GPU about twice, at least
+// 64 tokens per split.
+int noncausal_splits(int B, int H, int n, int m) {
+    int64_t heads = (int64_t)B * H * (m / simt::kSlice);
+    int64_t want = (2 * 148 + heads - 1) / (heads > 0 ? heads : 1);
+    int64_t cap = (n + 63) / 64;
+    int64_t s = want < cap ? want : cap;
+    if (s < 1) s = 1;
+    if (s > kMaxSplits) s = kMaxSplits;
+    return (int)s;
+}
+
+struct NoncausalWs {
+    int splits;
+    size_t off_pS, off_pz, off_pst, off_S, off_z, total;
+};
+
+NoncausalWs noncausal_ws(int B, int H, int n, int d, int m) {
+    NoncausalWs w{};
+    const size_t BH = (size_t)B * H;
+    w.splits = noncausal_splits(B, H, n, m);
+    size_t o = 0;
+    w.off_pS = o; o = align_up(o + BH * w.splits * m * d * sizeof(float), 256);
+    w.off_pz = o; o = align_up(o + BH * w.splits * m * sizeof(float), 256);
+    w.off_pst = o; o = align_up(o + BH * w.splits * (m / simt::kSlice) * sizeof(float), 256);
+    w.off_S = o; o = align_up(o + BH * m * d * sizeof(float), 256);
+    w.off_z = o; o = align_up(o + BH * m * sizeof(float), 256);
+    w.total = o;
+    return w;
+}
+
+size_t causal_ws_bytes(int B, int H, int d, int m) {
+    const size_t BH = (size_t)B * H;
+    return align_up(BH * m * d * sizeof(float), 256) + align_up(BH * m * sizeof(float), 256);
+}
+
+size_t features_ws_bytes(int B, int H, favor_kind_t kind, favor_stab_t stab) {
+    if (kind != FAVOR_EXP || stab != FAVOR_STAB_HEAD) return 0;
+    return align_up((size_t)B * H * sizeof(unsigned), 256);
+}
+
+float qk_scale(int d) { return (float)std::pow((double)d, -0.25); }
+
+template <class Kern>
+favor_status_t set_smem(Kern k, size_t bytes) {
+    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) == cudaSuccess
+               ? FAVOR_OK
+               : FAVOR_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------------------------------------
+// SIMT launchers
+// ------------------------------------------------------------------------------------------------
+template <typename T, int D>
+favor_status_t simt_features(const void* X, const void* Om, float* Phi, int B, int H, int n, int m, int kind,
+                             float eps, int stab, void* ws, cudaStream_t s) {
+    using namespace simt;
+    const int BH = B * H;
+    unsigned* head_max = static_cast<unsigned*>(ws);
+    if (kind == kKindExp && stab == kStabHead) {
+        if (cudaMemsetAsync(head_max, 0, sizeof(unsigned) * BH, s) != cudaSuccess) return FAVOR_ERR_CUDA;
+    }
+    size_t smem = sizeof(float) * (kTok * D + kOmChunk * (D + 1) + kTok * m + kTok);
+    auto kern = features_kernel<T, D>;
+    FAVOR_TRY(set_smem(kern, smem));
+    dim3 grid((n + kTok - 1) / kTok, BH);
+    FAVOR_TRY(traced(FAVOR_KERNEL_FEATURES, s, [&] {
+        kern<<<grid, kThreads, smem, s>>>(static_cast<const T*>(X), static_cast<const T*>(Om), Phi, n, m, kind, eps,
+                                          stab, qk_scale(D), head_max);
+    }));
+    if (kind == kKindExp && stab == kStabHead) {
+        int64_t per_head = (int64_t)n * m;
+        int bx = (int)std::min<int64_t>((per_head + 255) / 256, 1024);
+        FAVOR_TRY(traced(FAVOR_KERNEL_FEATURES_HEAD, s, [&] {
+            features_head_apply_kernel<<<dim3(bx, BH), 256, 0, s>>>(Phi, per_head, m, head_max);
+        }));
+    }
+    return FAVOR_OK;
+}
+
+template <typename T, int D>
+favor_status_t simt_noncausal(const void* Q, const void* K, const void* V, const void* Om, void* Y, int B, int H,
+                              int n, int m, int kind, float eps, void* ws, cudaStream_t s) {
+    using namespace simt;
+    const int BH = B * H;
+    NoncausalWs w = noncausal_ws(B, H, n, D, m);
+    char* base = static_cast<char*>(ws);
+    float* pS = reinterpret_cast<float*>(base + w.off_pS);
+    float* pz = reinterpret_cast<float*>(base + w.off_pz);
+    float* pst = reinterpret_cast<float*>(base + w.off_pst);
+    float* S = reinterpret_cast<float*>(base + w.off_S);
+    float* z = reinterpret_cast<float*>(base + w.off_z);
+    int64_t tps = ((int64_t)n + w.splits - 1) / w.splits;
+    tps = (tps + kTok - 1) / kTok * kTok;
+    int splits = (int)((n + tps - 1) / tps);  // every split owns at least one token
+    const float sc = qk_scale(D);
+
+    size_t smem_state = sizeof(float) * (2 * kTok * D + kOmChunk * (D + 1) + kTok * kSlice + kTok + 8);
+    auto kstate = state_kernel<T, D>;
+    FAVOR_TRY(set_smem(kstate, smem_state));
+    FAVOR_TRY(traced(FAVOR_KERNEL_STATE, s, [&] {
+        kstate<<<dim3(splits, BH, m / kSlice), kThreads, smem_state, s>>>(
+            static_cast<const T*>(K), static_cast<const T*>(V), static_cast<const T*>(Om), n, m, kind, eps, sc, tps,
+            pS, pz, pst);
+    }));
+    FAVOR_TRY(traced(FAVOR_KERNEL_COMBINE, s, [&] {
+        combine_kernel<D><<<BH, kThreads, 0, s>>>(pS, pz, pst, splits, m, S, z);
+    }));
+    size_t smem_read = sizeof(float) * (kTok * D + kOmChunk * (D + 1) + kTok * m + 2 * kTok);
+    auto kread = readout_kernel<T, D>;
+    FAVOR_TRY(set_smem(kread, smem_read));
+    FAVOR_TRY(traced(FAVOR_KERNEL_READOUT, s, [&] {
+        kread<<<dim3((n + kTok - 1) / kTok, BH), kThreads, smem_read, s>>>(
+            static_cast<const T*>(Q), static_cast<const T*>(Om), S, z, static_cast<T*>(Y), n, m, kind, eps, sc);
+    }));
+    return FAVOR_OK;
+}
+
+template <typename T, int D>
+favor_status_t simt_causal(const void* Q, const void* K, const void* V, const void* Om, void* Y, int B, int H, int n,
+                           int m, int kind, float eps, void* ws, cudaStream_t s) {
+    using namespace simt;
+    const int BH = B * H;
+    float* Sg = static_cast<float*>(ws);
+    float* zg = reinterpret_cast<float*>(static_cast<char*>(ws) + align_up((size_t)BH * m * D * sizeof(float), 256));
+    size_t smem = sizeof(float) * (3 * kTok * D + 2 * kTok * m + kTok * kTok + 2 * kTok + kOmChunk * (D + 1) + 8);
+    auto kern = causal_kernel<T, D>;
+    FAVOR_TRY(set_smem(kern, smem));
+    FAVOR_TRY(traced(FAVOR_KERNEL_CAUSAL, s, [&] {
+        kern<<<BH, kThreads, smem, s>>>(static_cast<const T*>(Q), static_cast<const T*>(K), static_cast<const T*>(V),
+                                        static_cast<const T*>(Om), static_cast<T*>(Y), n, m, kind, eps, qk_scale(D), Sg,
+                                        zg);
+    }));
+    return FAVOR_OK;
+}
+
+// dtype x d dispatch
+#define FAVOR_DISPATCH(dt, d, FN, ...)                                                     \
+    ((dt) == FAVOR_F32 ? ((d) == 64 ? FN<float, 64>(__VA_ARGS__) : FN<float, 128>(__VA_ARGS__)) \
+                       : ((d) == 64 ? FN<__nv_bfloat16, 64>(__VA_ARGS__) : FN<__nv_bfloat16, 128>(__VA_ARGS__)))
+
+favor_status_t check_attn_args(const void* Q, const void* K, const void* V, const void* Om, const void* Y, int B,
+                               int H, int n, int d, int m, favor_dtype_t dt, favor_kind_t kind, float eps) {
+    FAVOR_TRY(check_shape(B, H, n, d, m, dt, kind));
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return FAVOR_ERR_INVALID_ARG;
+    if ((int64_t)B * H * n == 0) return FAVOR_OK;
+    if (!Q || !K || !V || !Om || !Y) return FAVOR_ERR_INVALID_ARG;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(Om, 16) || !aligned(Y, 16))
+        return FAVOR_ERR_MISALIGNED;
+    return FAVOR_OK;
+}
+
+favor_status_t check_ws(void* ws, size_t ws_bytes, size_t need) {
+    if (need == 0) return FAVOR_OK;
+    if (!ws) return FAVOR_ERR_INVALID_ARG;
+    if (!aligned(ws, 256)) return FAVOR_ERR_MISALIGNED;
+    if (ws_bytes < need) return FAVOR_ERR_WORKSPACE;
+    return FAVOR_OK;
+}
+
+}  // namespace
+}  // namespace favor
+
+using namespace favor;
+
+extern "C" {
+
+int favor_abi_version(void) { return FAVOR_ABI_VERSION; }
+
+const char* favor_status_string(favor_status_t st) {
+    switch (st) {
+        case FAVOR_OK: return "FAVOR_OK";
+        case FAVOR_ERR_INVALID_ARG: return "FAVOR_ERR_INVALID_ARG: null pointer, negative size or bad enum";
+        case FAVOR_ERR_UNSUPPORTED: return "FAVOR_ERR_UNSUPPORTED: d must be 64 or 128, m a multiple of 64 in [64, 512]";
+        case FAVOR_ERR_MISALIGNED: return "FAVOR_ERR_MISALIGNED: pointers need 16-byte (workspace 256-byte) alignment";
+        case FAVOR_ERR_WORKSPACE: return "FAVOR_ERR_WORKSPACE: workspace smaller than favor_workspace_bytes()";
+        case FAVOR_ERR_CUDA: return "FAVOR_ERR_CUDA: CUDA call or kernel launch failed";
+        case FAVOR_ERR_TIMEOUT: return "FAVOR_ERR_TIMEOUT: a device-side bounded wait gave up";
+    }
+    return "unknown favor_status_t";
+}
+
+const char* favor_kernel_name(int kid) {
+    switch (kid) {
+        case FAVOR_KERNEL_FEATURES: return "features";
+        case FAVOR_KERNEL_FEATURES_HEAD: return "features_head_stab";
+        case FAVOR_KERNEL_STATE: return "state";
+        case FAVOR_KERNEL_COMBINE: return "combine";
+        case FAVOR_KERNEL_READOUT: return "readout";
+        case FAVOR_KERNEL_CAUSAL: return "causal";
+    }
+    return "unknown";
+}
+
+size_t favor_workspace_bytes(favor_op_t op, int B, int H, int n, int d, int m, favor_dtype_t dt, favor_kind_t kind,
+                             favor_stab_t stab, int chunk) {
+    if (check_shape(B, H, n, d, m, dt, kind) != FAVOR_OK) return (size_t)-1;
+    if ((int64_t)B * H * n == 0) return 0;
+    switch (op) {
+        case FAVOR_OP_FEATURES: return features_ws_bytes(B, H, kind, stab);
+        case FAVOR_OP_NONCAUSAL: return noncausal_ws(B, H, n, d, m).total;
+        case FAVOR_OP_CAUSAL:
+            if (chunk != 0 && chunk != 64) return (size_t)-1;
+            return causal_ws_bytes(B, H, d, m);
+    }
+    return (size_t)-1;
+}
+
+favor_status_t favor_features(const void* X, const void* Omega, float* Phi, int B, int H, int n, int d, int m,
+                              favor_dtype_t dt, favor_kind_t kind, float relu_eps, favor_stab_t stab, void* workspace,
+                              size_t ws_bytes, void* stream) {
+    FAVOR_TRY(check_shape(B, H, n, d, m, dt, kind));
+    if (stab != FAVOR_STAB_NONE && stab != FAVOR_STAB_ROW && stab != FAVOR_STAB_HEAD) return FAVOR_ERR_INVALID_ARG;
+    if (!(relu_eps >= 0.f) || !std::isfinite(relu_eps)) return FAVOR_ERR_INVALID_ARG;
+    if ((int64_t)B * H * n == 0) return FAVOR_OK;
+    if (!X || !Omega || !Phi) return FAVOR_ERR_INVALID_ARG;
+    if (!aligned(X, 16) || !aligned(Omega, 16) || !aligned(Phi, 16)) return FAVOR_ERR_MISALIGNED;
+    FAVOR_TRY(check_ws(workspace, ws_bytes, features_ws_bytes(B, H, kind, stab)));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return FAVOR_DISPATCH(dt, d, simt_features, X, Omega, Phi, B, H, n, m, (int)kind, relu_eps, (int)stab, workspace,
+                          s);
+}
+
+favor_status_t favor_attn_noncausal(const void* Q, const void* K, const void* V, const void* Omega, void* Y, int B,
+                                    int H, int n, int d, int m, favor_dtype_t dt, favor_kind_t kind, float relu_eps,
+                                    void* workspace, size_t ws_bytes, void* stream) {
+    FAVOR_TRY(check_attn_args(Q, K, V, Omega, Y, B, H, n, d, m, dt, kind, relu_eps));
+    if ((int64_t)B * H * n == 0) return FAVOR_OK;
+    FAVOR_TRY(check_ws(workspace, ws_bytes, noncausal_ws(B, H, n, d, m).total));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return FAVOR_DISPATCH(dt, d, simt_noncausal, Q, K, V, Omega, Y, B, H, n, m, (int)kind, relu_eps, workspace, s);
+}
+
+favor_status_t favor_attn_causal(const void* Q, const void* K, const void* V, const void* Omega, void* Y, int B,
+                                 int H, int n, int d, int m, int chunk, favor_dtype_t dt, favor_kind_t kind,
+                                 float relu_eps, void* workspace, size_t ws_bytes, void* stream) {
+    FAVOR_TRY(check_attn_args(Q, K, V, Omega, Y, B, H, n, d, m, dt, kind, relu_eps));
+    if (chunk != 0 && chunk != 64) return FAVOR_ERR_UNSUPPORTED;
+    if ((int64_t)B * H * n == 0) return FAVOR_OK;
+    FAVOR_TRY(check_ws(workspace, ws_bytes, causal_ws_bytes(B, H, d, m)));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return FAVOR_DISPATCH(dt, d, simt_causal, Q, K, V, Omega, Y, B, H, n, m, (int)kind, relu_eps, workspace, s);
+}
+
+favor_status_t favor_last_device_error(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FAVOR_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_favor_error, sizeof(v)) != cudaSuccess) return FAVOR_ERR_CUDA;
+    if (v == 0) return FAVOR_OK;
+    unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_favor_error, &zero, sizeof(zero)) != cudaSuccess) return FAVOR_ERR_CUDA;
+    return FAVOR_ERR_TIMEOUT;
+}
+
+favor_status_t favor_trace_enable(int on) {
+    std::lock_guard<std::mutex> g(g_trace_mu);
+    if (on) release_records();
+    g_trace_on = on != 0;
+    return FAVOR_OK;
+}
+
+favor_status_t favor_trace_read(int* launches, double* total_ms) {
+    if (!launches || !total_ms) return FAVOR_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> g(g_trace_mu);
+    for (int k = 0; k < FAVOR_KERNEL_COUNT; ++k) {
+        launches[k] = 0;
+        total_ms[k] = 0.0;
+    }
+    for (auto& r : g_recs) {
+        if (cudaEventSynchronize(r.b) != cudaSuccess) return FAVOR_ERR_CUDA;
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) return FAVOR_ERR_CUDA;
+        launches[r.kid] += 1;
+        total_ms[r.kid] += ms;
+    }
+    return FAVOR_OK;
+}
+
+}  // extern "C"

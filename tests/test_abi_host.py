@@ -1,0 +1,110 @@
+"""The C-ABI library loads, exports what include/favor.h declares, and rejects bad arguments on the
+host before launching anything (CPU; no compute calls)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "favor.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(favor_[a-z_]+)\s*\(", text)))
+
+
+def test_library_loads_and_exports_every_declared_symbol():
+    import kernelized_linear_attention_04_b300 as favor
+
+    decl = declared_functions()
+    assert set(decl) == set(favor.EXPORTED_SYMBOLS), decl
+    out = subprocess.run(["nm", "-D", "--defined-only", favor.LIB_PATH], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (favor_\w+)", out))
+    for name in decl:
+        assert name in exported, name
+        assert hasattr(favor.lib, name)
+    assert favor.abi_version() == 1
+
+
+def test_status_strings_and_kernel_names():
+    import kernelized_linear_attention_04_b300 as favor
+
+    for code in range(7):
+        assert favor.lib.favor_status_string(code).decode().startswith("FAVOR_")
+    assert favor.KERNEL_NAMES[0] == "features"
+
+
+def test_workspace_sizes():
+    import kernelized_linear_attention_04_b300 as favor
+
+    bf = torch.bfloat16
+    assert favor.workspace_bytes("features", 1, 8, 1024, 64, 256, bf, stab="row") == 0
+    assert favor.workspace_bytes("features", 1, 8, 1024, 64, 256, bf, stab="head") >= 8 * 4
+    assert favor.workspace_bytes("noncausal", 1, 8, 0, 64, 256, bf) == 0
+    nc = favor.workspace_bytes("noncausal", 1, 8, 1024, 64, 256, bf)
+    assert nc % 256 == 0 and nc >= 8 * (256 * 64 + 256) * 4
+    with pytest.raises(favor.FavorError):
+        favor.workspace_bytes("noncausal", 1, 8, 1024, 96, 256, bf)
+    with pytest.raises(favor.FavorError):
+        favor.workspace_bytes("causal", 1, 8, 1024, 64, 256, bf, chunk=48)
+
+
+# Argument checks. Fake (never dereferenced) addresses are only passed where an earlier check
+# must fail; to keep even that off a real device these run only without a GPU.
+needs_no_gpu = pytest.mark.skipif(torch.cuda.is_available(), reason="host-only argument checks")
+
+
+@needs_no_gpu
+def test_argument_checks_reject_before_launch():
+    import kernelized_linear_attention_04_b300 as favor
+
+    L = favor.lib
+    P = ctypes.c_void_p(0x10000)      # aligned fake pointer
+    Mis = ctypes.c_void_p(0x10008)    # 8-byte aligned only
+    N = ctypes.c_void_p(0)
+    S = ctypes.c_void_p(0)
+    nc = L.favor_attn_noncausal
+    # null pointer
+    assert nc(P, N, P, P, P, 1, 1, 16, 64, 64, 1, 0, 0.0, P, 1 << 20, S) == 1
+    # unsupported d / m
+    assert nc(P, P, P, P, P, 1, 1, 16, 96, 64, 1, 0, 0.0, P, 1 << 20, S) == 2
+    assert nc(P, P, P, P, P, 1, 1, 16, 64, 100, 1, 0, 0.0, P, 1 << 20, S) == 2
+    assert nc(P, P, P, P, P, 1, 1, 16, 64, 1024, 1, 0, 0.0, P, 1 << 20, S) == 2
+    # bad enums / sizes / eps
+    assert nc(P, P, P, P, P, 1, 1, 16, 64, 64, 7, 0, 0.0, P, 1 << 20, S) == 1
+    assert nc(P, P, P, P, P, 1, 1, 16, 64, 64, 1, 5, 0.0, P, 1 << 20, S) == 1
+    assert nc(P, P, P, P, P, -1, 1, 16, 64, 64, 1, 0, 0.0, P, 1 << 20, S) == 1
+    assert nc(P, P, P, P, P, 1, 1, 16, 64, 64, 1, 1, -1.0, P, 1 << 20, S) == 1
+    # misaligned
+    assert nc(P, P, Mis, P, P, 1, 1, 16, 64, 64, 1, 0, 0.0, P, 1 << 20, S) == 3
+    assert nc(P, P, P, P, P, 1, 1, 16, 64, 64, 1, 0, 0.0, ctypes.c_void_p(0x10010), 1 << 20, S) == 3
+    # workspace too small / missing
+    assert nc(P, P, P, P, P, 1, 1, 16, 64, 64, 1, 0, 0.0, P, 16, S) == 4
+    assert nc(P, P, P, P, P, 1, 1, 16, 64, 64, 1, 0, 0.0, N, 1 << 20, S) == 1
+    # empty call is a no-op even with null pointers
+    assert nc(N, N, N, N, N, 1, 1, 0, 64, 64, 1, 0, 0.0, N, 0, S) == 0
+    assert nc(N, N, N, N, N, 0, 4, 16, 64, 64, 1, 0, 0.0, N, 0, S) == 0
+    ca = L.favor_attn_causal
+    assert ca(P, P, P, P, P, 1, 1, 16, 64, 64, 32, 1, 0, 0.0, P, 1 << 20, S) == 2
+    assert ca(N, N, N, N, N, 1, 1, 0, 64, 64, 64, 1, 0, 0.0, N, 0, S) == 0
+    ft = L.favor_features
+    assert ft(P, P, N, 1, 1, 16, 64, 64, 1, 0, 0.0, 1, N, 0, S) == 1
+    assert ft(P, P, P, 1, 1, 16, 64, 64, 1, 0, 0.0, 9, N, 0, S) == 1
+    assert ft(P, P, P, 1, 1, 16, 64, 64, 1, 0, 0.0, 2, N, 0, S) == 1       # head stab needs workspace
+
+
+def test_python_binding_validates_shapes():
+    import kernelized_linear_attention_04_b300 as favor
+
+    q = torch.zeros(1, 1, 4, 64)
+    with pytest.raises(ValueError):
+        favor.favor_attn_noncausal(q, q, q[:, :, :2], torch.zeros(64, 64))
+    with pytest.raises(TypeError):
+        favor.favor_attn_noncausal(q, q, q, torch.zeros(64, 64, dtype=torch.bfloat16))
+    with pytest.raises(ValueError):
+        favor.favor_attn_noncausal(q[0], q[0], q[0], torch.zeros(64, 64))
