@@ -10,8 +10,8 @@ linear-attention lesson's exercise with m = 256 random features, bf16 in / fp32 
 
 Timing: W untimed warm-up steps; K timed steps bracketed by a barrier and device synchronisation;
 each step timed by CUDA events on the launching stream; L2 flushed (a 512 MB write) before every
-timed step when the step's inputs are smaller than 2x L2; SM clocks sampled through NVML during the
-timed region. Multi-GPU (torchrun): every rank runs an independent replica of the workload (the
+timed step when the step's inputs are smaller than 2x L2; SM clocks and throttle reasons sampled with
+nvidia-smi from the warm-up through the timed region. Multi-GPU (torchrun): every rank runs an independent replica of the workload (the
 path has no exchange step), `value` is the tokens of all ranks over the slowest rank's time.
 
 --impl reference times the fp64 CPU oracle (the only reference implementation: the pages ship no
@@ -26,7 +26,6 @@ import math
 import os
 import statistics
 import sys
-import threading
 import time
 
 import numpy as np
@@ -95,61 +94,67 @@ def path_work(w) -> tuple[float, float]:
 
 
 # ------------------------------------------------------------------------------------------------
-# Clock sampling (NVML) during the timed region
+# Clock sampling (nvidia-smi) during the warm-up and timed region
 # ------------------------------------------------------------------------------------------------
 
 class ClockSampler:
-    REASONS = {
-        "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
-        "hw_power_brake_slowdown": 0x80, "sw_power_cap": 0x4,
-    }
+    """Samples SM clocks and throttle reasons with `nvidia-smi -lms` while the timed region runs."""
 
-    def __init__(self, device_index: int, period_s: float = 0.01):
-        self.samples: list[tuple[int, int]] = []
-        self.max_mhz = None
-        self.period = period_s
-        self._stop = threading.Event()
-        self._thread = None
-        try:
-            import pynvml
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    FLAGS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
-            self.max_mhz = int(pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM))
-        except Exception as e:  # pragma: no cover - reported in the JSON line
-            self.nv = None
-            self.err = str(e)
-
-    def _run(self):
-        while not self._stop.is_set():
-            try:
-                mhz = int(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
-                rs = int(self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h))
-                self.samples.append((mhz, rs))
-            except Exception:
-                pass
-            time.sleep(self.period)
+    def __init__(self, device_index: int, period_ms: int = 100):
+        self.index = device_index
+        self.period_ms = period_ms
+        self.proc = None
+        self.err = ""
+        self.out = None
 
     def __enter__(self):
-        if self.nv is not None:
-            self._thread = threading.Thread(target=self._run, daemon=True)
-            self._thread.start()
+        import subprocess
+        import tempfile
+
+        try:
+            self.out = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 f"-lms={self.period_ms}"], stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)  # let the first sample land before the timed region starts
+        except Exception as e:  # pragma: no cover - reported in the JSON line
+            self.proc, self.err = None, str(e)
         return self
 
     def __exit__(self, *a):
-        self._stop.set()
-        if self._thread is not None:
-            self._thread.join()
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
 
     def summary(self) -> dict:
-        if self.nv is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "error": getattr(self, "err", "")}
-        if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
-        mhz = statistics.median(s[0] for s in self.samples)
-        reasons = sorted({name for _, rs in self.samples for name, bit in self.REASONS.items() if rs & bit})
-        return {"sm_mhz": mhz, "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(self.samples)}
+        if self.proc is None or self.out is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "error": self.err}
+        self.out.seek(0)
+        mhz, maxes, reasons = [], [], set()
+        for line in self.out.read().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                maxes.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(self.FLAGS, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
+                "samples": len(mhz)}
 
 
 # ------------------------------------------------------------------------------------------------
@@ -334,19 +339,18 @@ def run_ours(args, w):
         torch.cuda.synchronize()
         return [a.elapsed_time(b) for a, b in evs]
 
-    for _ in range(args.warmup):
-        call()
-    torch.cuda.synchronize()
-    assert favor.last_device_error() == 0
-
-    # -- device-resident throughput ---------------------------------------------------------
+    # -- device-resident throughput (clocks sampled from the warm-up on, so the GPU is under load) --
     sampler = ClockSampler(local)
-    barrier()
-    torch.cuda.synchronize()
     with sampler:
+        for _ in range(args.warmup):
+            call()
+        torch.cuda.synchronize()
+        assert favor.last_device_error() == 0
+        barrier()
+        torch.cuda.synchronize()
         ms = timed_loop(args.steps, call)
-    barrier()
-    torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
     ms_per_step = max_over_ranks(sum(ms) / len(ms), dev)
     value = world * w.tokens / (ms_per_step * 1e-3)
 
