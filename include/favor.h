@@ -107,6 +107,31 @@ favor_status_t favor_attn_causal(const void* Q, const void* K, const void* V, co
                                  favor_kind_t kind, float relu_eps, void* workspace, size_t ws_bytes,
                                  void* stream);
 
+/*
+ * Non-causal attention for callers that cannot allocate device memory. There is no counterpart on
+ * the pages: this is a packaging variant of favor_attn_noncausal, for code that runs where
+ * cudaMalloc is unavailable or forbidden (a plugin inside a host application that owns every
+ * allocation, a real-time loop that must not block in the allocator, a context whose memory pool
+ * is fixed at start-up).
+ *
+ * It computes exactly what favor_attn_noncausal computes, with the same arguments minus the
+ * workspace. Its scratch (the per-split partial key states) lives in one fixed device array of
+ * FAVOR_NOALLOC_SCRATCH_BYTES compiled into the library, so every GPU that loads libfavor.so holds
+ * that array until the process exits. Shapes whose scratch need (favor_workspace_bytes for
+ * FAVOR_OP_NONCAUSAL) exceeds it are rejected with FAVOR_ERR_WORKSPACE before anything runs.
+ *
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress, with that
+ * device current) and caches it; make that first call outside any CUDA stream capture. The call
+ * allocates nothing and frees nothing. All calls share the one array: two calls that may overlap
+ * on the GPU (different streams, or several host threads) race on it and give undefined results,
+ * so serialise them. The array keeps the last call's contents; nothing in it needs to start at
+ * zero.
+ */
+#define FAVOR_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+favor_status_t favor_attn_noncausal_noalloc(const void* Q, const void* K, const void* V, const void* Omega,
+                                            void* Y, int B, int H, int n, int d, int m, favor_dtype_t dt,
+                                            favor_kind_t kind, float relu_eps, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* favor_status_string(favor_status_t status);
 

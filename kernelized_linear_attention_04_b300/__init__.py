@@ -19,7 +19,8 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "FavorError", "favor_features", "favor_attn_noncausal", "favor_attn_causal", "workspace_bytes",
+    "FavorError", "favor_features", "favor_attn_noncausal", "favor_attn_causal", "favor_attn_noncausal_noalloc",
+    "workspace_bytes", "NOALLOC_SCRATCH_BYTES",
     "last_device_error", "trace_enable", "trace_read", "abi_version", "lib", "LIB_PATH",
     "KERNEL_NAMES", "EXPORTED_SYMBOLS",
 ]
@@ -33,12 +34,14 @@ _OPS = {"features": 0, "noncausal": 1, "causal": 2}
 _STATUS = {0: "FAVOR_OK", 1: "FAVOR_ERR_INVALID_ARG", 2: "FAVOR_ERR_UNSUPPORTED", 3: "FAVOR_ERR_MISALIGNED",
            4: "FAVOR_ERR_WORKSPACE", 5: "FAVOR_ERR_CUDA", 6: "FAVOR_ERR_TIMEOUT"}
 KERNEL_COUNT = 6
+# Size of the library's fixed scratch array used by favor_attn_noncausal_noalloc.
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 # Every function include/favor.h declares.
 EXPORTED_SYMBOLS = (
     "favor_workspace_bytes", "favor_features", "favor_attn_noncausal", "favor_attn_causal",
     "favor_status_string", "favor_last_device_error", "favor_abi_version", "favor_trace_enable",
-    "favor_trace_read", "favor_kernel_name",
+    "favor_trace_read", "favor_kernel_name", "favor_attn_noncausal_noalloc",
 )
 
 
@@ -61,6 +64,8 @@ def _load() -> ctypes.CDLL:
     L.favor_attn_noncausal.restype = i32
     L.favor_attn_causal.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, f32, vp, sz, vp]
     L.favor_attn_causal.restype = i32
+    L.favor_attn_noncausal_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, vp]
+    L.favor_attn_noncausal_noalloc.restype = i32
     L.favor_status_string.argtypes = [i32]
     L.favor_status_string.restype = ctypes.c_char_p
     L.favor_last_device_error.argtypes = [vp]
@@ -173,6 +178,23 @@ def favor_attn_causal(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, Omega: 
     _check(lib.favor_attn_causal(_ptr(Q), _ptr(K), _ptr(V), _ptr(Omega), _ptr(out), B, H, n, d, m, chunk,
                                  _DTYPES[Q.dtype], _KINDS[kind], relu_eps, _ptr(ws), wsb, _stream_handle(stream)),
            "favor_attn_causal")
+    return out
+
+
+def favor_attn_noncausal_noalloc(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, Omega: torch.Tensor, *,
+                                 kind: str = "exp", relu_eps: float = 1e-3, out: torch.Tensor | None = None,
+                                 stream=None) -> torch.Tensor:
+    """Same result as favor_attn_noncausal, for callers that cannot allocate device scratch.
+
+    The library keeps the scratch in one fixed device array of NOALLOC_SCRATCH_BYTES, so this call
+    allocates nothing on the device (pass `out` to avoid even the output allocation here). Calls
+    share that array: do not let two of them overlap on the GPU. Make the first call on a device
+    outside stream capture (it looks up the array's address).
+    """
+    B, H, n, d, m, out = _attn_prep(Q, K, V, Omega, out)
+    _check(lib.favor_attn_noncausal_noalloc(_ptr(Q), _ptr(K), _ptr(V), _ptr(Omega), _ptr(out), B, H, n, d, m,
+                                            _DTYPES[Q.dtype], _KINDS[kind], relu_eps, _stream_handle(stream)),
+           "favor_attn_noncausal_noalloc")
     return out
 
 

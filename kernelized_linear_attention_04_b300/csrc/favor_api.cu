@@ -339,6 +339,54 @@ favor_status_t favor_attn_causal(const void* Q, const void* K, const void* V, co
     return FAVOR_DISPATCH(dt, d, simt_causal, Q, K, V, Omega, Y, B, H, n, m, (int)kind, relu_eps, workspace, s);
 }
 
+// ------------------------------------------------------------------------------------------------
+// favor_attn_noncausal_noalloc: the non-causal path with its scratch in a fixed device array.
+// ------------------------------------------------------------------------------------------------
+}  // extern "C"
+
+namespace favor {
+namespace {
+
+// In host code this name is only a host-side stand-in: kernels get the device address that
+// cudaGetSymbolAddress returns for the current device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FAVOR_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device, looked up once per device.
+favor_status_t noalloc_scratch(void** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FAVOR_ERR_CUDA;
+    std::lock_guard<std::mutex> g(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return FAVOR_ERR_CUDA;
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return FAVOR_OK;
+}
+
+}  // namespace
+}  // namespace favor
+
+extern "C" {
+
+favor_status_t favor_attn_noncausal_noalloc(const void* Q, const void* K, const void* V, const void* Omega, void* Y,
+                                            int B, int H, int n, int d, int m, favor_dtype_t dt, favor_kind_t kind,
+                                            float relu_eps, void* stream) {
+    FAVOR_TRY(check_attn_args(Q, K, V, Omega, Y, B, H, n, d, m, dt, kind, relu_eps));
+    if ((int64_t)B * H * n == 0) return FAVOR_OK;
+    const size_t need = favor_workspace_bytes(FAVOR_OP_NONCAUSAL, B, H, n, d, m, dt, kind, FAVOR_STAB_NONE, 0);
+    if (need > FAVOR_NOALLOC_SCRATCH_BYTES) return FAVOR_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    FAVOR_TRY(noalloc_scratch(&scratch));
+    return favor_attn_noncausal(Q, K, V, Omega, Y, B, H, n, d, m, dt, kind, relu_eps, scratch,
+                                FAVOR_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 favor_status_t favor_last_device_error(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FAVOR_ERR_CUDA;
     unsigned v = 0;
