@@ -2,6 +2,7 @@
 // dispatch, launch tracing and the device error word. One translation unit holds every kernel.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -11,6 +12,8 @@
 #include "../../include/favor.h"
 #include "common.cuh"
 #include "simt_kernels.cuh"
+#include "tc_noncausal.cuh"
+#include "tma_host.h"
 
 namespace favor {
 namespace {
@@ -126,6 +129,49 @@ NoncausalWs noncausal_ws(int B, int H, int n, int d, int m) {
     return w;
 }
 
+// ---- tensor-core non-causal path (bf16) ----------------------------------------------------------
+constexpr int kNumSMs = 148;
+
+int m_padded(int m) { return (m + 127) / 128 * 128; }
+
+// The tensor-core kernels take bf16 with d = 64 (m up to 512) or d = 128 (m up to 256); the
+// readout's shared memory holds Omega and the S image, which bounds m at d = 128.
+bool tc_noncausal_ok(int d, int m, favor_dtype_t dt) {
+    return dt == FAVOR_BF16 && (d == 64 || m_padded(m) <= 256);
+}
+
+struct TcNcWs {
+    int splits, tokens_per_split, chunks, tiles_per_cta, m_pad;
+    size_t off_pS, off_pz, off_pst, off_img, off_z, total;
+};
+
+// One CTA per SM (each holds all 512 TMEM columns): about one wave of (head, split) CTAs.
+TcNcWs tc_noncausal_ws(int B, int H, int n, int d, int m) {
+    TcNcWs w{};
+    const int64_t BH = (int64_t)B * H;
+    const int tiles = (n + tcnc::kTile - 1) / tcnc::kTile;
+    int64_t want = std::max<int64_t>(1, kNumSMs / std::max<int64_t>(BH, 1));
+    w.splits = (int)std::max<int64_t>(1, std::min<int64_t>(want, tiles));
+    const int tps = (tiles + w.splits - 1) / w.splits;
+    w.tokens_per_split = tps * tcnc::kTile;
+    w.splits = (tiles + tps - 1) / tps;  // every split owns at least one token
+    w.chunks = w.splits;
+    w.tiles_per_cta = tps;
+    w.m_pad = m_padded(m);
+    size_t o = 0;
+    w.off_pS = o; o = align_up(o + (size_t)BH * w.splits * w.m_pad * d * sizeof(float), 256);
+    w.off_pz = o; o = align_up(o + (size_t)BH * w.splits * w.m_pad * sizeof(float), 256);
+    w.off_pst = o; o = align_up(o + (size_t)BH * w.splits * sizeof(float), 256);
+    w.off_img = o; o = align_up(o + (size_t)BH * w.m_pad * d * 2, 256);
+    w.off_z = o; o = align_up(o + (size_t)BH * w.m_pad * sizeof(float), 256);
+    w.total = o;
+    return w;
+}
+
+size_t noncausal_ws_bytes(int B, int H, int n, int d, int m, favor_dtype_t dt) {
+    return tc_noncausal_ok(d, m, dt) ? tc_noncausal_ws(B, H, n, d, m).total : noncausal_ws(B, H, n, d, m).total;
+}
+
 size_t causal_ws_bytes(int B, int H, int d, int m) {
     const size_t BH = (size_t)B * H;
     return align_up(BH * m * d * sizeof(float), 256) + align_up(BH * m * sizeof(float), 256);
@@ -231,6 +277,48 @@ favor_status_t simt_causal(const void* Q, const void* K, const void* V, const vo
     return FAVOR_OK;
 }
 
+template <int D>
+favor_status_t tc_noncausal(const void* Q, const void* K, const void* V, const void* Om, void* Y, int B, int H, int n,
+                            int m, int kind, float eps, void* ws, cudaStream_t s) {
+    const int BH = B * H;
+    const TcNcWs w = tc_noncausal_ws(B, H, n, D, m);
+    char* base = static_cast<char*>(ws);
+    float* pS = reinterpret_cast<float*>(base + w.off_pS);
+    float* pz = reinterpret_cast<float*>(base + w.off_pz);
+    float* pst = reinterpret_cast<float*>(base + w.off_pst);
+    uint8_t* img = reinterpret_cast<uint8_t*>(base + w.off_img);
+    float* zf = reinterpret_cast<float*>(base + w.off_z);
+    CUtensorMap mK, mV, mQ, mY, mOm;
+    if (!tma::encode_bf16_3d(&mK, K, D, n, BH, 64, tcnc::kTile) || !tma::encode_bf16_3d(&mV, V, D, n, BH, 64, tcnc::kTile) ||
+        !tma::encode_bf16_3d(&mQ, Q, D, n, BH, 64, tcnc::kTile) || !tma::encode_bf16_3d(&mY, Y, D, n, BH, 64, tcnc::kTile) ||
+        !tma::encode_bf16_2d(&mOm, Om, D, m, 64, 128))
+        return FAVOR_ERR_CUDA;
+    const float sc = qk_scale(D);
+    const float eps_s = eps * std::sqrt((float)m);
+    const int groups = w.m_pad / 128;
+
+    tcnc::StateParams sp{n, w.m_pad, groups, w.tokens_per_split, kind, eps_s, sc, pS, pz, pst};
+    const size_t smem_state = tcnc::StateSmem<D>::bytes(groups);
+    auto kstate = tcnc::nc_state_tc<D>;
+    FAVOR_TRY(set_smem(kstate, smem_state));
+    FAVOR_TRY(traced(FAVOR_KERNEL_STATE, s, [&] {
+        kstate<<<dim3(w.splits, BH, 1), tcnc::kThreads, smem_state, s>>>(mK, mV, mOm, sp);
+    }));
+    const int rows_per_block = 128 / (D / 8);
+    FAVOR_TRY(traced(FAVOR_KERNEL_COMBINE, s, [&] {
+        tcnc::nc_combine<D><<<dim3(w.m_pad / rows_per_block, BH), 128, 0, s>>>(pS, pz, pst, w.splits, 1, m, w.m_pad,
+                                                                                w.m_pad, img, zf);
+    }));
+    tcnc::ReadoutParams rp{n, w.m_pad, m, w.tiles_per_cta, kind, eps_s, sc, img, zf};
+    const size_t smem_read = tcnc::ReadoutSmem<D>::bytes(w.m_pad);
+    auto kread = tcnc::nc_readout_tc<D>;
+    FAVOR_TRY(set_smem(kread, smem_read));
+    FAVOR_TRY(traced(FAVOR_KERNEL_READOUT, s, [&] {
+        kread<<<dim3(w.chunks, BH), tcnc::kThreads, smem_read, s>>>(mQ, mOm, mY, rp);
+    }));
+    return FAVOR_OK;
+}
+
 // dtype x d dispatch
 #define FAVOR_DISPATCH(dt, d, FN, ...)                                                     \
     ((dt) == FAVOR_F32 ? ((d) == 64 ? FN<float, 64>(__VA_ARGS__) : FN<float, 128>(__VA_ARGS__)) \
@@ -295,7 +383,7 @@ size_t favor_workspace_bytes(favor_op_t op, int B, int H, int n, int d, int m, f
     if ((int64_t)B * H * n == 0) return 0;
     switch (op) {
         case FAVOR_OP_FEATURES: return features_ws_bytes(B, H, kind, stab);
-        case FAVOR_OP_NONCAUSAL: return noncausal_ws(B, H, n, d, m).total;
+        case FAVOR_OP_NONCAUSAL: return noncausal_ws_bytes(B, H, n, d, m, dt);
         case FAVOR_OP_CAUSAL:
             if (chunk != 0 && chunk != 64) return (size_t)-1;
             return causal_ws_bytes(B, H, d, m);
@@ -323,8 +411,11 @@ favor_status_t favor_attn_noncausal(const void* Q, const void* K, const void* V,
                                     void* workspace, size_t ws_bytes, void* stream) {
     FAVOR_TRY(check_attn_args(Q, K, V, Omega, Y, B, H, n, d, m, dt, kind, relu_eps));
     if ((int64_t)B * H * n == 0) return FAVOR_OK;
-    FAVOR_TRY(check_ws(workspace, ws_bytes, noncausal_ws(B, H, n, d, m).total));
+    FAVOR_TRY(check_ws(workspace, ws_bytes, noncausal_ws_bytes(B, H, n, d, m, dt)));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (tc_noncausal_ok(d, m, dt))
+        return d == 64 ? tc_noncausal<64>(Q, K, V, Omega, Y, B, H, n, m, (int)kind, relu_eps, workspace, s)
+                       : tc_noncausal<128>(Q, K, V, Omega, Y, B, H, n, m, (int)kind, relu_eps, workspace, s);
     return FAVOR_DISPATCH(dt, d, simt_noncausal, Q, K, V, Omega, Y, B, H, n, m, (int)kind, relu_eps, workspace, s);
 }
 
