@@ -89,6 +89,15 @@ def kernel_work(w, kernel: str) -> tuple[float, float]:
     return 0.0, 0.0
 
 
+def tensor_core_path(w) -> bool:
+    """True when the library runs workload w on its tcgen05 kernels (bf16 non-causal with d = 64, or
+    d = 128 with m <= 256 after padding to a multiple of 128)."""
+    if w.dtype != "bf16" or w.causal:
+        return False
+    m_pad = -(-w.m // 128) * 128
+    return w.d == 64 or m_pad <= 256
+
+
 def path_work(w) -> tuple[float, float]:
     return 8.0 * w.m * w.d * w.tokens, 4.0 * w.d * w.elem_bytes * w.tokens + w.m * w.d * w.elem_bytes
 
@@ -366,7 +375,7 @@ def run_ours(args, w):
     flops, nbytes = kernel_work(w, dom)
     peaks, peak_kind = load_peaks()
     t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
-    simt = w.dtype == "f32" or not getattr(favor, "TENSOR_CORE_PATH", False)
+    simt = not tensor_core_path(w)
     if simt:
         t_cmp, cmp_unit, cmp_peak, cmp_bound = flops / (FP32_SIMT_PEAK_TFLOPS * 1e12), "TFLOP/s", FP32_SIMT_PEAK_TFLOPS, "alu"
         cmp_note = "nominal fp32 FFMA: 148 SMs x 128 lanes x 2 flop x 2.032 GHz"
@@ -440,6 +449,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=si.workloads.WORKLOAD_ORDER)
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the host-core oracle timing")
+    ap.add_argument("--n", type=int, default=None,
+                    help="override the sequence length (smaller cases for profiler captures; not a bench line)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -447,6 +458,8 @@ def main(argv=None):
     if args.gpus > 1 and ws != args.gpus:
         ap.error("--gpus N > 1 runs under torchrun with N processes")
     w = si.get_workload(args.workload)
+    if args.n is not None:
+        w = w.with_(n=args.n, name=f"{w.name}@n={args.n}")
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

@@ -288,10 +288,9 @@ favor_status_t tc_noncausal(const void* Q, const void* K, const void* V, const v
     float* pst = reinterpret_cast<float*>(base + w.off_pst);
     uint8_t* img = reinterpret_cast<uint8_t*>(base + w.off_img);
     float* zf = reinterpret_cast<float*>(base + w.off_z);
-    CUtensorMap mK, mV, mQ, mY, mOm;
+    CUtensorMap mK, mV, mQ, mOm;
     if (!tma::encode_bf16_3d(&mK, K, D, n, BH, 64, tcnc::kTile) || !tma::encode_bf16_3d(&mV, V, D, n, BH, 64, tcnc::kTile) ||
-        !tma::encode_bf16_3d(&mQ, Q, D, n, BH, 64, tcnc::kTile) || !tma::encode_bf16_3d(&mY, Y, D, n, BH, 64, tcnc::kTile) ||
-        !tma::encode_bf16_2d(&mOm, Om, D, m, 64, 128))
+        !tma::encode_bf16_3d(&mQ, Q, D, n, BH, 64, tcnc::kTile) || !tma::encode_bf16_2d(&mOm, Om, D, m, 64, 128))
         return FAVOR_ERR_CUDA;
     const float sc = qk_scale(D);
     const float eps_s = eps * std::sqrt((float)m);
@@ -302,19 +301,19 @@ favor_status_t tc_noncausal(const void* Q, const void* K, const void* V, const v
     auto kstate = tcnc::nc_state_tc<D>;
     FAVOR_TRY(set_smem(kstate, smem_state));
     FAVOR_TRY(traced(FAVOR_KERNEL_STATE, s, [&] {
-        kstate<<<dim3(w.splits, BH, 1), tcnc::kThreads, smem_state, s>>>(mK, mV, mOm, sp);
+        kstate<<<dim3(w.splits, BH, 1), tcnc::kStateThreads, smem_state, s>>>(mK, mV, mOm, sp);
     }));
     const int rows_per_block = 128 / (D / 8);
     FAVOR_TRY(traced(FAVOR_KERNEL_COMBINE, s, [&] {
         tcnc::nc_combine<D><<<dim3(w.m_pad / rows_per_block, BH), 128, 0, s>>>(pS, pz, pst, w.splits, 1, m, w.m_pad,
                                                                                 w.m_pad, img, zf);
     }));
-    tcnc::ReadoutParams rp{n, w.m_pad, m, w.tiles_per_cta, kind, eps_s, sc, img, zf};
+    tcnc::ReadoutParams rp{n, w.m_pad, m, w.tiles_per_cta, kind, eps_s, sc, img, zf, static_cast<__nv_bfloat16*>(Y)};
     const size_t smem_read = tcnc::ReadoutSmem<D>::bytes(w.m_pad);
     auto kread = tcnc::nc_readout_tc<D>;
     FAVOR_TRY(set_smem(kread, smem_read));
     FAVOR_TRY(traced(FAVOR_KERNEL_READOUT, s, [&] {
-        kread<<<dim3(w.chunks, BH), tcnc::kThreads, smem_read, s>>>(mQ, mOm, mY, rp);
+        kread<<<dim3(w.chunks, BH), tcnc::kThreads, smem_read, s>>>(mQ, mOm, rp);
     }));
     return FAVOR_OK;
 }

@@ -11,7 +11,7 @@
 //                 readout copies into shared memory unchanged.
 //   nc_readout_tc query side. Per 128-token tile: U = Q_tile Omega^T (tokens on the lanes),
 //                 phi(Q) in place with an exact per-row stabiliser, den = phi(Q) z on the CUDA
-//                 cores, num = phi(Q) S on the tensor cores, Y = num / den stored by TMA.
+//                 cores, num = phi(Q) S on the tensor cores, Y = num / den stored in whole sectors.
 //
 // Stabilisers. A query row may use any constant of its own and a head's keys any one constant:
 // both cancel between numerator and denominator. Queries use their exact row maximum. Keys use
@@ -29,8 +29,9 @@ namespace tcnc {
 using namespace favor::tc;
 
 constexpr int kTile = 128;            // tokens per tile (the MMA M or N extent)
-constexpr int kThreads = 192;         // warp 0: TMA, warp 1: MMA, warps 2-5: epilogue
-constexpr int kEpiThreads = 128;
+constexpr int kEpiWarps = 16;         // four column groups x four TMEM lane quarters
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kThreads = 64 + kEpiThreads;  // warp 0: TMA, warp 1: MMA, then the epilogue warps
 constexpr float kStabSlackLo = 12.f;  // after a (re)set, the key stabiliser sits this far below the bound
 constexpr float kStabSlackHi = 24.f;  // ... and is raised once a tile's bound exceeds it by this much
 
@@ -38,6 +39,21 @@ __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// TMEM column of the packed phi^T for state-MMA K step ks (16 tokens): each epilogue warp packs its
+// 64 tokens into the first 32 columns of its own 64-column range.
+__host__ __device__ constexpr uint32_t phi_col(int ks) { return 64u * (uint32_t)(ks / 4) + 8u * (uint32_t)(ks % 4); }
+
+// a0 += lo^2, a1 += hi^2 for the two bf16 values of w, with one packed fp32x2 FMA.
+__device__ __forceinline__ void sq_acc_bf16x2(uint32_t w, float& a0, float& a1) {
+    asm("{\n\t.reg .b64 x, acc;\n\t.reg .b32 lo, hi;\n\t"
+        "shl.b32 lo, %2, 16;\n\tand.b32 hi, %2, 0xffff0000;\n\t"
+        "mov.b64 x, {lo, hi};\n\tmov.b64 acc, {%0, %1};\n\t"
+        "fma.rn.f32x2 acc, x, x, acc;\n\t"
+        "mov.b64 {%0, %1}, acc;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "r"(w));
 }
 
 // Squared norm of row `row` of a [128 x D] bf16 tile stored as D/64 swizzled regions of 16 KB.
@@ -51,11 +67,7 @@ __device__ __forceinline__ float tile_row_sqnorm(const uint8_t* tile, int row) {
             uint4 v = *reinterpret_cast<const uint4*>(tile + a * 16384 + sw128_offset(row, c));
             uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xFFFF0000u);
-                s0 = fmaf(lo, lo, s0);
-                s1 = fmaf(hi, hi, s1);
-            }
+            for (int i = 0; i < 4; ++i) sq_acc_bf16x2(w[i], s0, s1);
         }
     }
     return s0 + s1;
@@ -79,30 +91,53 @@ struct StateParams {
 
 template <int D>
 struct StateSmem {
-    static constexpr int kStages = (D == 64) ? 4 : 2;
+    // K tile t is needed by the first projection of tile t and V tile t by the first state MMA of
+    // tile t, which comes three MMA groups later; a K tile is refilled after its tile's last
+    // projection, a V tile after its tile's last state MMA. The K ring is the deeper one so that
+    // a refill has about as many MMA groups of lead time as the V refill.
+    static constexpr int kKStages = (D == 64) ? 5 : 3;
+    static constexpr int kVStages = (D == 64) ? 5 : 2;
     static constexpr int kTileBytes = kTile * D * 2;  // one [128 x D] bf16 tile
     // Omega region: D/64 swizzled regions of (groups * 128) rows, each row 128 B.
     __host__ __device__ static size_t omega_bytes(int groups) { return (size_t)groups * 128 * D * 2; }
-    static size_t bytes(int groups) { return 1024 + omega_bytes(groups) + (size_t)kStages * 2 * kTileBytes + 1024; }
+    static size_t bytes(int groups) {
+        return 1024 + omega_bytes(groups) + (size_t)(kKStages + kVStages) * kTileBytes + 2 * 128 * 4 /*sC*/ + 64;
+    }
 };
 
+// Key-side kernel roles: warp 0 TMA (lane 0 K tiles, lane 1 V tiles), warp 1 MMA issue, warps 2-3
+// norms and the key stabiliser, warps 4.. two epilogue teams of 8 warps. A unit is one 128-token
+// tile for one 128-feature group; unit u = tile * groups + group sits in TMEM slot u % 2 and is
+// handled by team u % 2.
+constexpr int kStateUnitTok = 128;
+constexpr int kStateSlots = 2;
+constexpr int kStateTeamWarps = 8;
+constexpr int kStateEpiWarps = 2 * kStateTeamWarps;
+constexpr int kStateNormWarps = 2;
+constexpr int kStateEpiWarp0 = 2 + kStateNormWarps;
+constexpr int kStateThreads = 32 * (kStateEpiWarp0 + kStateEpiWarps);
+
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kStateThreads, 1)
     nc_state_tc(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
                 const __grid_constant__ CUtensorMap mOm, StateParams p) {
     using SM = StateSmem<D>;
-    constexpr int NS = SM::kStages;
+    constexpr int NK = SM::kKStages, NV = SM::kVStages;
     constexpr int kAtoms = D / 64;
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    extern __shared__ __align__(16) uint8_t smem_raw[];  // aligned to 1024 by hand below
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int G = p.groups;
     uint8_t* sOm = smem;                                   // kAtoms regions of G*128 rows
-    uint8_t* sStage = sOm + SM::omega_bytes(G);            // NS x {K tile, V tile}
-    float* sC = reinterpret_cast<float*>(sStage + (size_t)NS * 2 * SM::kTileBytes);  // [128] per-token constants
-    __shared__ uint64_t bar_full[NS], bar_empty[NS], bar_om, bar_ufull[2], bar_ufree[2], bar_phi[2];
+    uint8_t* sK = sOm + SM::omega_bytes(G);                // NK K tiles
+    uint8_t* sV = sK + (size_t)NK * SM::kTileBytes;        // NV V tiles
+    float* sC = reinterpret_cast<float*>(sV + (size_t)NV * SM::kTileBytes);  // [2][128] per-token constants
+    __shared__ uint64_t bar_kfull[NK], bar_kempty[NK], bar_vfull[NV], bar_vempty[NV], bar_om;
+    __shared__ uint64_t bar_ufull[kStateSlots], bar_ufree[kStateSlots], bar_phi[kStateSlots];
+    __shared__ uint64_t bar_nfull[2], bar_nempty[2];
+    __shared__ float sF[2];  // per-tile rescale factor of the accumulated state (1 = none)
+    __shared__ float sRed[2][kStateNormWarps];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
-    __shared__ float red[4];
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int split = blockIdx.x, splits = gridDim.x;
@@ -112,19 +147,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int j0 = split * p.tokens_per_split;
     const int j1 = min(p.n, j0 + p.tokens_per_split);
     const int T = (j1 - j0 + kTile - 1) / kTile;
-    const int U = T * G;  // units = (tile, group) pairs
+    const int UPT = G;        // units per tile
+    const int U = T * UPT;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        for (int i = 0; i < NS; ++i) {
-            mbar_init(&bar_full[i], 1);
-            mbar_init(&bar_empty[i], 1 + 4);  // MMA commit + one arrive per epilogue warp
+        for (int i = 0; i < NK; ++i) {
+            mbar_init(&bar_kfull[i], 1);
+            mbar_init(&bar_kempty[i], 1 + kStateNormWarps);  // MMA commit after the tile's last projection + norm warps
+        }
+        for (int i = 0; i < NV; ++i) {
+            mbar_init(&bar_vfull[i], 1);
+            mbar_init(&bar_vempty[i], 1);
         }
         mbar_init(&bar_om, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kStateSlots; ++i) {
             mbar_init(&bar_ufull[i], 1);
             mbar_init(&bar_ufree[i], 1);
-            mbar_init(&bar_phi[i], 4);
+            mbar_init(&bar_phi[i], kStateTeamWarps);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar_nfull[i], kStateNormWarps);
+            mbar_init(&bar_nempty[i], kStateEpiWarps);
         }
         fence_mbar_init();
     }
@@ -132,54 +176,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = tmem_base;
-    // TMEM: S_g at columns [g*D, (g+1)*D); U slots at 256 and 384.
+    // TMEM: S_g at columns [g*D, (g+1)*D); two 128-column U slots from column 256.
     auto u_col = [](int s) { return 256u + 128u * (uint32_t)s; };
 
     if (warp == 0) {
-        // ---------------- TMA producer ----------------
+        // ---------------- TMA producers: lane 0 streams K tiles, lane 1 V tiles ----------------
         if (lane == 0) {
             tma_prefetch_desc(&mK);
-            tma_prefetch_desc(&mV);
             tma_prefetch_desc(&mOm);
             mbar_arrive_expect_tx(&bar_om, (uint32_t)SM::omega_bytes(G));
             for (int g = 0; g < G; ++g)
                 for (int a = 0; a < kAtoms; ++a)
                     tma_load_2d(sOm + (size_t)a * G * 16384 + g * 16384, &mOm, &bar_om, a * 64, f0 + g * 128);
+        } else if (lane == 1) {
+            tma_prefetch_desc(&mV);
+        }
+        if (lane < 2) {
+            const int NR = lane == 0 ? NK : NV;
+            uint64_t* full = lane == 0 ? bar_kfull : bar_vfull;
+            uint64_t* empty = lane == 0 ? bar_kempty : bar_vempty;
+            uint8_t* ring = lane == 0 ? sK : sV;
+            const CUtensorMap* map = lane == 0 ? &mK : &mV;
             int issued = 0;
             for (int t = 0; t < T; ++t) {
-                const int st = t % NS;
-                if (!mbar_wait(&bar_empty[st], ((t / NS) & 1) ^ 1, &abort_flag)) break;
-                uint8_t* kt = sStage + (size_t)st * 2 * SM::kTileBytes;
-                uint8_t* vt = kt + SM::kTileBytes;
-                mbar_arrive_expect_tx(&bar_full[st], 2 * SM::kTileBytes);
-                for (int a = 0; a < kAtoms; ++a) {
-                    tma_load_3d(kt + a * 16384, &mK, &bar_full[st], a * 64, j0 + t * kTile, bh);
-                    tma_load_3d(vt + a * 16384, &mV, &bar_full[st], a * 64, j0 + t * kTile, bh);
-                }
+                const int st = t % NR;
+                if (!mbar_wait(&empty[st], ((t / NR) & 1) ^ 1, &abort_flag)) break;
+                mbar_arrive_expect_tx(&full[st], SM::kTileBytes);
+                for (int a = 0; a < kAtoms; ++a)
+                    tma_load_3d(ring + (size_t)st * SM::kTileBytes + a * 16384, map, &full[st], a * 64, j0 + t * kTile, bh);
                 issued = t + 1;
             }
             // Drain: every issued load must land before the CTA may exit.
-            for (int t = max(0, issued - NS); t < issued; ++t) {
+            for (int t = max(0, issued - NR); t < issued; ++t) {
                 volatile int never = 0;
-                mbar_wait(&bar_full[t % NS], (t / NS) & 1, &never);
+                mbar_wait(&full[t % NR], (t / NR) & 1, &never);
             }
-            volatile int never = 0;
-            mbar_wait(&bar_om, 0, &never);
+            if (lane == 0) {
+                volatile int never = 0;
+                mbar_wait(&bar_om, 0, &never);
+            }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
-            constexpr uint32_t idesc_p = idesc_bf16(128, 128, false, false);  // U^T = Om_g K^T
-            constexpr uint32_t idesc_s = idesc_bf16(128, D, false, true);     // S_g += phi^T V
+            constexpr uint32_t idesc_p = idesc_bf16(128, kStateUnitTok, false, false);  // U^T = Om_g K_half^T
+            constexpr uint32_t idesc_s = idesc_bf16(128, D, false, true);               // S_g += phi^T V_half
             bool ok = mbar_wait(&bar_om, 0, &abort_flag);
             tc_fence_after();
-            // Unit u = (tile u / G, group u % G) uses U slot u % 2.
+            // unit u: tile u / G, group u % G, slot u % 2
             auto issue_proj = [&](int u) -> bool {
-                const int t = u / G, g = u % G, s = u & 1, st = t % NS;
-                if (g == 0 && !mbar_wait(&bar_full[st], (t / NS) & 1, &abort_flag)) return false;
-                if (!mbar_wait(&bar_ufree[s], ((u >> 1) & 1) ^ 1, &abort_flag)) return false;
+                const int t = u / UPT, g = u % UPT, s = u % kStateSlots, st = t % NK;
+                if (u % UPT == 0 && !mbar_wait(&bar_kfull[st], (t / NK) & 1, &abort_flag)) return false;
+                if (!mbar_wait(&bar_ufree[s], ((u / kStateSlots) & 1) ^ 1, &abort_flag)) return false;
                 tc_fence_after();
-                const uint8_t* kt = sStage + (size_t)st * 2 * SM::kTileBytes;
+                const uint8_t* kt = sK + (size_t)st * SM::kTileBytes;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const int a = ks / 4, w = ks % 4;
@@ -188,22 +238,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_ss(tbase + u_col(s), ad, bd, idesc_p, ks > 0);
                 }
                 mma_commit(&bar_ufull[s]);
+                if (u % UPT == UPT - 1) mma_commit(&bar_kempty[st]);
                 return true;
             };
             auto issue_state = [&](int u) -> bool {
-                const int t = u / G, g = u % G, s = u & 1, st = t % NS;
-                if (!mbar_wait(&bar_phi[s], (u >> 1) & 1, &abort_flag)) return false;
+                const int t = u / UPT, g = u % UPT, s = u % kStateSlots, st = t % NV;
+                if (u % UPT == 0 && !mbar_wait(&bar_vfull[st], (t / NV) & 1, &abort_flag)) return false;
+                if (!mbar_wait(&bar_phi[s], (u / kStateSlots) & 1, &abort_flag)) return false;
                 tc_fence_after();
-                const uint8_t* vt = sStage + (size_t)st * 2 * SM::kTileBytes + SM::kTileBytes;
+                const uint8_t* vt = sV + (size_t)st * SM::kTileBytes;
 #pragma unroll
-                for (int ks = 0; ks < kTile / 16; ++ks) {
+                for (int ks = 0; ks < kStateUnitTok / 16; ++ks) {
                     uint64_t bd = sdesc_sw128(smem_u32(vt + ks * 2048), 16384, 1024);
-                    mma_ts(tbase + (uint32_t)(g * D), tbase + u_col(s) + ks * 8, bd, idesc_s, (t > 0 || ks > 0));
+                    mma_ts(tbase + (uint32_t)(g * D), tbase + u_col(s) + phi_col(ks), bd, idesc_s, (t > 0 || ks > 0));
                 }
                 mma_commit(&bar_ufree[s]);
-                if (g == G - 1) mma_commit(&bar_empty[st]);
+                if (u % UPT == UPT - 1) mma_commit(&bar_vempty[st]);
                 return true;
             };
+            // Order P(0), P(1), S(0), P(2), S(1), ...: the projection into a slot waits for the state
+            // MMA that last read it, which was issued one step earlier.
             if (ok) {
                 for (int u = 0; u < U; ++u) {
                     if (!issue_proj(u)) break;
@@ -212,159 +266,228 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!abort_flag && U > 0) issue_state(U - 1);
             }
         }
-    } else {
-        // ---------------- epilogue (warps 2-5) ----------------
-        const int q = warp & 3;
-        const int r = q * 32 + lane;  // TMEM lane = feature row within a group; also the token row for norms
-        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        const float A2 = p.scale * kLog2e;
-        float zacc[4] = {0.f, 0.f, 0.f, 0.f};
-        float stab = 0.f;
-        bool failed = !mbar_wait(&bar_om, 0, &abort_flag);
-        __syncwarp();
-        // W = largest row norm of this CTA's Omega rows (zero rows past m do not matter).
+    } else if (warp < kStateEpiWarp0) {
+        // ---------------- norms and the key stabiliser (two warps) ----------------
+        // Norm warp nw owns tokens [64 nw, 64 nw + 64) of every tile, two per lane. Per tile:
+        // sC[t & 1][j] = (|k^_j|^2 / 2 + stab) log2 e (+inf for tokens outside the split) and
+        // sF[t & 1] = the factor by which the state accumulated so far must be rescaled before this
+        // tile (1 when the stabiliser did not move). Both warps run the same stabiliser logic.
+        const int nw = warp - 2;
+        const int nt = 32 * kStateNormWarps;
+        bool ok = mbar_wait(&bar_om, 0, &abort_flag);
         float W = 0.f;
         if (p.kind == kKindExp) {
             float w2 = 0.f;
-            for (int g = 0; g < G; ++g) {
-                float s = 0.f;
-                for (int a = 0; a < kAtoms; ++a) s += tile_row_sqnorm<64>(sOm + (size_t)a * G * 16384 + g * 16384, r);
-                w2 = fmaxf(w2, s);
+            for (int row = nw * 32 + lane; row < G * 128; row += nt) {
+                const int g = row >> 7, rr = row & 127;
+                float s2 = 0.f;
+                for (int a = 0; a < kAtoms; ++a) s2 += tile_row_sqnorm<64>(sOm + (size_t)a * G * 16384 + g * 16384, rr);
+                w2 = fmaxf(w2, s2);
             }
             w2 = warp_max(w2);
-            if (lane == 0) red[q] = w2;
-            named_bar(1, kEpiThreads);
-            W = sqrtf(fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])));
-            named_bar(1, kEpiThreads);
+            if (lane == 0) sRed[1][nw] = w2;
+            named_bar(2, nt);
+            float m2 = 0.f;
+#pragma unroll
+            for (int i = 0; i < kStateNormWarps; ++i) m2 = fmaxf(m2, sRed[1][i]);
+            W = sqrtf(m2);
         }
-        // On a failed wait the loop keeps running (the waits then return at once) so that every
-        // epilogue thread passes the same named barriers; only the results are garbage.
+        float stab = 0.f;
         for (int t = 0; t < T; ++t) {
-            const int st = t % NS;
-            failed |= !mbar_wait(&bar_full[st], (t / NS) & 1, &abort_flag);
+            const int st = t % NK, b2 = t & 1;
+            ok &= mbar_wait(&bar_nempty[b2], ((t >> 1) & 1) ^ 1, &abort_flag);
+            ok &= mbar_wait(&bar_kfull[st], (t / NK) & 1, &abort_flag);
             __syncwarp();
-            const uint8_t* kt = sStage + (size_t)st * 2 * SM::kTileBytes;
-            const int j = j0 + t * kTile + r;
-            const bool valid = j < j1;
-            float cj = INFINITY;
+            const uint8_t* kt = sK + (size_t)st * SM::kTileBytes;
+            float h2[2], bmax = -INFINITY;
+            bool v2[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int tok = nw * 64 + lane + 32 * i;
+                v2[i] = j0 + t * kTile + tok < j1;
+                const float xn2 = p.kind == kKindExp ? p.scale * p.scale * tile_row_sqnorm<D>(kt, tok) : 0.f;
+                h2[i] = 0.5f * xn2;
+                if (v2[i]) bmax = fmaxf(bmax, W * sqrtf(xn2) - h2[i]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_kempty[st]);
+            float f = 1.f;
             if (p.kind == kKindExp) {
-                const float xn2 = p.scale * p.scale * tile_row_sqnorm<D>(kt, r);  // |k^|^2
-                const float h = 0.5f * xn2;
-                const float b = valid ? W * sqrtf(xn2) - h : -INFINITY;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar_empty[st]);
-                const float bm = warp_max(b);
-                if (lane == 0) red[q] = bm;
-                named_bar(1, kEpiThreads);
-                const float Bt = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-                named_bar(1, kEpiThreads);
+                const float wm = warp_max(bmax);
+                if (lane == 0) sRed[b2][nw] = wm;
+                named_bar(2, nt);
+                float Bt = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < kStateNormWarps; ++i) Bt = fmaxf(Bt, sRed[b2][i]);
                 if (t == 0) {
                     stab = Bt - kStabSlackLo;
                 } else if (Bt > stab + kStabSlackHi) {
-                    // Raise the stabiliser: wait for every state MMA issued so far, rescale S and z.
                     const float nst = Bt - kStabSlackLo;
-                    const float f = ex2((stab - nst) * kLog2e);
-                    const int ul = t * G - 1;  // last unit of the previous tile
-                    failed |= !mbar_wait(&bar_ufree[ul & 1], (ul >> 1) & 1, &abort_flag);
-                    __syncwarp();
-                    tc_fence_after();
-                    for (int g = 0; g < G; ++g) {
-#pragma unroll
-                        for (int c0 = 0; c0 < D; c0 += 32) {
-                            uint32_t v[32];
-                            tmem_ld32(tbase + lane_off + g * D + c0, v);
-                            tmem_ld_wait();
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
-                            tmem_st32(tbase + lane_off + g * D + c0, v);
-                        }
-                        zacc[g] *= f;
-                    }
-                    tmem_st_wait();
+                    f = ex2((stab - nst) * kLog2e);
                     stab = nst;
                 }
-                cj = valid ? (h + stab) * kLog2e : INFINITY;
-            } else {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar_empty[st]);
-                cj = valid ? 0.f : INFINITY;
-                named_bar(1, kEpiThreads);  // previous tile's readers of sC are done
             }
-            sC[r] = cj;
-            named_bar(1, kEpiThreads);
-            for (int g = 0; g < G; ++g) {
-                const int u = t * G + g, s = u & 1;
-                failed |= !mbar_wait(&bar_ufull[s], (u >> 1) & 1, &abort_flag);
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+                sC[b2 * 128 + nw * 64 + lane + 32 * i] =
+                    v2[i] ? (p.kind == kKindExp ? (h2[i] + stab) * kLog2e : 0.f) : INFINITY;
+            if (nw == 0 && lane == 0) sF[b2] = f;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_nfull[b2]);
+        }
+        if (nw == 0 && lane == 0)
+            p.pstab[((size_t)bh * splits + split) * fslices + fslice] = (p.kind == kKindExp && ok) ? stab : 0.f;
+    } else {
+        // ---------------- epilogue: two teams of 8 warps ----------------
+        // Team tm handles the units u = tm (mod 2). Within a team, warp (cg, q) reads TMEM lane
+        // quarter q = warp % 4 (a hardware rule) and the 32 tokens [32 cg, 32 cg + 32) of the unit.
+        const int ew = warp - kStateEpiWarp0;
+        const int tm = ew / kStateTeamWarps, cg = (ew % kStateTeamWarps) >> 2, q = warp & 3;
+        const int r = q * 32 + lane;  // feature lane within a group
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        const float A2 = p.scale * kLog2e;
+        float zacc[4] = {0.f, 0.f, 0.f, 0.f};
+        bool failed = false;
+        for (int t = 0; t < T; ++t) {
+            const int b2 = t & 1;
+            failed |= !mbar_wait(&bar_nfull[b2], (t >> 1) & 1, &abort_flag);
+            __syncwarp();
+            const float f = sF[b2];
+            if (f != 1.f) {
+                // The key stabiliser moved: once every state MMA so far has completed, scale S and z.
+                const int ul = t * UPT - 1;
+                failed |= !mbar_wait(&bar_ufree[ul % kStateSlots], (ul / kStateSlots) & 1, &abort_flag);
                 __syncwarp();
                 tc_fence_after();
-                const uint32_t ua = tbase + lane_off + u_col(s);
-                float z = zacc[g];
+                const int part = tm * 2 + cg;  // this warp's quarter of the S columns
 #pragma unroll
-                for (int c = 0; c < kTile / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(ua + 32 * c, v);
-                    tmem_ld_wait();
+                for (int g = 0; g < 4; ++g) {
+                    if (g >= G) break;
+                    constexpr int kC = D / 4;
+                    const uint32_t sa = tbase + lane_off + g * D + part * kC;
+                    if constexpr (kC == 32) {
+                        uint32_t v[32];
+                        tmem_ld32(sa, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
+                        tmem_st32(sa, v);
+                    } else {
+                        uint32_t v[16];
+                        tmem_ld16(sa, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
+                        tmem_st16(sa, v);
+                    }
+                    zacc[g] *= f;
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                named_bar(1, 32 * kStateEpiWarps);  // both teams' parts are rescaled before any phi of tile t
+            }
+            const float* cj = sC + b2 * 128 + 64 * cg;
+            for (int g = 0; g < G; ++g) {
+                const int u = t * UPT + g;
+                if ((u & 1) != tm) continue;
+                const int s = u % kStateSlots;
+                failed |= !mbar_wait(&bar_ufull[s], (u / kStateSlots) & 1, &abort_flag);
+                __syncwarp();
+                tc_fence_after();
+                const uint32_t ua = tbase + lane_off + u_col(s) + 64 * cg;
+                uint32_t v[64];
+                tmem_ld32(ua, *reinterpret_cast<uint32_t(*)[32]>(v));
+                tmem_ld32(ua + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+                tmem_ld_wait();
+                float zs0 = 0.f, zs1 = 0.f;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
                     float ph[32];
+                    const uint32_t* vv = v + 32 * hh;
+                    const float* cc = cj + 32 * hh;
                     if (p.kind == kKindExp) {
 #pragma unroll
                         for (int i = 0; i < 32; i += 4) {
-                            const float4 c4 = *reinterpret_cast<const float4*>(sC + 32 * c + i);
-                            ph[i + 0] = ex2(fmaf(__uint_as_float(v[i + 0]), A2, -c4.x));
-                            ph[i + 1] = ex2(fmaf(__uint_as_float(v[i + 1]), A2, -c4.y));
-                            ph[i + 2] = ex2(fmaf(__uint_as_float(v[i + 2]), A2, -c4.z));
-                            ph[i + 3] = ex2(fmaf(__uint_as_float(v[i + 3]), A2, -c4.w));
+                            const float4 c4 = *reinterpret_cast<const float4*>(cc + i);
+                            ph[i + 0] = ex2(fmaf(__uint_as_float(vv[i + 0]), A2, -c4.x));
+                            ph[i + 1] = ex2(fmaf(__uint_as_float(vv[i + 1]), A2, -c4.y));
+                            ph[i + 2] = ex2(fmaf(__uint_as_float(vv[i + 2]), A2, -c4.z));
+                            ph[i + 3] = ex2(fmaf(__uint_as_float(vv[i + 3]), A2, -c4.w));
                         }
                     } else {
 #pragma unroll
                         for (int i = 0; i < 32; i += 4) {
-                            const float4 c4 = *reinterpret_cast<const float4*>(sC + 32 * c + i);
-                            ph[i + 0] = c4.x == 0.f ? fmaxf(__uint_as_float(v[i + 0]) * p.scale, 0.f) + p.relu_eps_s : 0.f;
-                            ph[i + 1] = c4.y == 0.f ? fmaxf(__uint_as_float(v[i + 1]) * p.scale, 0.f) + p.relu_eps_s : 0.f;
-                            ph[i + 2] = c4.z == 0.f ? fmaxf(__uint_as_float(v[i + 2]) * p.scale, 0.f) + p.relu_eps_s : 0.f;
-                            ph[i + 3] = c4.w == 0.f ? fmaxf(__uint_as_float(v[i + 3]) * p.scale, 0.f) + p.relu_eps_s : 0.f;
+                            const float4 c4 = *reinterpret_cast<const float4*>(cc + i);
+                            ph[i + 0] = c4.x == 0.f ? fmaxf(__uint_as_float(vv[i + 0]) * p.scale, 0.f) + p.relu_eps_s : 0.f;
+                            ph[i + 1] = c4.y == 0.f ? fmaxf(__uint_as_float(vv[i + 1]) * p.scale, 0.f) + p.relu_eps_s : 0.f;
+                            ph[i + 2] = c4.z == 0.f ? fmaxf(__uint_as_float(vv[i + 2]) * p.scale, 0.f) + p.relu_eps_s : 0.f;
+                            ph[i + 3] = c4.w == 0.f ? fmaxf(__uint_as_float(vv[i + 3]) * p.scale, 0.f) + p.relu_eps_s : 0.f;
                         }
                     }
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const uint32_t w = pack_bf16(ph[2 * i], ph[2 * i + 1]);
-                        pk[i] = w;
-                        // z sums the bf16-rounded features the MMA sees.
-                        z += __uint_as_float(w << 16) + __uint_as_float(w & 0xFFFF0000u);
+                        pk[i] = pack_bf16(ph[2 * i], ph[2 * i + 1]);
+                        zs0 += ph[2 * i];
+                        zs1 += ph[2 * i + 1];
                     }
-                    tmem_st16(ua + 16 * c, pk);
+                    // Packed phi goes to the first 32 columns of this warp's own 64: no other warp reads them.
+                    tmem_st16(ua + 16 * hh, pk);
                 }
-                zacc[g] = z;
+                if (g == 0) zacc[0] += zs0 + zs1;
+                else if (g == 1) zacc[1] += zs0 + zs1;
+                else if (g == 2) zacc[2] += zs0 + zs1;
+                else zacc[3] += zs0 + zs1;
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar_phi[s]);
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_nempty[b2]);
         }
-        // Final state: wait for the last state MMA, then write this CTA's partial S, z and stabiliser.
-        if (__all_sync(0xffffffffu, !failed) && U > 0) {
-            const int ul = U - 1;
-            const bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_ufree[ul & 1], (ul >> 1) & 1, &abort_flag));
-            if (ok) {
-                tc_fence_after();
-                const size_t part = (size_t)bh * splits + split;
-                for (int g = 0; g < G; ++g) {
-                    const int feat = f0 + g * 128 + r;
-                    float* out = p.pS + (part * p.m_pad + feat) * D;
+        // Final state: wait for the last state MMA, then write this CTA's partial S and z.
+        const int ul = U - 1;
+        const bool done =
+            __all_sync(0xffffffffu, U > 0 && mbar_wait(&bar_ufree[ul % kStateSlots], (ul / kStateSlots) & 1, &abort_flag));
+        tc_fence_after();
+        const size_t part_idx = (size_t)bh * splits + split;
+        // z partials of the two teams and two column groups meet in shared memory (the V ring is idle now).
+        float* sZ = reinterpret_cast<float*>(sV);
+        const int zpart = tm * 2 + cg;
 #pragma unroll
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        uint32_t v[32];
-                        tmem_ld32(tbase + lane_off + g * D + c0, v);
-                        tmem_ld_wait();
+        for (int g = 0; g < 4; ++g)
+            if (g < G) sZ[(zpart * 4 + g) * 128 + r] = zacc[g];
+        named_bar(1, 32 * kStateEpiWarps);
+        if (__all_sync(0xffffffffu, done && !failed)) {
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            *reinterpret_cast<float4*>(out + c0 + i) =
-                                make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]), __uint_as_float(v[i + 2]),
-                                            __uint_as_float(v[i + 3]));
-                    }
-                    p.pz[part * p.m_pad + feat] = zacc[g];
+            for (int g = 0; g < 4; ++g) {
+                if (g >= G) break;
+                const int feat = f0 + g * 128 + r;
+                constexpr int kC = D / 4;
+                float* out = p.pS + (part_idx * p.m_pad + feat) * D + zpart * kC;
+                const uint32_t sa = tbase + lane_off + g * D + zpart * kC;
+                if constexpr (kC == 32) {
+                    uint32_t v[32];
+                    tmem_ld32(sa, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4*>(out + i) = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                                                          __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+                } else {
+                    uint32_t v[16];
+                    tmem_ld16(sa, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; i += 4)
+                        *reinterpret_cast<float4*>(out + i) = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                                                          __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
                 }
-                if (threadIdx.x == 64) p.pstab[part * fslices + fslice] = p.kind == kKindExp ? stab : 0.f;
+                if (zpart == 0)
+                    p.pz[part_idx * p.m_pad + feat] =
+                        ((sZ[(0 * 4 + g) * 128 + r] + sZ[(1 * 4 + g) * 128 + r]) + sZ[(2 * 4 + g) * 128 + r]) +
+                        sZ[(3 * 4 + g) * 128 + r];
             }
         }
     }
@@ -439,6 +562,7 @@ struct ReadoutParams {
     float scale;
     const uint8_t* Simg;  // [BH][m_pad * D * 2] from nc_combine
     const float* z;       // [BH][m_pad]
+    __nv_bfloat16* Y;     // [BH][n][D] output
 };
 
 template <int D>
@@ -447,25 +571,25 @@ struct ReadoutSmem {
     static constexpr int kTileBytes = kTile * D * 2;
     static size_t bytes(int m_pad) {
         return 1024 + (size_t)m_pad * D * 2 /*Omega*/ + (size_t)m_pad * D * 2 /*S image*/ + (size_t)m_pad * 4 /*z*/ +
-               (size_t)kStages * kTileBytes + kTileBytes /*Y staging*/;
+               (size_t)kStages * kTileBytes + 2 * 2 * 4 * 128 * 4 /*max, den partials*/;
     }
 };
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    nc_readout_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mOm,
-                  const __grid_constant__ CUtensorMap mY, ReadoutParams p) {
+    nc_readout_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mOm, ReadoutParams p) {
     using SM = ReadoutSmem<D>;
     constexpr int NS = SM::kStages;
     constexpr int kAtoms = D / 64;
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    extern __shared__ __align__(16) uint8_t smem_raw[];  // aligned to 1024 by hand below
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int MP = p.m_pad;
     uint8_t* sOm = smem;                                   // kAtoms regions of MP rows x 128 B
     uint8_t* sS = sOm + (size_t)MP * D * 2;                // S image: kAtoms regions of MP rows x 128 B
     uint8_t* sQ = sS + (size_t)MP * D * 2;                 // NS stages
-    uint8_t* sY = sQ + (size_t)NS * SM::kTileBytes;        // Y staging tile
-    float* sz = reinterpret_cast<float*>(sY + SM::kTileBytes);  // [MP]
+    float* sz = reinterpret_cast<float*>(sQ + (size_t)NS * SM::kTileBytes);  // [MP]
+    float* sMax = sz + MP;                                 // [2][4][128] row-max partials
+    float* sDen = sMax + 2 * 4 * 128;                      // [2][4][128] denominator partials
     __shared__ uint64_t bar_full[NS], bar_empty[NS], bar_const, bar_ufull[2], bar_ufree[2], bar_phi[2], bar_num[2];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
@@ -475,9 +599,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tiles_head = (p.n + kTile - 1) / kTile;
     const int t0 = blockIdx.x * p.tiles_per_cta;
     const int T = max(0, min(tiles_head, t0 + p.tiles_per_cta) - t0);
-    const int nslot = MP <= 256 ? 2 : 1;
-    const uint32_t slot_cols = MP <= 256 ? 256u : 512u;
-    const uint32_t num_off = MP <= 256 ? 128u : 256u;
+    // Two TMEM slots of 256 columns when m_pad <= 256, else one slot of 512.
+    const bool two = MP <= 256;
+    const int nslot = two ? 2 : 1;
+    const uint32_t slot_cols = two ? 256u : 512u;
+    const int Wf = MP / 4;  // features per column group of epilogue warps
+    // Packed phi: compact [0, MP/2) when m_pad <= 256 (all U values are in registers before any
+    // warp overwrites U); otherwise each warp packs into the first half of its own column range.
+    auto phi_col_r = [&](int ks) -> uint32_t {
+        if (two) return (uint32_t)ks * 8u;
+        const int f = ks * 16;
+        return (uint32_t)((f / Wf) * Wf + (f % Wf) / 2);
+    };
+    const uint32_t num_off = two ? 128u : (MP < 512 ? (uint32_t)MP : 64u);
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -488,8 +622,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bar_const, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar_ufull[i], 1);
-            mbar_init(&bar_ufree[i], 4);
-            mbar_init(&bar_phi[i], 4);
+            mbar_init(&bar_ufree[i], kEpiWarps);
+            mbar_init(&bar_phi[i], kEpiWarps);
             mbar_init(&bar_num[i], 1);
         }
         fence_mbar_init();
@@ -503,7 +637,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             tma_prefetch_desc(&mQ);
             tma_prefetch_desc(&mOm);
-            tma_prefetch_desc(&mY);
             const uint32_t sbytes = (uint32_t)MP * D * 2;
             mbar_arrive_expect_tx(&bar_const, sbytes * 2 + (uint32_t)MP * 4);
             for (int a = 0; a < kAtoms; ++a)
@@ -530,8 +663,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            const int nN = MP <= 256 ? 1 : 2;    // N blocks of the projection
-            const int Nb = MP <= 256 ? MP : MP / 2;
+            const int nN = two ? 1 : 2;    // N blocks of the projection
+            const int Nb = two ? MP : MP / 2;
             const uint32_t idesc_p = idesc_bf16(128, Nb, false, false);
             constexpr uint32_t idesc_o = idesc_bf16(128, D, false, true);
             bool ok = mbar_wait(&bar_const, 0, &abort_flag);
@@ -563,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 for (int ks = 0; ks < MP / 16; ++ks) {
                     uint64_t bd = sdesc_sw128(smem_u32(sS + ks * 2048), (uint32_t)MP * 128, 1024);
-                    mma_ts(tbase + s * slot_cols + num_off, tbase + s * slot_cols + ks * 8, bd, idesc_o, ks > 0);
+                    mma_ts(tbase + s * slot_cols + num_off, tbase + s * slot_cols + phi_col_r(ks), bd, idesc_o, ks > 0);
                 }
                 mma_commit(&bar_num[s]);
                 return true;
@@ -583,14 +716,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------- epilogue ----------------
-        const int q = warp & 3;
+        // Warp ew reads TMEM lane quarter q = warp % 4 (tokens 32q..32q+31 of the tile) and column
+        // group cg = ew / 4: features [cg Wf, (cg+1) Wf) in the first pass, output columns
+        // [cg D/4, (cg+1) D/4) in the second.
+        const int ew = warp - 2;
+        const int q = warp & 3, cg = ew >> 2;
         const int r = q * 32 + lane;  // token row of the tile
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         const float A2 = p.scale * kLog2e;
-        const bool is_issuer = (warp == 2 && lane == 0);
-        float den[2] = {0.f, 0.f};
+        const bool exp_kind = p.kind == kKindExp;
         bool failed = !mbar_wait(&bar_const, 0, &abort_flag);
         __syncwarp();
+
+        // phi for 32 raw projections, row constant cst; den accumulates bf16(phi) * z.
+        auto features32 = [&](uint32_t (&v)[32], const float* zr, float cst, uint32_t (&pk)[16], float& dsum) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+                const float4 z4 = *reinterpret_cast<const float4*>(zr + i);
+                float f[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    f[k] = exp_kind ? ex2(fmaf(__uint_as_float(v[i + k]), A2, -cst))
+                                    : fmaxf(__uint_as_float(v[i + k]) * p.scale, 0.f) + p.relu_eps_s;
+                const uint32_t w0 = pack_bf16(f[0], f[1]), w1 = pack_bf16(f[2], f[3]);
+                pk[i / 2] = w0;
+                pk[i / 2 + 1] = w1;
+                dsum = fmaf(__uint_as_float(w0 << 16), z4.x, dsum);
+                dsum = fmaf(__uint_as_float(w0 & 0xFFFF0000u), z4.y, dsum);
+                dsum = fmaf(__uint_as_float(w1 << 16), z4.z, dsum);
+                dsum = fmaf(__uint_as_float(w1 & 0xFFFF0000u), z4.w, dsum);
+            }
+        };
 
         auto epi1 = [&](int t) -> bool {
             const int s = t % nslot, k = t / nslot;
@@ -598,52 +754,56 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             tc_fence_after();
             const uint32_t ua = tbase + lane_off + s * slot_cols;
-            float rmax = 0.f;
-            if (p.kind == kKindExp) {
-                rmax = -INFINITY;
-                for (int c0 = 0; c0 < MP; c0 += 32) {
+            float* mx = sMax + (t & 1) * 512;
+            float* dn = sDen + (t & 1) * 512;
+            float dsum = 0.f;
+            if (two) {
+                // Wf <= 64: hold this warp's projections in registers across the row-max exchange.
+                uint32_t v0[32], v1[32];
+                float rmax = -INFINITY;
+                tmem_ld32(ua + cg * Wf, v0);
+                if (Wf == 64) tmem_ld32(ua + cg * Wf + 32, v1);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) rmax = fmaxf(rmax, __uint_as_float(v0[i]));
+                if (Wf == 64) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) rmax = fmaxf(rmax, __uint_as_float(v1[i]));
+                }
+                mx[cg * 128 + r] = rmax;
+                named_bar(1, kEpiThreads);  // every warp has its U values: U may now be overwritten
+                rmax = fmaxf(fmaxf(mx[r], mx[128 + r]), fmaxf(mx[256 + r], mx[384 + r]));
+                const float cst = exp_kind ? A2 * rmax : 0.f;
+                uint32_t pk[16];
+                features32(v0, sz + cg * Wf, cst, pk, dsum);
+                tmem_st16(ua + cg * (Wf / 2), pk);
+                if (Wf == 64) {
+                    features32(v1, sz + cg * Wf + 32, cst, pk, dsum);
+                    tmem_st16(ua + cg * (Wf / 2) + 16, pk);
+                }
+            } else {
+                // Wf = 96 or 128: max pass, exchange, then reload and pack into the own range.
+                float rmax = -INFINITY;
+                for (int c0 = 0; c0 < Wf; c0 += 32) {
                     uint32_t v[32];
-                    tmem_ld32(ua + c0, v);
+                    tmem_ld32(ua + cg * Wf + c0, v);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; i += 2)
-                        rmax = fmaxf(rmax, fmaxf(__uint_as_float(v[i]), __uint_as_float(v[i + 1])));
+                    for (int i = 0; i < 32; ++i) rmax = fmaxf(rmax, __uint_as_float(v[i]));
+                }
+                mx[cg * 128 + r] = rmax;
+                named_bar(1, kEpiThreads);
+                rmax = fmaxf(fmaxf(mx[r], mx[128 + r]), fmaxf(mx[256 + r], mx[384 + r]));
+                const float cst = exp_kind ? A2 * rmax : 0.f;
+                for (int c0 = 0; c0 < Wf; c0 += 32) {
+                    uint32_t v[32], pk[16];
+                    tmem_ld32(ua + cg * Wf + c0, v);
+                    tmem_ld_wait();
+                    features32(v, sz + cg * Wf + c0, cst, pk, dsum);
+                    tmem_st16(ua + cg * Wf + c0 / 2, pk);
                 }
             }
-            const float cst = A2 * rmax;
-            float dsum = 0.f;
-            for (int c0 = 0; c0 < MP; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(ua + c0, v);
-                tmem_ld_wait();
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    const float4 z4 = *reinterpret_cast<const float4*>(sz + c0 + i);
-                    float f0, f1, f2, f3;
-                    if (p.kind == kKindExp) {
-                        f0 = ex2(fmaf(__uint_as_float(v[i + 0]), A2, -cst));
-                        f1 = ex2(fmaf(__uint_as_float(v[i + 1]), A2, -cst));
-                        f2 = ex2(fmaf(__uint_as_float(v[i + 2]), A2, -cst));
-                        f3 = ex2(fmaf(__uint_as_float(v[i + 3]), A2, -cst));
-                    } else {
-                        f0 = fmaxf(__uint_as_float(v[i + 0]) * p.scale, 0.f) + p.relu_eps_s;
-                        f1 = fmaxf(__uint_as_float(v[i + 1]) * p.scale, 0.f) + p.relu_eps_s;
-                        f2 = fmaxf(__uint_as_float(v[i + 2]) * p.scale, 0.f) + p.relu_eps_s;
-                        f3 = fmaxf(__uint_as_float(v[i + 3]) * p.scale, 0.f) + p.relu_eps_s;
-                    }
-                    const uint32_t w0 = pack_bf16(f0, f1), w1 = pack_bf16(f2, f3);
-                    pk[i / 2] = w0;
-                    pk[i / 2 + 1] = w1;
-                    // den uses the same bf16-rounded features as the numerator MMA.
-                    dsum = fmaf(__uint_as_float(w0 << 16), z4.x, dsum);
-                    dsum = fmaf(__uint_as_float(w0 & 0xFFFF0000u), z4.y, dsum);
-                    dsum = fmaf(__uint_as_float(w1 << 16), z4.z, dsum);
-                    dsum = fmaf(__uint_as_float(w1 & 0xFFFF0000u), z4.w, dsum);
-                }
-                tmem_st16(ua + c0 / 2, pk);
-            }
-            den[t & 1] = dsum;
+            dn[cg * 128 + r] = dsum;
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -655,40 +815,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool ok = mbar_wait(&bar_num[s], k & 1, &abort_flag);
             __syncwarp();
             tc_fence_after();
-            const uint32_t na = tbase + lane_off + s * slot_cols + num_off;
-            const float inv = 1.f / den[t & 1];
-            // The staging tile is free once the previous TMA store has read it.
-            if (is_issuer) bulk_wait_read0();
-            named_bar(2, kEpiThreads);
+            const float* dn = sDen + (t & 1) * 512;
+            const float inv = 1.f / (((dn[r] + dn[128 + r]) + dn[256 + r]) + dn[384 + r]);
+            constexpr int kC = D / 4;  // output columns per column group
+            const uint32_t na = tbase + lane_off + s * slot_cols + num_off + cg * kC;
+            uint32_t v[32];
+            if constexpr (kC == 32) {
+                tmem_ld32(na, v);
+            } else {
+                uint32_t v16[16];
+                tmem_ld16(na, v16);
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(na + c0, v);
-                tmem_ld_wait();
+                for (int i = 0; i < 16; ++i) v[i] = v16[i];
+            }
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_ufree[s]);
+            // Each thread stores whole 32-byte sectors of its own row (rows past n are not written).
+            const int row = (t0 + t) * kTile + r;
+            if (row < p.n) {
+                uint4* dst = reinterpret_cast<uint4*>(p.Y + ((size_t)bh * p.n + row) * D + cg * kC);
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
+                for (int cc = 0; cc < kC / 8; ++cc) {
                     uint4 o;
                     o.x = pack_bf16(__uint_as_float(v[8 * cc + 0]) * inv, __uint_as_float(v[8 * cc + 1]) * inv);
                     o.y = pack_bf16(__uint_as_float(v[8 * cc + 2]) * inv, __uint_as_float(v[8 * cc + 3]) * inv);
                     o.z = pack_bf16(__uint_as_float(v[8 * cc + 4]) * inv, __uint_as_float(v[8 * cc + 5]) * inv);
                     o.w = pack_bf16(__uint_as_float(v[8 * cc + 6]) * inv, __uint_as_float(v[8 * cc + 7]) * inv);
-                    const int chunk = (c0 / 8 + cc);  // 16-byte chunk index along the row (0..D/8)
-                    *reinterpret_cast<uint4*>(sY + (chunk / 8) * 16384 + sw128_offset(r, chunk % 8)) = o;
+                    dst[cc] = o;
                 }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar_ufree[s]);
-            fence_async_smem();
-            named_bar(2, kEpiThreads);
-            if (is_issuer) {
-                for (int a = 0; a < kAtoms; ++a) tma_store_3d(&mY, sY + a * 16384, a * 64, (t0 + t) * kTile, bh);
-                bulk_commit();
             }
             return ok;
         };
         // Every epilogue thread runs the whole schedule (failed waits return at once), so the named
-        // barriers inside epi2 always see all 128 threads.
+        // barriers always see all epilogue threads.
         if (T > 0) {
             if (nslot == 2) {
                 failed |= !epi1(0);
@@ -704,7 +865,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         (void)failed;
-        if (is_issuer) bulk_wait0();
     }
     tc_fence_before();
     __syncthreads();
