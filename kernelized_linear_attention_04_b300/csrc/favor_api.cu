@@ -13,6 +13,7 @@
 #include "common.cuh"
 #include "simt_kernels.cuh"
 #include "tc_noncausal.cuh"
+#include "tc_causal.cuh"
 #include "tma_host.h"
 
 namespace favor {
@@ -172,6 +173,9 @@ size_t noncausal_ws_bytes(int B, int H, int n, int d, int m, favor_dtype_t dt) {
     return tc_noncausal_ok(d, m, dt) ? tc_noncausal_ws(B, H, n, d, m).total : noncausal_ws(B, H, n, d, m).total;
 }
 
+// The tensor-core causal scan takes bf16 with d = 64 and m up to 256 (one CTA holds every feature).
+bool tc_causal_ok(int d, int m, favor_dtype_t dt) { return dt == FAVOR_BF16 && d == 64 && m_padded(m) <= 256; }
+
 size_t causal_ws_bytes(int B, int H, int d, int m) {
     const size_t BH = (size_t)B * H;
     return align_up(BH * m * d * sizeof(float), 256) + align_up(BH * m * sizeof(float), 256);
@@ -318,6 +322,23 @@ favor_status_t tc_noncausal(const void* Q, const void* K, const void* V, const v
     return FAVOR_OK;
 }
 
+favor_status_t tc_causal(const void* Q, const void* K, const void* V, const void* Om, void* Y, int B, int H, int n,
+                         int m, int kind, float eps, cudaStream_t s) {
+    const int BH = B * H;
+    CUtensorMap mQ, mK, mV, mOm;
+    if (!tma::encode_bf16_3d(&mQ, Q, 64, n, BH, 64, tcc::kTile) || !tma::encode_bf16_3d(&mK, K, 64, n, BH, 64, tcc::kTile) ||
+        !tma::encode_bf16_3d(&mV, V, 64, n, BH, 64, tcc::kTile) || !tma::encode_bf16_2d(&mOm, Om, 64, m, 64, 128))
+        return FAVOR_ERR_CUDA;
+    const int m_pad = m_padded(m);
+    tcc::CausalParams cp{n, m, m_pad, kind, eps * std::sqrt((float)m), qk_scale(64), static_cast<__nv_bfloat16*>(Y)};
+    const size_t smem = tcc::CausalSmem::bytes(m_pad);
+    FAVOR_TRY(set_smem(tcc::causal_tc, smem));
+    FAVOR_TRY(traced(FAVOR_KERNEL_CAUSAL, s, [&] {
+        tcc::causal_tc<<<BH, tcc::kThreads, smem, s>>>(mQ, mK, mV, mOm, cp);
+    }));
+    return FAVOR_OK;
+}
+
 // dtype x d dispatch
 #define FAVOR_DISPATCH(dt, d, FN, ...)                                                     \
     ((dt) == FAVOR_F32 ? ((d) == 64 ? FN<float, 64>(__VA_ARGS__) : FN<float, 128>(__VA_ARGS__)) \
@@ -384,8 +405,8 @@ size_t favor_workspace_bytes(favor_op_t op, int B, int H, int n, int d, int m, f
         case FAVOR_OP_FEATURES: return features_ws_bytes(B, H, kind, stab);
         case FAVOR_OP_NONCAUSAL: return noncausal_ws_bytes(B, H, n, d, m, dt);
         case FAVOR_OP_CAUSAL:
-            if (chunk != 0 && chunk != 64) return (size_t)-1;
-            return causal_ws_bytes(B, H, d, m);
+            if (chunk != 0 && chunk != 64 && chunk != 128) return (size_t)-1;
+            return tc_causal_ok(d, m, dt) ? 0 : causal_ws_bytes(B, H, d, m);
     }
     return (size_t)-1;
 }
@@ -422,10 +443,11 @@ favor_status_t favor_attn_causal(const void* Q, const void* K, const void* V, co
                                  int H, int n, int d, int m, int chunk, favor_dtype_t dt, favor_kind_t kind,
                                  float relu_eps, void* workspace, size_t ws_bytes, void* stream) {
     FAVOR_TRY(check_attn_args(Q, K, V, Omega, Y, B, H, n, d, m, dt, kind, relu_eps));
-    if (chunk != 0 && chunk != 64) return FAVOR_ERR_UNSUPPORTED;
+    if (chunk != 0 && chunk != 64 && chunk != 128) return FAVOR_ERR_UNSUPPORTED;
     if ((int64_t)B * H * n == 0) return FAVOR_OK;
-    FAVOR_TRY(check_ws(workspace, ws_bytes, causal_ws_bytes(B, H, d, m)));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (tc_causal_ok(d, m, dt)) return tc_causal(Q, K, V, Omega, Y, B, H, n, m, (int)kind, relu_eps, s);
+    FAVOR_TRY(check_ws(workspace, ws_bytes, causal_ws_bytes(B, H, d, m)));
     return FAVOR_DISPATCH(dt, d, simt_causal, Q, K, V, Omega, Y, B, H, n, m, (int)kind, relu_eps, workspace, s);
 }
 

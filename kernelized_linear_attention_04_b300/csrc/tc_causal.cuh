@@ -1,0 +1,510 @@
+// Tensor-core (tcgen05 + TMA + TMEM) causal FAVOR+ scan, bf16 in / fp32 accumulate, d = 64.
+//
+// One CTA walks the 128-token tiles of one head in order. Per tile t (rows i, keys j of the tile):
+//   num_i = phi(q_i) S_<t + sum_{j <= i} (phi(q_i) . phi(k_j)) v_j
+//   den_i = phi(q_i) z_<t + sum_{j <= i}  phi(q_i) . phi(k_j)
+//   y_i   = num_i / den_i;   then S_<t+1 = S_<t + Phi(K_t)^T V_t,  z_<t+1 = z_<t + Phi(K_t)^T 1.
+// The prefix state is carried at every tile boundary (128 tokens); within a tile the keys are
+// masked by j <= i, which for two 64-token chunks is exactly their chunked prefix-sum result.
+//
+// Features are processed in 128-feature groups g (m <= 256 here). Per group:
+//   U = Q_t Omega_g^T -> phi_g(Q) (tokens on TMEM lanes) -> shared memory (K-major);
+//   U = K_t Omega_g^T -> phi_g(K) -> shared memory;
+//   scores D_sc += phi_g(Q) phi_g(K)^T, inter D_num += phi_g(Q) S_g (the state as taken at the tile
+//   start, split into hi + lo bf16 images so that it keeps about 16 significant bits), state S_g += phi_g(K)^T V_t and z_g += phi_g(K)^T 1 (MMA with a block
+//   of ones), all on the tensor cores with fp32 accumulation in TMEM.
+// After the groups: the masked scores A~ are split into two bf16 operands (hi + lo, about 16
+// significant bits) for D_num += A~ V_t; den takes phi(q) . z_<t on the CUDA cores plus the fp32
+// row sums of the masked scores.
+//
+// Stabilisers: a query row uses c_i = W |q^_i| (W = largest row norm of Omega; Cauchy-Schwarz bounds
+// every w_r . q^_i by it), the same in every feature group; keys use one running per-head constant
+// raised (with a rescale of S and z) when a tile's bound W |k^| - |k^|^2/2 exceeds it by more than
+// kStabSlackHi. Both cancel in num / den; the common 1/sqrt(m) is dropped.
+#pragma once
+
+#include "tc.cuh"
+#include "tc_noncausal.cuh"  // shared helpers: ex2, tile_row_sqnorm, slack constants
+
+namespace favor {
+namespace tcc {
+
+using namespace favor::tc;
+using tcnc::ex2;
+using tcnc::kStabSlackHi;
+using tcnc::kStabSlackLo;
+using tcnc::tile_row_sqnorm;
+
+constexpr int kTile = 128;
+constexpr int kD = 64;                 // head dimension handled by this kernel
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kTileBytes = kTile * kD * 2;  // 16 KB: one [128 x 64] bf16 tile
+constexpr int kPhiBytes = kTile * 128 * 2;  // 32 KB: [128 tokens x 128 features] bf16, two K atoms
+
+// TMEM columns
+constexpr uint32_t kColS = 0;      // S_g at g * 80: 64 columns of S, 16 of z (all equal)
+constexpr uint32_t kColU = 160;    // projection output, 128 columns
+constexpr uint32_t kColSc = 288;   // scores, 128 columns
+constexpr uint32_t kColNum = 416;  // numerator, 64 columns
+
+struct CausalParams {
+    int n;
+    int m;
+    int m_pad;
+    int kind;
+    float relu_eps_s;
+    float scale;
+    __nv_bfloat16* Y;
+};
+
+struct CausalSmem {
+    // Omega (m_pad x 64, K-major), Q, K and V tiles, phi(Q) / A~lo, phi(K) / A~hi, the state snapshot
+    // as hi and lo bf16 images (m_pad x 64 each, MN-major), ones block (16 x 128 bf16, K-major), z
+    // snapshot (m_pad fp32).
+    static size_t bytes(int m_pad) {
+        return 1024 + (size_t)m_pad * 128 + 3 * kTileBytes + 2 * kPhiBytes + 2 * (size_t)m_pad * 128 + 4096 +
+               (size_t)m_pad * 4;
+    }
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    causal_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+              const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mOm, CausalParams p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];  // aligned to 1024 by hand below
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int MP = p.m_pad;
+    const int G = MP / 128;
+    uint8_t* sOm = smem;                          // G regions of 128 rows x 128 B
+    uint8_t* sQ = sOm + (size_t)MP * 128;
+    uint8_t* sK = sQ + kTileBytes;
+    uint8_t* sV = sK + kTileBytes;
+    uint8_t* sPQ = sV + kTileBytes;               // phi(Q): 2 K-atom regions of 128 rows x 128 B; later A~lo
+    uint8_t* sPK = sPQ + kPhiBytes;               // phi(K); later A~hi
+    uint8_t* sS = sPK + kPhiBytes;                // S snapshot hi: MP rows x 128 B (MN-major, d contiguous)
+    uint8_t* sSl = sS + (size_t)MP * 128;         // S snapshot lo (S - hi, rounded)
+    uint8_t* sOnes = sSl + (size_t)MP * 128;      // 2 K-atom regions of 16 rows x 128 B
+    float* sZ = reinterpret_cast<float*>(sOnes + 4096);  // [MP] z snapshot
+    __shared__ uint64_t bar_om, bar_qfull, bar_kfull, bar_qkempty, bar_vfull, bar_vempty;
+    __shared__ uint64_t bar_snap, bar_ufull, bar_ufree, bar_phq, bar_phk, bar_grp, bar_atil, bar_num, bar_dfree;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+    __shared__ float red[kEpiWarps];
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int bh = blockIdx.x;
+    const int T = (p.n + kTile - 1) / kTile;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(&bar_om, 1);
+        mbar_init(&bar_qfull, 1);
+        mbar_init(&bar_kfull, 1);
+        mbar_init(&bar_qkempty, 1);
+        mbar_init(&bar_vfull, 1);
+        mbar_init(&bar_vempty, 1);
+        mbar_init(&bar_snap, kEpiWarps);
+        mbar_init(&bar_ufull, 1);
+        mbar_init(&bar_ufree, kEpiWarps);
+        mbar_init(&bar_phq, kEpiWarps);
+        mbar_init(&bar_phk, kEpiWarps);
+        mbar_init(&bar_grp, 1);
+        mbar_init(&bar_atil, kEpiWarps);
+        mbar_init(&bar_num, 1);
+        mbar_init(&bar_dfree, kEpiWarps);
+        fence_mbar_init();
+    }
+    // ones block (K-major, every element 1.0): z_g = phi_g(K)^T 1 via the tensor cores
+    for (int i = threadIdx.x; i < 4096 / 16; i += blockDim.x)
+        reinterpret_cast<uint4*>(sOnes)[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    fence_async_smem();
+    if (warp == 1) tmem_alloc(&tmem_base, 512);
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = tmem_base;
+
+    if (warp == 0) {
+        // ---------------- TMA producer (lane 0) ----------------
+        if (lane == 0) {
+            tma_prefetch_desc(&mQ);
+            tma_prefetch_desc(&mK);
+            tma_prefetch_desc(&mV);
+            tma_prefetch_desc(&mOm);
+            mbar_arrive_expect_tx(&bar_om, (uint32_t)MP * 128);
+            for (int r0 = 0; r0 < MP; r0 += 128) tma_load_2d(sOm + (size_t)r0 * 128, &mOm, &bar_om, 0, r0);
+            bool ok = true;
+            for (int t = 0; t < T && ok; ++t) {
+                // Q and K of tile t once tile t-1 is projected; V of tile t once tile t-1's intra MMA is done.
+                if (!(ok = mbar_wait(&bar_qkempty, (t & 1) ^ 1, &abort_flag))) break;
+                mbar_arrive_expect_tx(&bar_qfull, kTileBytes);
+                tma_load_3d(sQ, &mQ, &bar_qfull, 0, t * kTile, bh);
+                mbar_arrive_expect_tx(&bar_kfull, kTileBytes);
+                tma_load_3d(sK, &mK, &bar_kfull, 0, t * kTile, bh);
+                if (!(ok = mbar_wait(&bar_vempty, (t & 1) ^ 1, &abort_flag))) break;
+                mbar_arrive_expect_tx(&bar_vfull, kTileBytes);
+                tma_load_3d(sV, &mV, &bar_vfull, 0, t * kTile, bh);
+            }
+            // Drain the loads in flight before the CTA may exit.
+            volatile int never = 0;
+            mbar_wait(&bar_om, 0, &never);
+            if (T > 0) {
+                mbar_wait(&bar_qfull, (T - 1) & 1, &never);
+                mbar_wait(&bar_kfull, (T - 1) & 1, &never);
+                mbar_wait(&bar_vfull, (T - 1) & 1, &never);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (lane 0) ----------------
+        if (lane == 0) {
+            constexpr uint32_t id_proj = idesc_bf16(128, 128, false, false);  // U = X Om_g^T
+            constexpr uint32_t id_sc = idesc_bf16(128, 128, false, false);    // phi(Q) phi(K)^T
+            constexpr uint32_t id_num = idesc_bf16(128, kD, false, true);     // phi(Q) S_g, A~ V
+            constexpr uint32_t id_st = idesc_bf16(128, kD, true, true);       // phi(K)^T V
+            constexpr uint32_t id_z = idesc_bf16(128, 16, true, false);       // phi(K)^T 1
+            bool ok = mbar_wait(&bar_om, 0, &abort_flag);
+            tc_fence_after();
+            int uuse = 0;  // uses of the U slot so far
+            auto proj = [&](const uint8_t* x, int g) {
+#pragma unroll
+                for (int ks = 0; ks < kD / 16; ++ks) {
+                    uint64_t ad = sdesc_sw128(smem_u32(x + ks * 32), 16, 1024);
+                    uint64_t bd = sdesc_sw128(smem_u32(sOm + (size_t)g * 16384 + ks * 32), 16, 1024);
+                    mma_ss(tbase + kColU, ad, bd, id_proj, ks > 0);
+                }
+                mma_commit(&bar_ufull);
+            };
+            for (int t = 0; t < T && ok; ++t) {
+                ok = ok && mbar_wait(&bar_qfull, t & 1, &abort_flag) && mbar_wait(&bar_kfull, t & 1, &abort_flag);
+                ok = ok && mbar_wait(&bar_snap, t & 1, &abort_flag);
+                ok = ok && mbar_wait(&bar_dfree, (t & 1) ^ 1, &abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                const uint8_t* vt = sV;
+                bool have_v = false;
+                for (int g = 0; g < G && ok; ++g) {
+                    // projections: Q then K into the one U slot
+                    ok = mbar_wait(&bar_ufree, (uuse & 1) ^ 1, &abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    proj(sQ, g);
+                    ++uuse;
+                    ok = mbar_wait(&bar_ufree, (uuse & 1) ^ 1, &abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    proj(sK, g);
+                    ++uuse;
+                    if (g == G - 1) mma_commit(&bar_qkempty);
+                    const int gu = t * G + g;  // group use count
+                    ok = mbar_wait(&bar_phq, gu & 1, &abort_flag) && mbar_wait(&bar_phk, gu & 1, &abort_flag);
+                    if (ok && !have_v) ok = have_v = mbar_wait(&bar_vfull, t & 1, &abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    // scores and inter numerator (K = 128 features of group g, two K atoms)
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const int a = ks / 4, w = ks % 4;
+                        uint64_t ad = sdesc_sw128(smem_u32(sPQ + a * 16384 + w * 32), 16, 1024);
+                        uint64_t bd = sdesc_sw128(smem_u32(sPK + a * 16384 + w * 32), 16, 1024);
+                        mma_ss(tbase + kColSc, ad, bd, id_sc, (g > 0 || ks > 0));
+                    }
+                    for (int part = 0; part < 2; ++part) {  // state snapshot hi, then lo
+                        const uint8_t* sp = part == 0 ? sS : sSl;
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const int a = ks / 4, w = ks % 4;
+                            uint64_t ad = sdesc_sw128(smem_u32(sPQ + a * 16384 + w * 32), 16, 1024);
+                            uint64_t bd = sdesc_sw128(smem_u32(sp + (size_t)(g * 128 + ks * 16) * 128), 16, 1024);
+                            mma_ss(tbase + kColNum, ad, bd, id_num, (g > 0 || part > 0 || ks > 0));
+                        }
+                    }
+                    // state update: S_g += phi_g(K)^T V_t, z_g += phi_g(K)^T 1 (K = 128 tokens)
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        uint64_t ad = sdesc_sw128(smem_u32(sPK + ks * 2048), 16384, 1024);
+                        uint64_t bd = sdesc_sw128(smem_u32(vt + ks * 2048), 16, 1024);
+                        mma_ss(tbase + kColS + g * 80, ad, bd, id_st, (t > 0 || ks > 0));
+                    }
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const int a = ks / 4, w = ks % 4;
+                        uint64_t ad = sdesc_sw128(smem_u32(sPK + ks * 2048), 16384, 1024);
+                        uint64_t bd = sdesc_sw128(smem_u32(sOnes + a * 2048 + w * 32), 16, 1024);
+                        mma_ss(tbase + kColS + g * 80 + 64, ad, bd, id_z, (t > 0 || ks > 0));
+                    }
+                    mma_commit(&bar_grp);
+                }
+                if (!ok) break;
+                // intra-tile numerator: D_num += (A~hi + A~lo) V_t (hi in the phi(K) buffer, lo in the
+                // phi(Q) buffer; K = 128 tokens)
+                ok = mbar_wait(&bar_atil, t & 1, &abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                for (int part = 0; part < 2; ++part) {
+                    const uint8_t* at = part == 0 ? sPK : sPQ;
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const int a = ks / 4, w = ks % 4;
+                        uint64_t ad = sdesc_sw128(smem_u32(at + a * 16384 + w * 32), 16, 1024);
+                        uint64_t bd = sdesc_sw128(smem_u32(vt + ks * 2048), 16, 1024);
+                        mma_ss(tbase + kColNum, ad, bd, id_num, 1);
+                    }
+                }
+                mma_commit(&bar_num);
+                mma_commit(&bar_vempty);
+            }
+        }
+    } else {
+        // ---------------- epilogue: thread = TMEM lane (token row for projections/scores,
+        // feature row for the state) ----------------
+        const int q = warp & 3;
+        const int r = q * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        const float A2 = p.scale * kLog2e;
+        const bool exp_kind = p.kind == kKindExp;
+        bool failed = !mbar_wait(&bar_om, 0, &abort_flag);
+        __syncwarp();
+        // W = largest row norm of Omega
+        float W = 0.f;
+        if (exp_kind) {
+            float w2 = 0.f;
+            for (int row = r; row < MP; row += 128) w2 = fmaxf(w2, tile_row_sqnorm<64>(sOm + (size_t)(row >> 7) * 16384, row & 127));
+            w2 = warp_max(w2);
+            if (lane == 0) red[q] = w2;
+            named_bar(1, 128);
+            W = sqrtf(fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])));
+            named_bar(1, 128);
+        }
+        float stab = 0.f;
+        int guse = 0;    // feature groups whose MMAs have been committed (bar_grp phases)
+        int uuse_e = 0;  // projections consumed (bar_ufull phases)
+        for (int t = 0; t < T; ++t) {
+            const int i_tok = t * kTile + r;  // this thread's token (query row / key row)
+            const bool valid = i_tok < p.n;
+            failed |= !mbar_wait(&bar_qfull, t & 1, &abort_flag);
+            failed |= !mbar_wait(&bar_kfull, t & 1, &abort_flag);
+            __syncwarp();
+            // norms of this thread's query and key rows
+            const float qn2 = exp_kind ? p.scale * p.scale * tile_row_sqnorm<64>(sQ, r) : 0.f;
+            const float kn2 = exp_kind ? p.scale * p.scale * tile_row_sqnorm<64>(sK, r) : 0.f;
+            const float cq = exp_kind ? W * sqrtf(qn2) * kLog2e : 0.f;
+            float f = 1.f;
+            if (exp_kind) {
+                const float b = valid ? W * sqrtf(kn2) - 0.5f * kn2 : -INFINITY;
+                const float bm = warp_max(b);
+                if (lane == 0) red[q] = bm;
+                named_bar(1, 128);
+                const float Bt = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+                named_bar(1, 128);
+                if (t == 0) {
+                    stab = Bt - kStabSlackLo;
+                } else if (Bt > stab + kStabSlackHi) {
+                    const float nst = Bt - kStabSlackLo;
+                    f = ex2((stab - nst) * kLog2e);
+                    stab = nst;
+                }
+            }
+            const float ck = valid ? (exp_kind ? (0.5f * kn2 + stab) * kLog2e : 0.f) : INFINITY;
+            // ---- state snapshot for this tile (thread = feature lane r of each group) ----
+            if (t > 0) {
+                // every state MMA of the previous tile has completed once its last group committed
+                failed |= !mbar_wait(&bar_grp, (guse - 1) & 1, &abort_flag);
+                __syncwarp();
+                tc_fence_after();
+            }
+            for (int g = 0; g < G; ++g) {
+                const int feat = g * 128 + r;
+                uint32_t v[64];
+                float zv = 0.f;
+                if (t > 0) {
+                    const uint32_t sa = tbase + lane_off + kColS + g * 80;
+                    tmem_ld32(sa, *reinterpret_cast<uint32_t(*)[32]>(v));
+                    tmem_ld32(sa + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+                    uint32_t zz[16];
+                    tmem_ld16(sa + 64, zz);
+                    tmem_ld_wait();
+                    zv = __uint_as_float(zz[0]);
+                    if (f != 1.f) {  // the key stabiliser moved: rescale the accumulated state
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) zz[i] = __float_as_uint(__uint_as_float(zz[i]) * f);
+                        zv *= f;
+                        tmem_st32(sa, *reinterpret_cast<uint32_t(*)[32]>(v));
+                        tmem_st32(sa + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+                        tmem_st16(sa + 64, zz);
+                        tmem_st_wait();
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) v[i] = 0u;
+                }
+                if (feat >= p.m) zv = 0.f;
+                // bf16 snapshot row `feat` as hi + lo (about 16 significant bits): 64 values each,
+                // 8 swizzled 16-byte chunks
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    float x[8], l[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) x[k] = __uint_as_float(v[8 * c + k]);
+                    uint4 o;
+                    o.x = pack_bf16(x[0], x[1]);
+                    o.y = pack_bf16(x[2], x[3]);
+                    o.z = pack_bf16(x[4], x[5]);
+                    o.w = pack_bf16(x[6], x[7]);
+                    const uint32_t hw[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        l[2 * k] = x[2 * k] - __uint_as_float(hw[k] << 16);
+                        l[2 * k + 1] = x[2 * k + 1] - __uint_as_float(hw[k] & 0xFFFF0000u);
+                    }
+                    uint4 ol;
+                    ol.x = pack_bf16(l[0], l[1]);
+                    ol.y = pack_bf16(l[2], l[3]);
+                    ol.z = pack_bf16(l[4], l[5]);
+                    ol.w = pack_bf16(l[6], l[7]);
+                    *reinterpret_cast<uint4*>(sS + sw128_offset(feat, c)) = o;
+                    *reinterpret_cast<uint4*>(sSl + sw128_offset(feat, c)) = ol;
+                }
+                sZ[feat] = zv;
+            }
+            tc_fence_before();
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_snap);
+            named_bar(1, 128);  // z snapshot visible to every epilogue thread
+            // ---- per feature group: phi(Q), phi(K) into shared memory ----
+            float den_inter = 0.f;
+            for (int g = 0; g < G; ++g) {
+                if (g > 0) {  // the previous group's MMAs have read the phi buffers
+                    failed |= !mbar_wait(&bar_grp, (guse - 1) & 1, &abort_flag);
+                    __syncwarp();
+                }
+                for (int which = 0; which < 2; ++which) {  // 0: queries, 1: keys
+                    failed |= !mbar_wait(&bar_ufull, uuse_e & 1, &abort_flag);
+                    __syncwarp();
+                    tc_fence_after();
+                    ++uuse_e;
+                    uint8_t* dst = which == 0 ? sPQ : sPK;
+                    const float cst = which == 0 ? cq : ck;
+                    const bool zero_row = which == 1 && !valid;
+                    for (int h = 0; h < 2; ++h) {  // 64 features at a time
+                        uint32_t v[64];
+                        tmem_ld32(tbase + lane_off + kColU + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(v));
+                        tmem_ld32(tbase + lane_off + kColU + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+                        tmem_ld_wait();
+                        if (h == 1) {  // U has been read: the next projection may overwrite it
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&bar_ufree);
+                        }
+                        const int f0 = g * 128 + 64 * h;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            float ph[8];
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) {
+                                const float a = __uint_as_float(v[8 * c + k]);
+                                float x = exp_kind ? ex2(fmaf(a, A2, -cst)) : fmaxf(a * p.scale, 0.f) + p.relu_eps_s;
+                                if (zero_row || f0 + 8 * c + k >= p.m) x = 0.f;
+                                ph[k] = x;
+                            }
+                            uint4 o;
+                            o.x = pack_bf16(ph[0], ph[1]);
+                            o.y = pack_bf16(ph[2], ph[3]);
+                            o.z = pack_bf16(ph[4], ph[5]);
+                            o.w = pack_bf16(ph[6], ph[7]);
+                            *reinterpret_cast<uint4*>(dst + h * 16384 + sw128_offset(r, c)) = o;
+                            if (which == 0) {  // den: phi(q) . z_<t with the bf16-rounded features
+                                const float4 za = *reinterpret_cast<const float4*>(sZ + f0 + 8 * c);
+                                const float4 zb = *reinterpret_cast<const float4*>(sZ + f0 + 8 * c + 4);
+                                den_inter = fmaf(__uint_as_float(o.x << 16), za.x, den_inter);
+                                den_inter = fmaf(__uint_as_float(o.x & 0xFFFF0000u), za.y, den_inter);
+                                den_inter = fmaf(__uint_as_float(o.y << 16), za.z, den_inter);
+                                den_inter = fmaf(__uint_as_float(o.y & 0xFFFF0000u), za.w, den_inter);
+                                den_inter = fmaf(__uint_as_float(o.z << 16), zb.x, den_inter);
+                                den_inter = fmaf(__uint_as_float(o.z & 0xFFFF0000u), zb.y, den_inter);
+                                den_inter = fmaf(__uint_as_float(o.w << 16), zb.z, den_inter);
+                                den_inter = fmaf(__uint_as_float(o.w & 0xFFFF0000u), zb.w, den_inter);
+                            }
+                        }
+                    }
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(which == 0 ? &bar_phq : &bar_phk);
+                }
+                ++guse;
+            }
+            // ---- masked scores -> A~ (bf16, in the phi(K) buffer), den_intra ----
+            failed |= !mbar_wait(&bar_grp, (guse - 1) & 1, &abort_flag);
+            __syncwarp();
+            tc_fence_after();
+            float den_intra = 0.f;
+            for (int h = 0; h < 2; ++h) {  // keys 64h .. 64h + 63
+                uint32_t v[64];
+                tmem_ld32(tbase + lane_off + kColSc + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(v));
+                tmem_ld32(tbase + lane_off + kColSc + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    float a[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        a[k] = (64 * h + 8 * c + k <= r) ? __uint_as_float(v[8 * c + k]) : 0.f;
+                        den_intra += a[k];
+                    }
+                    // A~ = hi + lo, both bf16: the intra-tile weights keep about 16 significant bits.
+                    uint4 o, ol;
+                    o.x = pack_bf16(a[0], a[1]);
+                    o.y = pack_bf16(a[2], a[3]);
+                    o.z = pack_bf16(a[4], a[5]);
+                    o.w = pack_bf16(a[6], a[7]);
+                    ol.x = pack_bf16(a[0] - __uint_as_float(o.x << 16), a[1] - __uint_as_float(o.x & 0xFFFF0000u));
+                    ol.y = pack_bf16(a[2] - __uint_as_float(o.y << 16), a[3] - __uint_as_float(o.y & 0xFFFF0000u));
+                    ol.z = pack_bf16(a[4] - __uint_as_float(o.z << 16), a[5] - __uint_as_float(o.z & 0xFFFF0000u));
+                    ol.w = pack_bf16(a[6] - __uint_as_float(o.w << 16), a[7] - __uint_as_float(o.w & 0xFFFF0000u));
+                    *reinterpret_cast<uint4*>(sPK + h * 16384 + sw128_offset(r, c)) = o;
+                    *reinterpret_cast<uint4*>(sPQ + h * 16384 + sw128_offset(r, c)) = ol;
+                }
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_atil);
+            // ---- y = num / den ----
+            failed |= !mbar_wait(&bar_num, t & 1, &abort_flag);
+            __syncwarp();
+            tc_fence_after();
+            {
+                uint32_t v[64];
+                tmem_ld32(tbase + lane_off + kColNum, *reinterpret_cast<uint32_t(*)[32]>(v));
+                tmem_ld32(tbase + lane_off + kColNum + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_dfree);
+                const float inv = 1.f / (den_inter + den_intra);
+                if (valid) {
+                    uint4* dst = reinterpret_cast<uint4*>(p.Y + ((size_t)bh * p.n + i_tok) * kD);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        uint4 o;
+                        o.x = pack_bf16(__uint_as_float(v[8 * c + 0]) * inv, __uint_as_float(v[8 * c + 1]) * inv);
+                        o.y = pack_bf16(__uint_as_float(v[8 * c + 2]) * inv, __uint_as_float(v[8 * c + 3]) * inv);
+                        o.z = pack_bf16(__uint_as_float(v[8 * c + 4]) * inv, __uint_as_float(v[8 * c + 5]) * inv);
+                        o.w = pack_bf16(__uint_as_float(v[8 * c + 6]) * inv, __uint_as_float(v[8 * c + 7]) * inv);
+                        dst[c] = o;
+                    }
+                }
+            }
+        }
+        (void)failed;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 512);
+    }
+}
+
+}  // namespace tcc
+}  // namespace favor

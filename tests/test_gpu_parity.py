@@ -127,6 +127,17 @@ def test_growing_key_norms_exercise_stabiliser_rescale(favor, causal, dtype):
     assert_close_attn(f64(Y), ref, dtype, "growing keys")
 
 
+def test_causal_concentrated_weights(favor):
+    """A seed where one key carries about 93% of a query's weight (|y| = 4.18, where a bf16 output
+    step is 0.03): the carried prefix state must keep more than bf16 precision for the max-abs gate."""
+    w = si.Workload("case", 2, 3, 777, 64, 256, "bf16", True, seed=17 + 777, omega_seed=13 + 256)
+    Q, K, V, Om, om64 = device_inputs(w)
+    Y = run_attn(favor, w, Q, K, V, Om)
+    ref = oracle_attn(w, f64(Q), f64(K), f64(V), om64)
+    assert abs(ref[1, 0, 166, 10]) > 4.0
+    assert_close_attn(f64(Y), ref, "bf16", "concentrated weights")
+
+
 def test_empty_sequence(favor):
     Q = torch.zeros(2, 3, 0, 64, device="cuda", dtype=torch.bfloat16)
     Om = torch.zeros(64, 64, device="cuda", dtype=torch.bfloat16)
