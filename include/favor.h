@@ -99,8 +99,12 @@ favor_status_t favor_attn_noncausal(const void* Q, const void* K, const void* V,
  * Causal FAVOR+ attention ("Performer for vision", *How It Works*, Step 2: prefix sums so that
  * each token attends only to itself and earlier tokens; "Performer" paper note, *Normalization*):
  *   y_i = phi(q_i)^T S_i / phi(q_i)^T z_i,  S_i = sum_{j<=i} phi(k_j) v_j^T,  z_i = sum_{j<=i} phi(k_j).
- * Computed as a chunked scan: per chunk of `chunk` tokens, an intra-chunk lower-triangular block
- * plus the carried prefix state. chunk: 0 (default, 64) or 64. Shapes and dtypes as above.
+ * Computed as a chunked scan: per chunk, an intra-chunk lower-triangular block plus the carried
+ * prefix state. chunk: 0 (implementation default), 64 or 128; the result does not depend on it
+ * beyond rounding. bf16 with d = 64 and m <= 256 runs the tensor-core scan, which carries the state
+ * every 128 tokens and masks j <= i inside each 128-token tile (two 64-token chunks give exactly
+ * that sum); other inputs run on CUDA cores in 16-token steps. Shapes and dtypes as above.
+ * Workspace: 0 bytes on the tensor-core scan.
  */
 favor_status_t favor_attn_causal(const void* Q, const void* K, const void* V, const void* Omega, void* Y,
                                  int B, int H, int n, int d, int m, int chunk, favor_dtype_t dt,
