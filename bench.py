@@ -91,12 +91,12 @@ def kernel_work(w, kernel: str) -> tuple[float, float]:
 
 def tensor_core_path(w) -> bool:
     """True when the library runs workload w on its tcgen05 kernels (bf16; non-causal with d = 64, or
-    d = 128 with m <= 256 after padding to a multiple of 128; causal with d = 64 and m <= 256)."""
+    d = 128 with m <= 256 after padding to a multiple of 128; causal with d = 64 and m <= 512)."""
     if w.dtype != "bf16":
         return False
     m_pad = -(-w.m // 128) * 128
     if w.causal:
-        return w.d == 64 and m_pad <= 256
+        return w.d == 64 and m_pad <= 512
     return w.d == 64 or m_pad <= 256
 
 

@@ -173,8 +173,18 @@ size_t noncausal_ws_bytes(int B, int H, int n, int d, int m, favor_dtype_t dt) {
     return tc_noncausal_ok(d, m, dt) ? tc_noncausal_ws(B, H, n, d, m).total : noncausal_ws(B, H, n, d, m).total;
 }
 
-// The tensor-core causal scan takes bf16 with d = 64 and m up to 256 (one CTA holds every feature).
-bool tc_causal_ok(int d, int m, favor_dtype_t dt) { return dt == FAVOR_BF16 && d == 64 && m_padded(m) <= 256; }
+// The tensor-core causal scan takes bf16 with d = 64; a head's 128-feature groups are spread over a
+// cluster of 1, 2 or 4 CTAs (each holding at most two groups in TMEM).
+bool tc_causal_ok(int d, int m, favor_dtype_t dt) { return dt == FAVOR_BF16 && d == 64 && m_padded(m) <= 512; }
+
+// Cluster size for the causal scan: with fewer heads than SMs, one group per CTA (more CTAs per
+// head); otherwise the fewest CTAs whose two-group TMEM budget holds the head's features.
+int causal_cluster(int BH, int m) {
+    const int groups = m_padded(m) / 128;
+    int cs = groups == 3 ? 4 : groups;                 // one group per CTA
+    if (BH >= kNumSMs) cs = groups <= 2 ? 1 : 2;       // two groups per CTA
+    return cs;
+}
 
 size_t causal_ws_bytes(int B, int H, int d, int m) {
     const size_t BH = (size_t)B * H;
@@ -329,14 +339,27 @@ favor_status_t tc_causal(const void* Q, const void* K, const void* V, const void
     if (!tma::encode_bf16_3d(&mQ, Q, 64, n, BH, 64, tcc::kTile) || !tma::encode_bf16_3d(&mK, K, 64, n, BH, 64, tcc::kTile) ||
         !tma::encode_bf16_3d(&mV, V, 64, n, BH, 64, tcc::kTile) || !tma::encode_bf16_2d(&mOm, Om, 64, m, 64, 128))
         return FAVOR_ERR_CUDA;
-    const int m_pad = m_padded(m);
-    tcc::CausalParams cp{n, m, m_pad, kind, eps * std::sqrt((float)m), qk_scale(64), static_cast<__nv_bfloat16*>(Y)};
-    const size_t smem = tcc::CausalSmem::bytes(m_pad);
+    const int cs = causal_cluster(BH, m);
+    const int groups = m_padded(m) / 128;
+    const int m_cta = ((groups + cs - 1) / cs) * 128;  // features per CTA
+    tcc::CausalParams cp{n, m, m_cta, kind, eps * std::sqrt((float)m), qk_scale(64), static_cast<__nv_bfloat16*>(Y)};
+    const size_t smem = tcc::CausalSmem::bytes(m_cta);
     FAVOR_TRY(set_smem(tcc::causal_tc, smem));
-    FAVOR_TRY(traced(FAVOR_KERNEL_CAUSAL, s, [&] {
-        tcc::causal_tc<<<BH, tcc::kThreads, smem, s>>>(mQ, mK, mV, mOm, cp);
-    }));
-    return FAVOR_OK;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(BH * cs, 1, 1);
+    cfg.blockDim = dim3(tcc::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t lerr = cudaSuccess;
+    FAVOR_TRY(traced(FAVOR_KERNEL_CAUSAL, s, [&] { lerr = cudaLaunchKernelEx(&cfg, tcc::causal_tc, mQ, mK, mV, mOm, cp); }));
+    return lerr == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;
 }
 
 // dtype x d dispatch

@@ -7,7 +7,9 @@
 // The prefix state is carried at every tile boundary (128 tokens); within a tile the keys are
 // masked by j <= i, which for two 64-token chunks is exactly their chunked prefix-sum result.
 //
-// Features are processed in 128-feature groups g (m <= 256 here). Per group:
+// Features are processed in 128-feature groups g; a head's groups are split over the CTAs of a
+// thread-block cluster (1, 2 or 4 CTAs, at most two groups each), which add their partial
+// numerators and denominators through distributed shared memory once per tile. Per group:
 //   U = Q_t Omega_g^T -> phi_g(Q) (tokens on TMEM lanes) -> shared memory (K-major);
 //   U = K_t Omega_g^T -> phi_g(K) -> shared memory;
 //   scores D_sc += phi_g(Q) phi_g(K)^T, inter D_num += phi_g(Q) S_g (the state as taken at the tile
@@ -37,7 +39,7 @@ using tcnc::tile_row_sqnorm;
 
 constexpr int kTile = 128;
 constexpr int kD = 64;                 // head dimension handled by this kernel
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 16;  // four column groups x four TMEM lane quarters
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kTileBytes = kTile * kD * 2;  // 16 KB: one [128 x 64] bf16 tile
 constexpr int kPhiBytes = kTile * 128 * 2;  // 32 KB: [128 tokens x 128 features] bf16, two K atoms
@@ -51,7 +53,7 @@ constexpr uint32_t kColNum = 416;  // numerator, 64 columns
 struct CausalParams {
     int n;
     int m;
-    int m_pad;
+    int m_pad;   // features handled by one CTA, a multiple of 128 (at most 256)
     int kind;
     float relu_eps_s;
     float scale;
@@ -73,8 +75,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mOm, CausalParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];  // aligned to 1024 by hand below
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int MP = p.m_pad;
+    const int MP = p.m_pad;  // this CTA's features
     const int G = MP / 128;
+    // A head's features are split over the CS CTAs of a cluster: CTA `rank` owns features
+    // [rank * MP, (rank + 1) * MP). Partial numerators and denominators are summed across the
+    // cluster once per tile; CTA `rank` finalises the rows [rank * RP, (rank + 1) * RP).
+    const int CS = (int)cluster_size();
+    const int rank = (int)cluster_rank();
+    const int RP = kTile / CS;
+    const int feat0 = rank * MP;
     uint8_t* sOm = smem;                          // G regions of 128 rows x 128 B
     uint8_t* sQ = sOm + (size_t)MP * 128;
     uint8_t* sK = sQ + kTileBytes;
@@ -87,12 +96,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* sZ = reinterpret_cast<float*>(sOnes + 4096);  // [MP] z snapshot
     __shared__ uint64_t bar_om, bar_qfull, bar_kfull, bar_qkempty, bar_vfull, bar_vempty;
     __shared__ uint64_t bar_snap, bar_ufull, bar_ufree, bar_phq, bar_phk, bar_grp, bar_atil, bar_num, bar_dfree;
+    __shared__ uint64_t bar_xfree, bar_xfull;  // cluster exchange of the partial sums
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
-    __shared__ float red[kEpiWarps];
+    __shared__ float red[2][kEpiWarps];
+    __shared__ float sW[4];  // per-rank largest squared row norm of Omega
+    __shared__ float sWred[kThreads / 32];
+    __shared__ float sDen[4 * 128];
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int bh = blockIdx.x;
+    const int bh = blockIdx.x / CS;
     const int T = (p.n + kTile - 1) / kTile;
 
     if (threadIdx.x == 0) {
@@ -112,6 +125,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bar_atil, kEpiWarps);
         mbar_init(&bar_num, 1);
         mbar_init(&bar_dfree, kEpiWarps);
+        mbar_init(&bar_xfree, CS > 1 ? CS - 1 : 1);
+        mbar_init(&bar_xfull, CS > 1 ? (CS - 1) * (RP / 32) * 4 : 1);
         fence_mbar_init();
     }
     // ones block (K-major, every element 1.0): z_g = phi_g(K)^T 1 via the tensor cores
@@ -120,8 +135,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_async_smem();
     if (warp == 1) tmem_alloc(&tmem_base, 512);
     __syncthreads();
+    cluster_sync();  // every CTA's barriers are initialised before any remote arrive
     tc_fence_after();
     const uint32_t tbase = tmem_base;
+
+    // Omega rows of this CTA, then W = largest row norm of Omega over the whole cluster: the query
+    // stabiliser c_i = W |q^_i| and the key bound must be the same in every CTA of the cluster.
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&mOm);
+        mbar_arrive_expect_tx(&bar_om, (uint32_t)MP * 128);
+        for (int r0 = 0; r0 < MP; r0 += 128) tma_load_2d(sOm + (size_t)r0 * 128, &mOm, &bar_om, 0, feat0 + r0);
+    }
+    bool om_ok = mbar_wait(&bar_om, 0, &abort_flag);
+    {
+        float w2 = 0.f;
+        if (p.kind == kKindExp)
+            for (int row = threadIdx.x; row < MP; row += blockDim.x)
+                w2 = fmaxf(w2, tile_row_sqnorm<64>(sOm + (size_t)(row >> 7) * 16384, row & 127));
+        w2 = warp_max(w2);
+        if (lane == 0) sWred[warp] = w2;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float m2 = 0.f;
+            for (int i = 0; i < kThreads / 32; ++i) m2 = fmaxf(m2, sWred[i]);
+            for (int c = 0; c < CS; ++c) st_cluster_f32(mapa(smem_u32(&sW[rank]), c), m2);
+        }
+        cluster_sync();
+    }
+    float W_all = 0.f;
+    for (int c = 0; c < CS; ++c) W_all = fmaxf(W_all, sW[c]);
+    W_all = sqrtf(W_all);
+    (void)om_ok;
 
     if (warp == 0) {
         // ---------------- TMA producer (lane 0) ----------------
@@ -129,9 +173,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&mQ);
             tma_prefetch_desc(&mK);
             tma_prefetch_desc(&mV);
-            tma_prefetch_desc(&mOm);
-            mbar_arrive_expect_tx(&bar_om, (uint32_t)MP * 128);
-            for (int r0 = 0; r0 < MP; r0 += 128) tma_load_2d(sOm + (size_t)r0 * 128, &mOm, &bar_om, 0, r0);
             bool ok = true;
             for (int t = 0; t < T && ok; ++t) {
                 // Q and K of tile t once tile t-1 is projected; V of tile t once tile t-1's intra MMA is done.
@@ -146,7 +187,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // Drain the loads in flight before the CTA may exit.
             volatile int never = 0;
-            mbar_wait(&bar_om, 0, &never);
             if (T > 0) {
                 mbar_wait(&bar_qfull, (T - 1) & 1, &never);
                 mbar_wait(&bar_kfull, (T - 1) & 1, &never);
@@ -254,26 +294,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // ---------------- epilogue: thread = TMEM lane (token row for projections/scores,
-        // feature row for the state) ----------------
-        const int q = warp & 3;
+        // ---------------- epilogue: 16 warps ----------------
+        // Warp ew = warp - 2 reads TMEM lane quarter q = warp % 4 (a hardware rule) and takes column
+        // group cg = ew / 4 of every row it handles. Its lane is a token row for the projections,
+        // the scores and the numerator, and a feature row for the state.
+        constexpr int NT = 32 * kEpiWarps;
+        const int ew = warp - 2;
+        const int q = warp & 3, cg = ew >> 2;
         const int r = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         const float A2 = p.scale * kLog2e;
         const bool exp_kind = p.kind == kKindExp;
         bool failed = !mbar_wait(&bar_om, 0, &abort_flag);
         __syncwarp();
-        // W = largest row norm of Omega
-        float W = 0.f;
-        if (exp_kind) {
-            float w2 = 0.f;
-            for (int row = r; row < MP; row += 128) w2 = fmaxf(w2, tile_row_sqnorm<64>(sOm + (size_t)(row >> 7) * 16384, row & 127));
-            w2 = warp_max(w2);
-            if (lane == 0) red[q] = w2;
-            named_bar(1, 128);
-            W = sqrtf(fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])));
-            named_bar(1, 128);
-        }
+        const float W = W_all;
         float stab = 0.f;
         int guse = 0;    // feature groups whose MMAs have been committed (bar_grp phases)
         int uuse_e = 0;  // projections consumed (bar_ufull phases)
@@ -283,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             failed |= !mbar_wait(&bar_qfull, t & 1, &abort_flag);
             failed |= !mbar_wait(&bar_kfull, t & 1, &abort_flag);
             __syncwarp();
-            // norms of this thread's query and key rows
+            // norms of this row's query and key (each column group recomputes them: 64 elements)
             const float qn2 = exp_kind ? p.scale * p.scale * tile_row_sqnorm<64>(sQ, r) : 0.f;
             const float kn2 = exp_kind ? p.scale * p.scale * tile_row_sqnorm<64>(sK, r) : 0.f;
             const float cq = exp_kind ? W * sqrtf(qn2) * kLog2e : 0.f;
@@ -291,10 +325,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (exp_kind) {
                 const float b = valid ? W * sqrtf(kn2) - 0.5f * kn2 : -INFINITY;
                 const float bm = warp_max(b);
-                if (lane == 0) red[q] = bm;
-                named_bar(1, 128);
-                const float Bt = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-                named_bar(1, 128);
+                if (lane == 0) red[t & 1][ew] = bm;
+                named_bar(1, NT);
+                float Bt = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < kEpiWarps; ++i) Bt = fmaxf(Bt, red[t & 1][i]);
                 if (t == 0) {
                     stab = Bt - kStabSlackLo;
                 } else if (Bt > stab + kStabSlackHi) {
@@ -304,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             const float ck = valid ? (exp_kind ? (0.5f * kn2 + stab) * kLog2e : 0.f) : INFINITY;
-            // ---- state snapshot for this tile (thread = feature lane r of each group) ----
+            // ---- state snapshot for this tile (lane = feature r of each group; 16 columns per warp) ----
             if (t > 0) {
                 // every state MMA of the previous tile has completed once its last group committed
                 failed |= !mbar_wait(&bar_grp, (guse - 1) & 1, &abort_flag);
@@ -313,36 +348,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             for (int g = 0; g < G; ++g) {
                 const int feat = g * 128 + r;
-                uint32_t v[64];
-                float zv = 0.f;
+                uint32_t v[16];
+                const uint32_t sa = tbase + lane_off + kColS + g * 80;
                 if (t > 0) {
-                    const uint32_t sa = tbase + lane_off + kColS + g * 80;
-                    tmem_ld32(sa, *reinterpret_cast<uint32_t(*)[32]>(v));
-                    tmem_ld32(sa + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+                    tmem_ld16(sa + 16 * cg, v);
                     uint32_t zz[16];
-                    tmem_ld16(sa + 64, zz);
+                    if (cg == 0) tmem_ld16(sa + 64, zz);
                     tmem_ld_wait();
-                    zv = __uint_as_float(zz[0]);
                     if (f != 1.f) {  // the key stabiliser moved: rescale the accumulated state
 #pragma unroll
-                        for (int i = 0; i < 64; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
+                        for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
+                        tmem_st16(sa + 16 * cg, v);
+                        if (cg == 0) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) zz[i] = __float_as_uint(__uint_as_float(zz[i]) * f);
-                        zv *= f;
-                        tmem_st32(sa, *reinterpret_cast<uint32_t(*)[32]>(v));
-                        tmem_st32(sa + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-                        tmem_st16(sa + 64, zz);
+                            for (int i = 0; i < 16; ++i) zz[i] = __float_as_uint(__uint_as_float(zz[i]) * f);
+                            tmem_st16(sa + 64, zz);
+                        }
                         tmem_st_wait();
                     }
+                    if (cg == 0) sZ[feat] = feat0 + feat < p.m ? __uint_as_float(zz[0]) : 0.f;
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) v[i] = 0u;
+                    for (int i = 0; i < 16; ++i) v[i] = 0u;
+                    if (cg == 0) sZ[feat] = 0.f;
                 }
-                if (feat >= p.m) zv = 0.f;
-                // bf16 snapshot row `feat` as hi + lo (about 16 significant bits): 64 values each,
-                // 8 swizzled 16-byte chunks
+                // bf16 snapshot of S row `feat`, columns [16 cg, 16 cg + 16), as hi + lo
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
+                for (int c = 0; c < 2; ++c) {
                     float x[8], l[8];
 #pragma unroll
                     for (int k = 0; k < 8; ++k) x[k] = __uint_as_float(v[8 * c + k]);
@@ -362,18 +394,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ol.y = pack_bf16(l[2], l[3]);
                     ol.z = pack_bf16(l[4], l[5]);
                     ol.w = pack_bf16(l[6], l[7]);
-                    *reinterpret_cast<uint4*>(sS + sw128_offset(feat, c)) = o;
-                    *reinterpret_cast<uint4*>(sSl + sw128_offset(feat, c)) = ol;
+                    *reinterpret_cast<uint4*>(sS + sw128_offset(feat, 2 * cg + c)) = o;
+                    *reinterpret_cast<uint4*>(sSl + sw128_offset(feat, 2 * cg + c)) = ol;
                 }
-                sZ[feat] = zv;
             }
             tc_fence_before();
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_snap);
-            named_bar(1, 128);  // z snapshot visible to every epilogue thread
-            // ---- per feature group: phi(Q), phi(K) into shared memory ----
-            float den_inter = 0.f;
+            named_bar(1, NT);  // z snapshot visible to every epilogue thread
+            // ---- per feature group: phi(Q), phi(K) into shared memory (32 features per warp) ----
+            float den = 0.f;  // this warp's share of the row's denominator
             for (int g = 0; g < G; ++g) {
                 if (g > 0) {  // the previous group's MMAs have read the phi buffers
                     failed |= !mbar_wait(&bar_grp, (guse - 1) & 1, &abort_flag);
@@ -384,48 +415,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     tc_fence_after();
                     ++uuse_e;
+                    uint32_t v[32];
+                    tmem_ld32(tbase + lane_off + kColU + 32 * cg, v);
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar_ufree);  // U has been read: the next projection may overwrite it
                     uint8_t* dst = which == 0 ? sPQ : sPK;
                     const float cst = which == 0 ? cq : ck;
                     const bool zero_row = which == 1 && !valid;
-                    for (int h = 0; h < 2; ++h) {  // 64 features at a time
-                        uint32_t v[64];
-                        tmem_ld32(tbase + lane_off + kColU + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(v));
-                        tmem_ld32(tbase + lane_off + kColU + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-                        tmem_ld_wait();
-                        if (h == 1) {  // U has been read: the next projection may overwrite it
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(&bar_ufree);
+                    const int f0 = g * 128 + 32 * cg;  // this CTA's feature index
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        float ph[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const float a = __uint_as_float(v[8 * c + k]);
+                            float x = exp_kind ? ex2(fmaf(a, A2, -cst)) : fmaxf(a * p.scale, 0.f) + p.relu_eps_s;
+                            if (zero_row || feat0 + f0 + 8 * c + k >= p.m) x = 0.f;
+                            ph[k] = x;
                         }
-                        const int f0 = g * 128 + 64 * h;
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            float ph[8];
-#pragma unroll
-                            for (int k = 0; k < 8; ++k) {
-                                const float a = __uint_as_float(v[8 * c + k]);
-                                float x = exp_kind ? ex2(fmaf(a, A2, -cst)) : fmaxf(a * p.scale, 0.f) + p.relu_eps_s;
-                                if (zero_row || f0 + 8 * c + k >= p.m) x = 0.f;
-                                ph[k] = x;
-                            }
-                            uint4 o;
-                            o.x = pack_bf16(ph[0], ph[1]);
-                            o.y = pack_bf16(ph[2], ph[3]);
-                            o.z = pack_bf16(ph[4], ph[5]);
-                            o.w = pack_bf16(ph[6], ph[7]);
-                            *reinterpret_cast<uint4*>(dst + h * 16384 + sw128_offset(r, c)) = o;
-                            if (which == 0) {  // den: phi(q) . z_<t with the bf16-rounded features
-                                const float4 za = *reinterpret_cast<const float4*>(sZ + f0 + 8 * c);
-                                const float4 zb = *reinterpret_cast<const float4*>(sZ + f0 + 8 * c + 4);
-                                den_inter = fmaf(__uint_as_float(o.x << 16), za.x, den_inter);
-                                den_inter = fmaf(__uint_as_float(o.x & 0xFFFF0000u), za.y, den_inter);
-                                den_inter = fmaf(__uint_as_float(o.y << 16), za.z, den_inter);
-                                den_inter = fmaf(__uint_as_float(o.y & 0xFFFF0000u), za.w, den_inter);
-                                den_inter = fmaf(__uint_as_float(o.z << 16), zb.x, den_inter);
-                                den_inter = fmaf(__uint_as_float(o.z & 0xFFFF0000u), zb.y, den_inter);
-                                den_inter = fmaf(__uint_as_float(o.w << 16), zb.z, den_inter);
-                                den_inter = fmaf(__uint_as_float(o.w & 0xFFFF0000u), zb.w, den_inter);
-                            }
+                        uint4 o;
+                        o.x = pack_bf16(ph[0], ph[1]);
+                        o.y = pack_bf16(ph[2], ph[3]);
+                        o.z = pack_bf16(ph[4], ph[5]);
+                        o.w = pack_bf16(ph[6], ph[7]);
+                        *reinterpret_cast<uint4*>(dst + (cg >> 1) * 16384 + sw128_offset(r, (cg & 1) * 4 + c)) = o;
+                        if (which == 0) {  // den: phi(q) . z_<t with the bf16-rounded features
+                            const float4 za = *reinterpret_cast<const float4*>(sZ + f0 + 8 * c);
+                            const float4 zb = *reinterpret_cast<const float4*>(sZ + f0 + 8 * c + 4);
+                            den = fmaf(__uint_as_float(o.x << 16), za.x, den);
+                            den = fmaf(__uint_as_float(o.x & 0xFFFF0000u), za.y, den);
+                            den = fmaf(__uint_as_float(o.y << 16), za.z, den);
+                            den = fmaf(__uint_as_float(o.y & 0xFFFF0000u), za.w, den);
+                            den = fmaf(__uint_as_float(o.z << 16), zb.x, den);
+                            den = fmaf(__uint_as_float(o.z & 0xFFFF0000u), zb.y, den);
+                            den = fmaf(__uint_as_float(o.w << 16), zb.z, den);
+                            den = fmaf(__uint_as_float(o.w & 0xFFFF0000u), zb.w, den);
                         }
                     }
                     fence_async_smem();
@@ -434,23 +460,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ++guse;
             }
-            // ---- masked scores -> A~ (bf16, in the phi(K) buffer), den_intra ----
+            // ---- masked scores (keys [32 cg, 32 cg + 32) of row r) -> A~ hi (phi(K) buffer), lo (phi(Q) buffer) ----
             failed |= !mbar_wait(&bar_grp, (guse - 1) & 1, &abort_flag);
             __syncwarp();
             tc_fence_after();
-            float den_intra = 0.f;
-            for (int h = 0; h < 2; ++h) {  // keys 64h .. 64h + 63
-                uint32_t v[64];
-                tmem_ld32(tbase + lane_off + kColSc + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(v));
-                tmem_ld32(tbase + lane_off + kColSc + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+            {
+                uint32_t v[32];
+                tmem_ld32(tbase + lane_off + kColSc + 32 * cg, v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
+                for (int c = 0; c < 4; ++c) {
                     float a[8];
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        a[k] = (64 * h + 8 * c + k <= r) ? __uint_as_float(v[8 * c + k]) : 0.f;
-                        den_intra += a[k];
+                        a[k] = (32 * cg + 8 * c + k <= r) ? __uint_as_float(v[8 * c + k]) : 0.f;
+                        den += a[k];
                     }
                     // A~ = hi + lo, both bf16: the intra-tile weights keep about 16 significant bits.
                     uint4 o, ol;
@@ -462,37 +486,87 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ol.y = pack_bf16(a[2] - __uint_as_float(o.y << 16), a[3] - __uint_as_float(o.y & 0xFFFF0000u));
                     ol.z = pack_bf16(a[4] - __uint_as_float(o.z << 16), a[5] - __uint_as_float(o.z & 0xFFFF0000u));
                     ol.w = pack_bf16(a[6] - __uint_as_float(o.w << 16), a[7] - __uint_as_float(o.w & 0xFFFF0000u));
-                    *reinterpret_cast<uint4*>(sPK + h * 16384 + sw128_offset(r, c)) = o;
-                    *reinterpret_cast<uint4*>(sPQ + h * 16384 + sw128_offset(r, c)) = ol;
+                    const uint32_t off = (cg >> 1) * 16384 + sw128_offset(r, (cg & 1) * 4 + c);
+                    *reinterpret_cast<uint4*>(sPK + off) = o;
+                    *reinterpret_cast<uint4*>(sPQ + off) = ol;
                 }
             }
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_atil);
-            // ---- y = num / den ----
+            sDen[cg * 128 + r] = den;
+            named_bar(1, NT);  // denominator shares visible
+            const float den_row = ((sDen[r] + sDen[128 + r]) + sDen[256 + r]) + sDen[384 + r];
+            // ---- y = num / den, output columns [16 cg, 16 cg + 16) ----
             failed |= !mbar_wait(&bar_num, t & 1, &abort_flag);
             __syncwarp();
             tc_fence_after();
-            {
-                uint32_t v[64];
-                tmem_ld32(tbase + lane_off + kColNum, *reinterpret_cast<uint32_t(*)[32]>(v));
-                tmem_ld32(tbase + lane_off + kColNum + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-                tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar_dfree);
-                const float inv = 1.f / (den_inter + den_intra);
-                if (valid) {
-                    uint4* dst = reinterpret_cast<uint4*>(p.Y + ((size_t)bh * p.n + i_tok) * kD);
+            uint32_t v[16];
+            tmem_ld16(tbase + lane_off + kColNum + 16 * cg, v);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_dfree);
+            float num[16];
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        uint4 o;
-                        o.x = pack_bf16(__uint_as_float(v[8 * c + 0]) * inv, __uint_as_float(v[8 * c + 1]) * inv);
-                        o.y = pack_bf16(__uint_as_float(v[8 * c + 2]) * inv, __uint_as_float(v[8 * c + 3]) * inv);
-                        o.z = pack_bf16(__uint_as_float(v[8 * c + 4]) * inv, __uint_as_float(v[8 * c + 5]) * inv);
-                        o.w = pack_bf16(__uint_as_float(v[8 * c + 6]) * inv, __uint_as_float(v[8 * c + 7]) * inv);
-                        dst[c] = o;
+            for (int i = 0; i < 16; ++i) num[i] = __uint_as_float(v[i]);
+            float dsum = den_row;
+            const int owner = r / RP;
+            if (CS > 1) {
+                // Partial sums of row r go to the CTA that finalises it, through its phi(Q) buffer
+                // (idle once this tile's intra MMA is done): slot [sender][row][80 floats].
+                if (ew == 0 && lane == 0)
+                    for (int c = 0; c < CS; ++c)
+                        if (c != rank) mbar_arrive_cluster(mapa(smem_u32(&bar_xfree), c));
+                if (owner != rank) {
+                    failed |= !mbar_wait_cluster(&bar_xfree, t & 1, &abort_flag);
+                    __syncwarp();
+                    const int slot = rank < owner ? rank : rank - 1;
+                    float* dstp = reinterpret_cast<float*>(sPQ) + ((size_t)slot * RP + (r - owner * RP)) * 80 + 16 * cg;
+                    const uint32_t ca = mapa(smem_u32(dstp), owner);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        st_cluster_v4(ca + 16 * c, make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]));
+                    if (cg == 0) st_cluster_f32(mapa(smem_u32(reinterpret_cast<float*>(sPQ) + ((size_t)slot * RP + (r - owner * RP)) * 80 + 64), owner), den_row);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(mapa(smem_u32(&bar_xfull), owner));
+                } else {
+                    failed |= !mbar_wait_cluster(&bar_xfull, t & 1, &abort_flag);
+                    __syncwarp();
+                    // sum the cluster's contributions in rank order (deterministic)
+                    float acc[16];
+                    float dacc = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+                    for (int c = 0; c < CS; ++c) {
+                        if (c == rank) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) acc[i] += num[i];
+                            dacc += den_row;
+                        } else {
+                            const int slot = c < rank ? c : c - 1;
+                            const float* src = reinterpret_cast<const float*>(sPQ) + ((size_t)slot * RP + (r - rank * RP)) * 80;
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) acc[i] += src[16 * cg + i];
+                            dacc += src[64];
+                        }
                     }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) num[i] = acc[i];
+                    dsum = dacc;
+                }
+            }
+            if (valid && owner == rank) {
+                const float inv = 1.f / dsum;
+                uint4* dst = reinterpret_cast<uint4*>(p.Y + ((size_t)bh * p.n + i_tok) * kD + 16 * cg);
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint4 o;
+                    o.x = pack_bf16(num[8 * c + 0] * inv, num[8 * c + 1] * inv);
+                    o.y = pack_bf16(num[8 * c + 2] * inv, num[8 * c + 3] * inv);
+                    o.z = pack_bf16(num[8 * c + 4] * inv, num[8 * c + 5] * inv);
+                    o.w = pack_bf16(num[8 * c + 6] * inv, num[8 * c + 7] * inv);
+                    dst[c] = o;
                 }
             }
         }
@@ -504,6 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tbase, 512);
     }
+    cluster_sync();  // no CTA leaves while a peer may still write into its shared memory
 }
 
 }  // namespace tcc
