@@ -14,6 +14,7 @@
 #include "simt_kernels.cuh"
 #include "tc_noncausal.cuh"
 #include "tc_causal.cuh"
+#include "tc_features.cuh"
 #include "tma_host.h"
 
 namespace favor {
@@ -317,19 +318,38 @@ favor_status_t tc_noncausal(const void* Q, const void* K, const void* V, const v
     FAVOR_TRY(traced(FAVOR_KERNEL_STATE, s, [&] {
         kstate<<<dim3(w.splits, BH, 1), tcnc::kStateThreads, smem_state, s>>>(mK, mV, mOm, sp);
     }));
+    // The combine and the readout are launched with programmatic stream serialisation: each may
+    // start (and run its independent prologue) while its predecessor finishes, and waits for it with
+    // griddepcontrol.wait before reading its output.
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
     const int rows_per_block = 128 / (D / 8);
+    cudaLaunchConfig_t cc = {};
+    cc.gridDim = dim3(w.m_pad / rows_per_block, BH, 1);
+    cc.blockDim = dim3(128, 1, 1);
+    cc.stream = s;
+    cc.attrs = pdl;
+    cc.numAttrs = 1;
+    cudaError_t lerr = cudaSuccess;
     FAVOR_TRY(traced(FAVOR_KERNEL_COMBINE, s, [&] {
-        tcnc::nc_combine<D><<<dim3(w.m_pad / rows_per_block, BH), 128, 0, s>>>(pS, pz, pst, w.splits, 1, m, w.m_pad,
-                                                                                w.m_pad, img, zf);
+        lerr = cudaLaunchKernelEx(&cc, tcnc::nc_combine<D>, (const float*)pS, (const float*)pz, (const float*)pst,
+                                  w.splits, 1, m, w.m_pad, w.m_pad, img, zf);
     }));
+    if (lerr != cudaSuccess) return FAVOR_ERR_CUDA;
     tcnc::ReadoutParams rp{n, w.m_pad, m, w.tiles_per_cta, kind, eps_s, sc, img, zf, static_cast<__nv_bfloat16*>(Y)};
     const size_t smem_read = tcnc::ReadoutSmem<D>::bytes(w.m_pad);
     auto kread = tcnc::nc_readout_tc<D>;
     FAVOR_TRY(set_smem(kread, smem_read));
-    FAVOR_TRY(traced(FAVOR_KERNEL_READOUT, s, [&] {
-        kread<<<dim3(w.chunks, BH), tcnc::kThreads, smem_read, s>>>(mQ, mOm, rp);
-    }));
-    return FAVOR_OK;
+    cudaLaunchConfig_t rc = {};
+    rc.gridDim = dim3(w.chunks, BH, 1);
+    rc.blockDim = dim3(tcnc::kThreads, 1, 1);
+    rc.dynamicSmemBytes = smem_read;
+    rc.stream = s;
+    rc.attrs = pdl;
+    rc.numAttrs = 1;
+    FAVOR_TRY(traced(FAVOR_KERNEL_READOUT, s, [&] { lerr = cudaLaunchKernelEx(&rc, kread, mQ, mOm, rp); }));
+    return lerr == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;
 }
 
 favor_status_t tc_causal(const void* Q, const void* K, const void* V, const void* Om, void* Y, int B, int H, int n,
@@ -360,6 +380,37 @@ favor_status_t tc_causal(const void* Q, const void* K, const void* V, const void
     cudaError_t lerr = cudaSuccess;
     FAVOR_TRY(traced(FAVOR_KERNEL_CAUSAL, s, [&] { lerr = cudaLaunchKernelEx(&cfg, tcc::causal_tc, mQ, mK, mV, mOm, cp); }));
     return lerr == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;
+}
+
+template <int D>
+favor_status_t tc_features(const void* X, const void* Om, float* Phi, int B, int H, int n, int m, int kind, float eps,
+                           int stab, void* ws, cudaStream_t s) {
+    const int BH = B * H;
+    CUtensorMap mX, mOm;
+    if (!tma::encode_bf16_3d(&mX, X, D, n, BH, 64, tcf::kTile) || !tma::encode_bf16_2d(&mOm, Om, D, m, 64, 128))
+        return FAVOR_ERR_CUDA;
+    const int m_pad = m_padded(m);
+    const int tiles = (n + tcf::kTile - 1) / tcf::kTile;
+    const int chunks = std::max(1, std::min(tiles, (kNumSMs + BH - 1) / std::max(BH, 1)));
+    const int tpc = (tiles + chunks - 1) / chunks;
+    const int grid_x = (tiles + tpc - 1) / tpc;
+    unsigned* head_max = static_cast<unsigned*>(ws);
+    tcf::FeatParams fp{n, m, m_pad, tpc, kind, stab, 0, eps, qk_scale(D), Phi, head_max};
+    const size_t smem = tcf::FeatSmem<D>::bytes(m_pad);
+    auto kern = tcf::features_tc<D>;
+    FAVOR_TRY(set_smem(kern, smem));
+    if (kind == kKindExp && stab == kStabHead) {
+        if (cudaMemsetAsync(head_max, 0, sizeof(unsigned) * BH, s) != cudaSuccess) return FAVOR_ERR_CUDA;
+        tcf::FeatParams fm = fp;
+        fm.max_only = 1;
+        FAVOR_TRY(traced(FAVOR_KERNEL_FEATURES_HEAD, s, [&] {
+            kern<<<dim3(grid_x, BH), tcf::kThreads, smem, s>>>(mX, mOm, fm);
+        }));
+    }
+    FAVOR_TRY(traced(FAVOR_KERNEL_FEATURES, s, [&] {
+        kern<<<dim3(grid_x, BH), tcf::kThreads, smem, s>>>(mX, mOm, fp);
+    }));
+    return FAVOR_OK;
 }
 
 // dtype x d dispatch
@@ -445,6 +496,9 @@ favor_status_t favor_features(const void* X, const void* Omega, float* Phi, int 
     if (!aligned(X, 16) || !aligned(Omega, 16) || !aligned(Phi, 16)) return FAVOR_ERR_MISALIGNED;
     FAVOR_TRY(check_ws(workspace, ws_bytes, features_ws_bytes(B, H, kind, stab)));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dt == FAVOR_BF16)
+        return d == 64 ? tc_features<64>(X, Omega, Phi, B, H, n, m, (int)kind, relu_eps, (int)stab, workspace, s)
+                       : tc_features<128>(X, Omega, Phi, B, H, n, m, (int)kind, relu_eps, (int)stab, workspace, s);
     return FAVOR_DISPATCH(dt, d, simt_features, X, Omega, Phi, B, H, n, m, (int)kind, relu_eps, (int)stab, workspace,
                           s);
 }

@@ -157,6 +157,15 @@ __device__ __forceinline__ void cluster_sync() {
 }
 
 // ---------------------------------------------------------------------------------------------
+// Programmatic dependent launch: a kernel launched with programmatic stream serialisation may start
+// before its predecessor ends; griddep_wait() blocks the calling thread until the predecessor grid
+// has completed and its memory is visible (a no-op without that launch attribute), and
+// griddep_launch() lets the successor start launching early.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor), tensor maps passed as __grid_constant__ kernel parameters
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

@@ -43,6 +43,7 @@ constexpr int kEpiWarps = 16;  // four column groups x four TMEM lane quarters
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kTileBytes = kTile * kD * 2;  // 16 KB: one [128 x 64] bf16 tile
 constexpr int kPhiBytes = kTile * 128 * 2;  // 32 KB: [128 tokens x 128 features] bf16, two K atoms
+constexpr int kXStride = 84;                // floats per row of the cluster exchange buffer (64 + den + pad)
 
 // TMEM columns
 constexpr uint32_t kColS = 0;      // S_g at g * 80: 64 columns of S, 16 of z (all equal)
@@ -514,7 +515,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int owner = r / RP;
             if (CS > 1) {
                 // Partial sums of row r go to the CTA that finalises it, through its phi(Q) buffer
-                // (idle once this tile's intra MMA is done): slot [sender][row][80 floats].
+                // (idle once this tile's intra MMA is done): slot [sender][row][kXStride floats]; the odd
+                // number of 16-byte groups per row keeps a warp's float4 accesses free of bank conflicts.
                 if (ew == 0 && lane == 0)
                     for (int c = 0; c < CS; ++c)
                         if (c != rank) mbar_arrive_cluster(mapa(smem_u32(&bar_xfree), c));
@@ -522,12 +524,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     failed |= !mbar_wait_cluster(&bar_xfree, t & 1, &abort_flag);
                     __syncwarp();
                     const int slot = rank < owner ? rank : rank - 1;
-                    float* dstp = reinterpret_cast<float*>(sPQ) + ((size_t)slot * RP + (r - owner * RP)) * 80 + 16 * cg;
+                    float* dstp = reinterpret_cast<float*>(sPQ) + ((size_t)slot * RP + (r - owner * RP)) * kXStride + 16 * cg;
                     const uint32_t ca = mapa(smem_u32(dstp), owner);
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
                         st_cluster_v4(ca + 16 * c, make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]));
-                    if (cg == 0) st_cluster_f32(mapa(smem_u32(reinterpret_cast<float*>(sPQ) + ((size_t)slot * RP + (r - owner * RP)) * 80 + 64), owner), den_row);
+                    if (cg == 0) st_cluster_f32(mapa(smem_u32(reinterpret_cast<float*>(sPQ) + ((size_t)slot * RP + (r - owner * RP)) * kXStride + 64), owner), den_row);
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(mapa(smem_u32(&bar_xfull), owner));
                 } else {
@@ -545,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             dacc += den_row;
                         } else {
                             const int slot = c < rank ? c : c - 1;
-                            const float* src = reinterpret_cast<const float*>(sPQ) + ((size_t)slot * RP + (r - rank * RP)) * 80;
+                            const float* src = reinterpret_cast<const float*>(sPQ) + ((size_t)slot * RP + (r - rank * RP)) * kXStride;
 #pragma unroll
                             for (int i = 0; i < 16; ++i) acc[i] += src[16 * cg + i];
                             dacc += src[64];

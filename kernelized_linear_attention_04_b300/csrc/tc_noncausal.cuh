@@ -175,6 +175,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     if (warp == 1) tmem_alloc(&tmem_base, 512);
     __syncthreads();
     tc_fence_after();
+    if (threadIdx.x == 0) griddep_launch();  // the combine may be scheduled now; it waits for this grid
     const uint32_t tbase = tmem_base;
     // TMEM: S_g at columns [g*D, (g+1)*D); two 128-column U slots from column 256.
     auto u_col = [](int s) { return 256u + 128u * (uint32_t)s; };
@@ -511,12 +512,23 @@ __global__ void __launch_bounds__(128) nc_combine(const float* __restrict__ pS, 
                                                   float* __restrict__ zout) {
     constexpr int kChunks = D / 8;  // 16-byte bf16 chunks per row
     __shared__ float wts[1024];
+    __shared__ float red[4];
+    griddep_launch();  // the readout may start its prologue; it waits for this grid before reading S
+    griddep_wait();    // the key-side partial states are complete
     const int bh = blockIdx.y;
     const int nst = splits * fslices;
     const float* st = pstab + (size_t)bh * nst;
+    // stabilisers: loaded in parallel, reduced, turned into weights exp(stab_s - max)
     float M = -INFINITY;
-    for (int i = 0; i < nst; ++i) M = fmaxf(M, st[i]);
-    for (int i = threadIdx.x; i < nst; i += blockDim.x) wts[i] = ex2((st[i] - M) * kLog2e);
+    for (int i = threadIdx.x; i < nst; i += blockDim.x) {
+        wts[i] = st[i];
+        M = fmaxf(M, wts[i]);
+    }
+    M = warp_max(M);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = M;
+    __syncthreads();
+    M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    for (int i = threadIdx.x; i < nst; i += blockDim.x) wts[i] = ex2((wts[i] - M) * kLog2e);
     __syncthreads();
     const int rows_per_block = 128 / kChunks;  // D=64: 16 rows, D=128: 8 rows
     const int row = blockIdx.x * rows_per_block + threadIdx.x / kChunks;
@@ -525,16 +537,30 @@ __global__ void __launch_bounds__(128) nc_combine(const float* __restrict__ pS, 
     const int fs = row / feats_per_slice;
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     float zs = 0.f;
-    for (int s = 0; s < splits; ++s) {
-        const float w = wts[s * fslices + fs];
-        const float* src = pS + (((size_t)bh * splits + s) * m_pad + row) * D + ch * 8;
-        const float4 a = *reinterpret_cast<const float4*>(src);
-        const float4 b = *reinterpret_cast<const float4*>(src + 4);
-        acc[0] = fmaf(w, a.x, acc[0]); acc[1] = fmaf(w, a.y, acc[1]);
-        acc[2] = fmaf(w, a.z, acc[2]); acc[3] = fmaf(w, a.w, acc[3]);
-        acc[4] = fmaf(w, b.x, acc[4]); acc[5] = fmaf(w, b.y, acc[5]);
-        acc[6] = fmaf(w, b.z, acc[6]); acc[7] = fmaf(w, b.w, acc[7]);
-        if (ch == 0) zs = fmaf(w, pz[((size_t)bh * splits + s) * m_pad + row], zs);
+    // Splits in a fixed order, eight at a time with their loads issued together.
+    for (int s0 = 0; s0 < splits; s0 += 8) {
+        float4 a[8], b[8];
+        float zp[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (s0 + k < splits) {
+                const float* src = pS + (((size_t)bh * splits + s0 + k) * m_pad + row) * D + ch * 8;
+                a[k] = *reinterpret_cast<const float4*>(src);
+                b[k] = *reinterpret_cast<const float4*>(src + 4);
+                zp[k] = ch == 0 ? pz[((size_t)bh * splits + s0 + k) * m_pad + row] : 0.f;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (s0 + k < splits) {
+                const float w = wts[(s0 + k) * fslices + fs];
+                acc[0] = fmaf(w, a[k].x, acc[0]); acc[1] = fmaf(w, a[k].y, acc[1]);
+                acc[2] = fmaf(w, a[k].z, acc[2]); acc[3] = fmaf(w, a[k].w, acc[3]);
+                acc[4] = fmaf(w, b[k].x, acc[4]); acc[5] = fmaf(w, b[k].y, acc[5]);
+                acc[6] = fmaf(w, b[k].z, acc[6]); acc[7] = fmaf(w, b[k].w, acc[7]);
+                zs = fmaf(w, zp[k], zs);
+            }
+        }
     }
     if (row >= m) {  // padding features: no contribution to the readout
 #pragma unroll
@@ -590,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* sz = reinterpret_cast<float*>(sQ + (size_t)NS * SM::kTileBytes);  // [MP]
     float* sMax = sz + MP;                                 // [2][4][128] row-max partials
     float* sDen = sMax + 2 * 4 * 128;                      // [2][4][128] denominator partials
-    __shared__ uint64_t bar_full[NS], bar_empty[NS], bar_const, bar_ufull[2], bar_ufree[2], bar_phi[2], bar_num[2];
+    __shared__ uint64_t bar_full[NS], bar_empty[NS], bar_const, bar_sz, bar_ufull[2], bar_ufree[2], bar_phi[2], bar_num[2];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
 
@@ -620,6 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bar_empty[i], 1);
         }
         mbar_init(&bar_const, 1);
+        mbar_init(&bar_sz, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar_ufull[i], 1);
             mbar_init(&bar_ufree[i], kEpiWarps);
@@ -638,14 +665,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&mQ);
             tma_prefetch_desc(&mOm);
             const uint32_t sbytes = (uint32_t)MP * D * 2;
-            mbar_arrive_expect_tx(&bar_const, sbytes * 2 + (uint32_t)MP * 4);
+            mbar_arrive_expect_tx(&bar_const, sbytes);
             for (int a = 0; a < kAtoms; ++a)
                 for (int r0 = 0; r0 < MP; r0 += 128)
                     tma_load_2d(sOm + (size_t)a * MP * 128 + r0 * 128, &mOm, &bar_const, a * 64, r0);
-            bulk_load(sS, p.Simg + (size_t)bh * sbytes, sbytes, &bar_const);
-            bulk_load(sz, p.z + (size_t)bh * MP, (uint32_t)MP * 4, &bar_const);
+            // The first query tiles do not depend on the preceding kernels: load them before waiting.
             int issued = 0;
-            for (int t = 0; t < T; ++t) {
+            for (int t = 0; t < min(T, NS); ++t) {
+                mbar_arrive_expect_tx(&bar_full[t], SM::kTileBytes);
+                for (int a = 0; a < kAtoms; ++a)
+                    tma_load_3d(sQ + (size_t)t * SM::kTileBytes + a * 16384, &mQ, &bar_full[t], a * 64,
+                                (t0 + t) * kTile, bh);
+                issued = t + 1;
+            }
+            griddep_wait();  // the combined state image and z are complete
+            mbar_arrive_expect_tx(&bar_sz, sbytes + (uint32_t)MP * 4);
+            bulk_load(sS, p.Simg + (size_t)bh * sbytes, sbytes, &bar_sz);
+            bulk_load(sz, p.z + (size_t)bh * MP, (uint32_t)MP * 4, &bar_sz);
+            for (int t = issued; t < T; ++t) {
                 const int st = t % NS;
                 if (!mbar_wait(&bar_empty[st], ((t / NS) & 1) ^ 1, &abort_flag)) break;
                 mbar_arrive_expect_tx(&bar_full[st], SM::kTileBytes);
@@ -660,6 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             volatile int never = 0;
             mbar_wait(&bar_const, 0, &never);
+            mbar_wait(&bar_sz, 0, &never);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -690,8 +728,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&bar_empty[st]);
                 return true;
             };
+            bool have_sz = false;
             auto issue_out = [&](int t) -> bool {
                 const int s = t % nslot, k = t / nslot;
+                if (!have_sz && !(have_sz = mbar_wait(&bar_sz, 0, &abort_flag))) return false;
                 if (!mbar_wait(&bar_phi[s], k & 1, &abort_flag)) return false;
                 tc_fence_after();
                 for (int ks = 0; ks < MP / 16; ++ks) {
@@ -727,6 +767,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool exp_kind = p.kind == kKindExp;
         bool failed = !mbar_wait(&bar_const, 0, &abort_flag);
         __syncwarp();
+        bool have_sz = false;
 
         // phi for 32 raw projections, row constant cst; den accumulates bf16(phi) * z.
         auto features32 = [&](uint32_t (&v)[32], const float* zr, float cst, uint32_t (&pk)[16], float& dsum) {
@@ -773,6 +814,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mx[cg * 128 + r] = rmax;
                 named_bar(1, kEpiThreads);  // every warp has its U values: U may now be overwritten
                 rmax = fmaxf(fmaxf(mx[r], mx[128 + r]), fmaxf(mx[256 + r], mx[384 + r]));
+                if (!have_sz) {  // z (from the preceding kernels) is needed from here on
+                    have_sz = mbar_wait(&bar_sz, 0, &abort_flag);
+                    __syncwarp();
+                }
                 const float cst = exp_kind ? A2 * rmax : 0.f;
                 uint32_t pk[16];
                 features32(v0, sz + cg * Wf, cst, pk, dsum);
@@ -794,6 +839,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mx[cg * 128 + r] = rmax;
                 named_bar(1, kEpiThreads);
                 rmax = fmaxf(fmaxf(mx[r], mx[128 + r]), fmaxf(mx[256 + r], mx[384 + r]));
+                if (!have_sz) {
+                    have_sz = mbar_wait(&bar_sz, 0, &abort_flag);
+                    __syncwarp();
+                }
                 const float cst = exp_kind ? A2 * rmax : 0.f;
                 for (int c0 = 0; c0 < Wf; c0 += 32) {
                     uint32_t v[32], pk[16];
