@@ -80,7 +80,7 @@ def kernel_work(w, kernel: str) -> tuple[float, float]:
         return 4.0 * md * T, 2.0 * w.d * s * T + om
     if kernel == "readout":      # project Q, contract with S, divide; reads Q, writes Y
         return 4.0 * md * T, 2.0 * w.d * s * T + om
-    if kernel == "causal":       # the whole causal path in one kernel
+    if kernel in ("causal", "fused"):  # the whole path in one kernel
         return 8.0 * md * T, 4.0 * w.d * s * T + om
     if kernel == "combine":      # partial states -> one state per head
         return 0.0, 0.0

@@ -155,7 +155,8 @@ typedef enum {
     FAVOR_KERNEL_COMBINE = 3,       /* non-causal combine of the partial states              */
     FAVOR_KERNEL_READOUT = 4,       /* non-causal query-side readout and divide              */
     FAVOR_KERNEL_CAUSAL = 5,        /* causal chunked scan                                    */
-    FAVOR_KERNEL_COUNT = 6
+    FAVOR_KERNEL_FUSED = 6,         /* single-launch non-causal path for short sequences      */
+    FAVOR_KERNEL_COUNT = 7
 } favor_kernel_id_t;
 
 /* Starts (on != 0) or stops recording. Starting clears previous records. While recording, every

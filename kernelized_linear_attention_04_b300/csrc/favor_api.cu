@@ -15,6 +15,7 @@
 #include "tc_noncausal.cuh"
 #include "tc_causal.cuh"
 #include "tc_features.cuh"
+#include "tc_fused.cuh"
 #include "tma_host.h"
 
 namespace favor {
@@ -292,6 +293,40 @@ favor_status_t simt_causal(const void* Q, const void* K, const void* V, const vo
     return FAVOR_OK;
 }
 
+// Short sequences (one cluster of at most 8 tiles per head) run as a single fused launch.
+bool tc_fused_ok(int n, int d, int m, favor_dtype_t dt) {
+    return dt == FAVOR_BF16 && d == 64 && m_padded(m) <= 256 && n >= 1 && n <= tcfu::kMaxCluster * tcfu::kTile;
+}
+
+favor_status_t tc_fused(const void* Q, const void* K, const void* V, const void* Om, void* Y, int B, int H, int n, int m,
+                        int kind, float eps, cudaStream_t s) {
+    const int BH = B * H;
+    CUtensorMap mQ, mK, mV, mOm;
+    if (!tma::encode_bf16_3d(&mQ, Q, 64, n, BH, 64, tcfu::kTile) || !tma::encode_bf16_3d(&mK, K, 64, n, BH, 64, tcfu::kTile) ||
+        !tma::encode_bf16_3d(&mV, V, 64, n, BH, 64, tcfu::kTile) || !tma::encode_bf16_2d(&mOm, Om, 64, m, 64, 128))
+        return FAVOR_ERR_CUDA;
+    const int m_pad = m_padded(m);
+    const int T = (n + tcfu::kTile - 1) / tcfu::kTile;
+    tcfu::FusedParams fp{n, m, m_pad, kind, eps * std::sqrt((float)m), qk_scale(64), static_cast<__nv_bfloat16*>(Y)};
+    const size_t smem = tcfu::FusedSmem::bytes(m_pad);
+    FAVOR_TRY(set_smem(tcfu::nc_fused_small, smem));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(BH * T, 1, 1);
+    cfg.blockDim = dim3(tcfu::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = T;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t lerr = cudaSuccess;
+    FAVOR_TRY(traced(FAVOR_KERNEL_FUSED, s, [&] { lerr = cudaLaunchKernelEx(&cfg, tcfu::nc_fused_small, mQ, mK, mV, mOm, fp); }));
+    return lerr == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;
+}
+
 template <int D>
 favor_status_t tc_noncausal(const void* Q, const void* K, const void* V, const void* Om, void* Y, int B, int H, int n,
                             int m, int kind, float eps, void* ws, cudaStream_t s) {
@@ -467,6 +502,7 @@ const char* favor_kernel_name(int kid) {
         case FAVOR_KERNEL_COMBINE: return "combine";
         case FAVOR_KERNEL_READOUT: return "readout";
         case FAVOR_KERNEL_CAUSAL: return "causal";
+        case FAVOR_KERNEL_FUSED: return "fused";
     }
     return "unknown";
 }
@@ -510,6 +546,7 @@ favor_status_t favor_attn_noncausal(const void* Q, const void* K, const void* V,
     if ((int64_t)B * H * n == 0) return FAVOR_OK;
     FAVOR_TRY(check_ws(workspace, ws_bytes, noncausal_ws_bytes(B, H, n, d, m, dt)));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (tc_fused_ok(n, d, m, dt)) return tc_fused(Q, K, V, Omega, Y, B, H, n, m, (int)kind, relu_eps, s);
     if (tc_noncausal_ok(d, m, dt))
         return d == 64 ? tc_noncausal<64>(Q, K, V, Omega, Y, B, H, n, m, (int)kind, relu_eps, workspace, s)
                        : tc_noncausal<128>(Q, K, V, Omega, Y, B, H, n, m, (int)kind, relu_eps, workspace, s);

@@ -142,6 +142,14 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t caddr, uint4 v) {
 __device__ __forceinline__ void st_cluster_f32(uint32_t caddr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(caddr), "f"(v) : "memory");
 }
+__device__ __forceinline__ uint4 ld_cluster_v4(uint32_t caddr) {
+    uint4 v;
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(caddr)
+                 : "memory");
+    return v;
+}
 __device__ __forceinline__ float ld_cluster_f32(uint32_t caddr) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr) : "memory");
