@@ -171,7 +171,14 @@ TcNcWs tc_noncausal_ws(int B, int H, int n, int d, int m) {
     return w;
 }
 
+// Short sequences (one cluster of at most 8 tiles per head) run as a single fused launch.
+bool tc_fused_ok(int n, int d, int m, favor_dtype_t dt) {
+    return dt == FAVOR_BF16 && d == 64 && m_padded(m) <= 256 && n >= 1 && n <= tcfu::kMaxCluster * tcfu::kTile;
+}
+
 size_t noncausal_ws_bytes(int B, int H, int n, int d, int m, favor_dtype_t dt) {
+    if (tc_fused_ok(n, d, m, dt))
+        return tcfu::fused_ws_bytes(B * H, (n + tcfu::kTile - 1) / tcfu::kTile, m_padded(m));
     return tc_noncausal_ok(d, m, dt) ? tc_noncausal_ws(B, H, n, d, m).total : noncausal_ws(B, H, n, d, m).total;
 }
 
@@ -293,13 +300,8 @@ favor_status_t simt_causal(const void* Q, const void* K, const void* V, const vo
     return FAVOR_OK;
 }
 
-// Short sequences (one cluster of at most 8 tiles per head) run as a single fused launch.
-bool tc_fused_ok(int n, int d, int m, favor_dtype_t dt) {
-    return dt == FAVOR_BF16 && d == 64 && m_padded(m) <= 256 && n >= 1 && n <= tcfu::kMaxCluster * tcfu::kTile;
-}
-
 favor_status_t tc_fused(const void* Q, const void* K, const void* V, const void* Om, void* Y, int B, int H, int n, int m,
-                        int kind, float eps, cudaStream_t s) {
+                        int kind, float eps, void* ws, cudaStream_t s) {
     const int BH = B * H;
     CUtensorMap mQ, mK, mV, mOm;
     if (!tma::encode_bf16_3d(&mQ, Q, 64, n, BH, 64, tcfu::kTile) || !tma::encode_bf16_3d(&mK, K, 64, n, BH, 64, tcfu::kTile) ||
@@ -307,7 +309,14 @@ favor_status_t tc_fused(const void* Q, const void* K, const void* V, const void*
         return FAVOR_ERR_CUDA;
     const int m_pad = m_padded(m);
     const int T = (n + tcfu::kTile - 1) / tcfu::kTile;
-    tcfu::FusedParams fp{n, m, m_pad, kind, eps * std::sqrt((float)m), qk_scale(64), static_cast<__nv_bfloat16*>(Y)};
+    char* base = static_cast<char*>(ws);
+    float4* Pp = reinterpret_cast<float4*>(base);
+    base += tcfu::fused_ws_part(tcfu::fused_ws_pp_bytes(BH, T, m_pad));
+    float* Zp = reinterpret_cast<float*>(base);
+    base += tcfu::fused_ws_part((size_t)BH * T * 2 * m_pad * 4);
+    float* Stab = reinterpret_cast<float*>(base);
+    tcfu::FusedParams fp{n,  m,  m_pad, kind, eps * std::sqrt((float)m), qk_scale(64), static_cast<__nv_bfloat16*>(Y),
+                         Pp, Zp, Stab};
     const size_t smem = tcfu::FusedSmem::bytes(m_pad);
     FAVOR_TRY(set_smem(tcfu::nc_fused_small, smem));
     cudaLaunchConfig_t cfg = {};
@@ -546,7 +555,7 @@ favor_status_t favor_attn_noncausal(const void* Q, const void* K, const void* V,
     if ((int64_t)B * H * n == 0) return FAVOR_OK;
     FAVOR_TRY(check_ws(workspace, ws_bytes, noncausal_ws_bytes(B, H, n, d, m, dt)));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (tc_fused_ok(n, d, m, dt)) return tc_fused(Q, K, V, Omega, Y, B, H, n, m, (int)kind, relu_eps, s);
+    if (tc_fused_ok(n, d, m, dt)) return tc_fused(Q, K, V, Omega, Y, B, H, n, m, (int)kind, relu_eps, workspace, s);
     if (tc_noncausal_ok(d, m, dt))
         return d == 64 ? tc_noncausal<64>(Q, K, V, Omega, Y, B, H, n, m, (int)kind, relu_eps, workspace, s)
                        : tc_noncausal<128>(Q, K, V, Omega, Y, B, H, n, m, (int)kind, relu_eps, workspace, s);

@@ -150,6 +150,9 @@ __device__ __forceinline__ uint4 ld_cluster_v4(uint32_t caddr) {
                  : "memory");
     return v;
 }
+__device__ __forceinline__ void st_cluster_v2(uint32_t caddr, uint32_t x, uint32_t y) {
+    asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(caddr), "r"(x), "r"(y) : "memory");
+}
 __device__ __forceinline__ float ld_cluster_f32(uint32_t caddr) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr) : "memory");
@@ -163,6 +166,10 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// The two halves of cluster_sync(), for work between them (each warp converged). The release /
+// acquire pair orders global as well as shared memory accesses among the cluster's threads.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------------------------
 // Programmatic dependent launch: a kernel launched with programmatic stream serialisation may start
@@ -210,6 +217,15 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+// Bulk copy from this CTA's shared memory into another CTA of the cluster (dst and bar are
+// shared::cluster addresses from mapa); completes bytes on the receiver's mbarrier.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_caddr, const void* src, uint32_t bytes,
+                                                  uint32_t bar_caddr) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst_caddr),
+        "r"(smem_u32(src)), "r"(bytes), "r"(bar_caddr)
         : "memory");
 }
 // Makes generic-proxy writes to shared memory visible to the async proxy (TMA, tensor cores).
@@ -295,6 +311,9 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld2(uint32_t taddr, uint32_t& r0, uint32_t& r1) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 

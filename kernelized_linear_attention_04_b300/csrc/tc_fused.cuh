@@ -4,14 +4,18 @@
 //   1. projects its key tile with the features on the TMEM lanes, turns U^T into phi(K)^T in place
 //      and accumulates its partial S = phi(K)^T V (tcgen05, A from TMEM) and z (per-lane sums), with
 //      a key stabiliser of its own (12 nats below the tile's largest bound W |k^| - |k^|^2 / 2);
-//   2. publishes the partial (fp32) in its shared memory; after a cluster barrier, CTA c sums the
-//      feature rows [c R, (c + 1) R) over the cluster in rank order, each partial rescaled to the
-//      cluster's largest stabiliser, and writes the bf16 rows of S (in the readout MMA's swizzled
-//      operand layout) and z into every CTA of the cluster through distributed shared memory;
-//   3. after a second cluster barrier, projects its query tile (tokens on the lanes), forms phi(Q)
-//      in place with the exact row stabiliser, den = phi(Q) . z on the CUDA cores and
-//      num = phi(Q) S on the tensor cores, and stores Y = num / den.
-// S never goes through global memory and the whole call is one launch.
+//   2. writes the partial (fp32, straight from TMEM), its z and its stabiliser to the workspace in
+//      global memory (L2) and arrives on a cluster barrier; while the barrier completes it projects
+//      its query tile (tokens on the lanes) and forms phi(Q) in place with the exact row stabiliser;
+//   3. sums the feature rows it owns ([c R, (c + 1) R) for CTA c) over the cluster's partials in
+//      rank order, each rescaled to the cluster's largest stabiliser, writes the bf16 rows into its
+//      own copy of the readout MMA's operand (swizzled, MN-major) and bulk-copies that contiguous
+//      block into every peer (completing on the peer's mbarrier); z it sums for all rows itself and
+//      stores as a bf16 hi + lo pair in two extra operand columns;
+//   4. once the peers' blocks have landed, takes [num | den] = phi(Q) [S | z_hi + z_lo] in one MMA
+//      (N = 64 + 16) and stores Y = num / den.
+// Distributed shared memory carries only the bf16 rows (per SM its bandwidth is far below L2's), in
+// bulk copies of whole row blocks.
 #pragma once
 
 #include "tc.cuh"
@@ -38,14 +42,24 @@ struct FusedParams {
     float relu_eps_s;  // relu_eps * sqrt(m)
     float scale;       // d^(-1/4)
     __nv_bfloat16* Y;
+    float4* Pp;        // [BH][T][16][m_pad] partial S: float4 column group c4 of feature row f at (c4, f)
+    float* Zp;         // [BH][T][2][m_pad] partial z of the two 64-token halves
+    float* Stab;       // [BH][kMaxCluster] key stabiliser of each CTA
 };
 
+// Workspace of one call: the partials of every CTA, 256-byte aligned pieces.
+inline size_t fused_ws_part(size_t b) { return (b + 255) & ~size_t(255); }
+inline size_t fused_ws_pp_bytes(int BH, int T, int m_pad) { return (size_t)BH * T * m_pad * 256; }
+inline size_t fused_ws_bytes(int BH, int T, int m_pad) {
+    return fused_ws_part(fused_ws_pp_bytes(BH, T, m_pad)) + fused_ws_part((size_t)BH * T * 2 * m_pad * 4) +
+           fused_ws_part((size_t)BH * kMaxCluster * 4);
+}
+
 struct FusedSmem {
-    // Omega (m_pad x 128 B), K, V, Q tiles, partial S (m_pad x 64 fp32), S image (m_pad x 128 B),
-    // z (m_pad fp32), z partials (2 x m_pad fp32), per-token constants, row-max / den exchange.
+    // Omega (m_pad x 128 B), K, V, Q tiles, the readout's B operand (two 64-column MN regions of
+    // m_pad x 128 B: S, then z_hi, z_lo and zeros), per-key constants, row-max exchange.
     static size_t bytes(int m_pad) {
-        return 1024 + (size_t)m_pad * 128 + 3 * kTileBytes + (size_t)m_pad * 256 + (size_t)m_pad * 128 +
-               (size_t)m_pad * 4 + 2 * (size_t)m_pad * 4 + 128 * 4 + 2 * 4 * 128 * 4;
+        return 1024 + (size_t)m_pad * 128 + 3 * kTileBytes + 2 * (size_t)m_pad * 128 + 128 * 4 + 4 * 128 * 4;
     }
 };
 
@@ -60,17 +74,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sK = sOm + (size_t)MP * 128;
     uint8_t* sV = sK + kTileBytes;
     uint8_t* sQ = sV + kTileBytes;
-    float* sP = reinterpret_cast<float*>(sQ + kTileBytes);  // [MP][64] partial S of this CTA
-    uint8_t* sS = reinterpret_cast<uint8_t*>(sP + (size_t)MP * 64);  // bf16 S image, MP rows x 128 B
-    float* sz = reinterpret_cast<float*>(sS + (size_t)MP * 128);     // [MP] z of the head
-    float* sZp = sz + MP;                                  // [2][MP] z partials of the two token halves
-    float* sC = sZp + 2 * MP;                              // [128] per-key constants
+    uint8_t* sS = sQ + kTileBytes;                         // bf16 [S | z] operand, 2 x MP x 128 B
+    float* sC = reinterpret_cast<float*>(sS + 2 * (size_t)MP * 128);  // [128] per-key constants
     float* sMax = sC + 128;                                // [4][128] row-max shares
-    float* sDen = sMax + 4 * 128;                          // [4][128] denominator shares
-    __shared__ uint64_t bar_load, bar_q, bar_u, bar_phi, bar_s, bar_pq, bar_phiq, bar_num;
+    __shared__ uint64_t bar_load, bar_q, bar_u, bar_phi, bar_s, bar_pq, bar_phiq, bar_num, bar_own, bar_img;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
-    __shared__ float sStab;
     __shared__ float red[kEpiWarps];
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -79,6 +88,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bh = blockIdx.x / T;
     const int j0 = rank * kTile;         // this CTA's tile
     const int nvalid = min(kTile, p.n - j0);
+    const int R = (MP + T - 1) / T;      // feature rows owned by each CTA
+    const int own_lo = min(MP, rank * R);
+    const int own_rows = min(MP, own_lo + R) - own_lo;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -90,27 +102,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bar_pq, 1);
         mbar_init(&bar_phiq, kEpiWarps);
         mbar_init(&bar_num, 1);
+        mbar_init(&bar_own, kEpiWarps);
+        mbar_init(&bar_img, 1);
         fence_mbar_init();
+        // the peers' rows of the operand arrive by bulk copies (after the first cluster barrier)
+        mbar_arrive_expect_tx(&bar_img, (uint32_t)(MP - own_rows) * 128);
+        // the loads start before the TMEM allocation and the CTA barrier
+        tma_prefetch_desc(&mQ);
+        tma_prefetch_desc(&mK);
+        tma_prefetch_desc(&mV);
+        tma_prefetch_desc(&mOm);
+        mbar_arrive_expect_tx(&bar_load, (uint32_t)MP * 128 + 2 * kTileBytes);
+        tma_load_3d(sK, &mK, &bar_load, 0, j0, bh);
+        for (int r0 = 0; r0 < MP; r0 += 128) tma_load_2d(sOm + (size_t)r0 * 128, &mOm, &bar_load, 0, r0);
+        tma_load_3d(sV, &mV, &bar_load, 0, j0, bh);
+        mbar_arrive_expect_tx(&bar_q, kTileBytes);
+        tma_load_3d(sQ, &mQ, &bar_q, 0, j0, bh);
     }
-    if (warp == 0) tmem_alloc(&tmem_base, 512);
+    if (warp == 0) {
+        __syncwarp();
+        tmem_alloc(&tmem_base, 512);
+    }
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = tmem_base;
     // TMEM: S_g at [64 g, 64 g + 64); U^T of group g at 256 + 128 g; later U(Q) at [256, 256 + MP)
-    // with phi(Q) packed in its first MP/2 columns, and num at [0, 64).
+    // with phi(Q) packed in its first MP/2 columns, and [num | den] at [0, 80).
 
     if (warp == 0) {
         if (lane == 0) {
-            tma_prefetch_desc(&mQ);
-            tma_prefetch_desc(&mK);
-            tma_prefetch_desc(&mV);
-            tma_prefetch_desc(&mOm);
-            mbar_arrive_expect_tx(&bar_load, (uint32_t)MP * 128 + 2 * kTileBytes);
-            for (int r0 = 0; r0 < MP; r0 += 128) tma_load_2d(sOm + (size_t)r0 * 128, &mOm, &bar_load, 0, r0);
-            tma_load_3d(sK, &mK, &bar_load, 0, j0, bh);
-            tma_load_3d(sV, &mV, &bar_load, 0, j0, bh);
-            mbar_arrive_expect_tx(&bar_q, kTileBytes);
-            tma_load_3d(sQ, &mQ, &bar_q, 0, j0, bh);
             bool ok = mbar_wait(&bar_load, 0, &abort_flag);
             tc_fence_after();
             // key projections U^T_g = Omega_g K^T (M = 128 features, N = 128 tokens, K = 64)
@@ -162,44 +182,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int r = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const int cg4 = ew >> 2;  // query side column group: features [cg4 Wf, cg4 Wf + Wf), outputs [16 cg4, +16)
+    const int Wf = MP / 4;
     bool failed = false;
-    float W = 0.f;
     if (warp > 0) {
         // ---------------- key side ----------------
         failed |= !mbar_wait(&bar_load, 0, &abort_flag);
         __syncwarp();
-        if (exp_kind) {  // W = largest row norm of Omega (identical in every CTA of the cluster)
+        // warps 1..4 own the tile's 128 keys (|k^|^2); warps 5..16 take the row norms of Omega for
+        // W = the largest of them (identical in every CTA of the cluster)
+        float kn2 = 0.f;
+        if (ew < 4) {
+            if (exp_kind) kn2 = p.scale * p.scale * tile_row_sqnorm<64>(sK, r);
+        } else if (exp_kind) {
             float w2 = 0.f;
-            for (int row = ew * 32 + lane; row < MP; row += 32 * kEpiWarps)
+            for (int row = (ew - 4) * 32 + lane; row < MP; row += 32 * (kEpiWarps - 4))
                 w2 = fmaxf(w2, tile_row_sqnorm<64>(sOm + (size_t)(row >> 7) * 16384, row & 127));
             w2 = warp_max(w2);
             if (lane == 0) red[ew] = w2;
         }
         named_bar(1, 32 * kEpiWarps);
-        if (exp_kind) {
-            float m2 = 0.f;
+        if (ew < 4) {  // the tile's stabiliser: largest bound W |k^| - |k^|^2 / 2 over its valid keys
+            float W = 0.f;
+            if (exp_kind) {
+                float m2 = 0.f;
 #pragma unroll
-            for (int i = 0; i < kEpiWarps; ++i) m2 = fmaxf(m2, red[i]);
-            W = sqrtf(m2);
-        }
-        named_bar(1, 32 * kEpiWarps);
-        // key norms and the tile's stabiliser (warps of column group 0 own the 128 key rows)
-        if (ew < 4) {
-            const bool valid = r < nvalid;
-            const float kn2 = exp_kind ? p.scale * p.scale * tile_row_sqnorm<64>(sK, r) : 0.f;
-            const float b = valid ? W * sqrtf(kn2) - 0.5f * kn2 : -INFINITY;
+                for (int i = 4; i < kEpiWarps; ++i) m2 = fmaxf(m2, red[i]);
+                W = sqrtf(m2);
+            }
+            const float b = r < nvalid ? W * sqrtf(kn2) - 0.5f * kn2 : -INFINITY;
             const float bm = warp_max(b);
             if (lane == 0) red[ew] = bm;
-            sC[r] = kn2;  // temporarily |k^|^2
         }
         named_bar(1, 32 * kEpiWarps);
         const float stab = exp_kind ? fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])) - kStabSlackLo : 0.f;
-        named_bar(1, 32 * kEpiWarps);
-        if (ew < 4) {
-            const float kn2 = sC[r];
-            sC[r] = r < nvalid ? (exp_kind ? (0.5f * kn2 + stab) * kLog2e : 0.f) : INFINITY;
-            if (ew == 0 && lane == 0) sStab = stab;
-        }
+        if (ew < 4) sC[r] = r < nvalid ? (exp_kind ? (0.5f * kn2 + stab) * kLog2e : 0.f) : INFINITY;
         named_bar(1, 32 * kEpiWarps);
         // phi^T for group tm (team of 8 warps), tokens [64 cg, 64 cg + 64) of the tile
         const int tm = ew / 8, cg = (ew % 8) >> 2;
@@ -238,102 +255,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_phi);
-        // partial S (fp32) and z of this CTA into shared memory for the cluster reduction
+        // the partial S row (fp32) and z of feature tm*128 + r to the workspace; a warp's 32 rows of
+        // one float4 column group are 512 contiguous bytes
         failed |= !mbar_wait(&bar_s, 0, &abort_flag);
         __syncwarp();
         tc_fence_after();
         if (tm < G) {
-            sZp[cg * MP + tm * 128 + r] = zpart;
             const int feat = tm * 128 + r;
             uint32_t v[32];
             tmem_ld32(tbase + lane_off + 64 * tm + 32 * cg, v);
             tmem_ld_wait();
-            float* dst = sP + (size_t)feat * 64 + 32 * cg;
+            float4* dst = p.Pp + ((size_t)(bh * T + rank) * 16 + 8 * cg) * MP + feat;
 #pragma unroll
-            for (int i = 0; i < 32; i += 4)
-                *reinterpret_cast<float4*>(dst + i) =
-                    make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]), __uint_as_float(v[i + 2]),
-                                __uint_as_float(v[i + 3]));
+            for (int c = 0; c < 8; ++c)
+                __stcg(dst + (size_t)c * MP, make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                                                         __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3])));
+            __stcg(p.Zp + ((size_t)(bh * T + rank) * 2 + cg) * MP + feat, zpart);
         }
+        if (ew == 0 && lane == 0) __stcg(p.Stab + bh * kMaxCluster + rank, stab);
         tc_fence_before();
         __syncwarp();
     }
-    cluster_sync();  // every CTA's partial S, z and stabiliser are in place
 
-    // ---------------- cluster reduction: CTA rank owns feature rows [rank * R, rank * R + R) ----------------
+    // ---------------- phi(Q), while the workspace stores drain ----------------
     if (warp > 0) {
-        float stabs[kMaxCluster];
-        float M = -INFINITY;
-        for (int c = 0; c < T; ++c) {
-            stabs[c] = ld_cluster_f32(mapa(smem_u32(&sStab), c));
-            M = fmaxf(M, stabs[c]);
-        }
-        const int R = (MP + T - 1) / T;
-        const int e = ew * 32 + lane;
-        const int part = e % 8;  // 8 threads per row, 8 columns each; 64 rows per pass
-        for (int rr = e / 8; rr < R; rr += 32 * kEpiWarps / 8) {
-            const int row = rank * R + rr;
-            if (row >= MP) break;
-            float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            float zs = 0.f;
-            for (int c = 0; c < T; ++c) {
-                const float wgt = ex2((stabs[c] - M) * kLog2e);
-                const uint32_t base = mapa(smem_u32(sP + (size_t)row * 64 + 8 * part), c);
-                const uint4 a = ld_cluster_v4(base), b = ld_cluster_v4(base + 16);
-                acc[0] = fmaf(wgt, __uint_as_float(a.x), acc[0]);
-                acc[1] = fmaf(wgt, __uint_as_float(a.y), acc[1]);
-                acc[2] = fmaf(wgt, __uint_as_float(a.z), acc[2]);
-                acc[3] = fmaf(wgt, __uint_as_float(a.w), acc[3]);
-                acc[4] = fmaf(wgt, __uint_as_float(b.x), acc[4]);
-                acc[5] = fmaf(wgt, __uint_as_float(b.y), acc[5]);
-                acc[6] = fmaf(wgt, __uint_as_float(b.z), acc[6]);
-                acc[7] = fmaf(wgt, __uint_as_float(b.w), acc[7]);
-                if (part == 0) {
-                    const float z0 = ld_cluster_f32(mapa(smem_u32(sZp + row), c));
-                    const float z1 = ld_cluster_f32(mapa(smem_u32(sZp + MP + row), c));
-                    zs = fmaf(wgt, z0 + z1, zs);
-                }
-            }
-            if (row >= p.m) {  // padding features contribute nothing
-#pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-                zs = 0.f;
-            }
-            const uint4 o = make_uint4(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]), pack_bf16(acc[4], acc[5]),
-                                       pack_bf16(acc[6], acc[7]));
-            const uint32_t off = sw128_offset(row, part);
-            for (int c = 0; c < T; ++c) {
-                st_cluster_v4(mapa(smem_u32(sS + off), c), o);
-                if (part == 0) st_cluster_f32(mapa(smem_u32(sz + row), c), zs);
-            }
-        }
-        // the S image is read by the tensor cores (async proxy) of the receiving CTAs
-        asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
-        __syncwarp();
-    }
-    cluster_sync();  // every CTA holds the head's S image and z
-    if (warp == 0) {
-        if (lane == 0) {
-            // numerator num = phi(Q) S (A = phi(Q) packed in TMEM, B = the S image, MN-major)
-            fence_async_smem();
-            constexpr uint32_t id_n = idesc_bf16(128, kD, false, true);
-            const bool ok = mbar_wait(&bar_phiq, 0, &abort_flag);
-            tc_fence_after();
-            if (ok) {
-                for (int ks = 0; ks < MP / 16; ++ks) {
-                    uint64_t bd = sdesc_sw128(smem_u32(sS + ks * 2048), (uint32_t)MP * 128, 1024);
-                    mma_ts(tbase, tbase + 256 + ks * 8, bd, id_n, ks > 0);
-                }
-            }
-            mma_commit(&bar_num);
-        }
-        __syncwarp();
-    }
-
-    // ---------------- query side ----------------
-    if (warp > 0) {
-        const int cg4 = ew >> 2;  // column group: features [cg4 Wf, cg4 Wf + Wf), outputs [16 cg4, 16 cg4 + 16)
-        const int Wf = MP / 4;
         failed |= !mbar_wait(&bar_pq, 0, &abort_flag);
         __syncwarp();
         tc_fence_after();
@@ -353,9 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar(1, 32 * kEpiWarps);  // every warp holds its U values: U may be overwritten now
         rmax = fmaxf(fmaxf(sMax[r], sMax[128 + r]), fmaxf(sMax[256 + r], sMax[384 + r]));
         const float cst = exp_kind ? A2 * rmax : 0.f;
-        float dsum = 0.f;
         auto feat32 = [&](const uint32_t (&v)[32], int h) {
-            const float* zr = sz + cg4 * Wf + 32 * h;
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
@@ -367,30 +310,132 @@ __global__ void __launch_bounds__(kThreads, 1)
                     f0 = fmaxf(__uint_as_float(v[i]) * p.scale, 0.f) + p.relu_eps_s;
                     f1 = fmaxf(__uint_as_float(v[i + 1]) * p.scale, 0.f) + p.relu_eps_s;
                 }
-                const uint32_t w = pack_bf16(f0, f1);
-                pk[i / 2] = w;
-                dsum = fmaf(__uint_as_float(w << 16), zr[i], dsum);
-                dsum = fmaf(__uint_as_float(w & 0xFFFF0000u), zr[i + 1], dsum);
+                pk[i / 2] = pack_bf16(f0, f1);
             }
             tmem_st16(tbase + lane_off + 256 + cg4 * (Wf / 2) + 16 * h, pk);
         };
         feat32(v0, 0);
         if (Wf == 64) feat32(v1, 1);
         tmem_st_wait();
-        sDen[cg4 * 128 + r] = dsum;
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_phiq);
-        named_bar(1, 32 * kEpiWarps);  // denominator shares visible
-        const float den = ((sDen[r] + sDen[128 + r]) + sDen[256 + r]) + sDen[384 + r];
+        __syncwarp();
+    }
+    cluster_arrive();  // (partials) this CTA's workspace writes are visible to the peers after the wait
+    cluster_wait();    // every CTA's partial S, z and stabiliser are in the workspace
+
+    // ---------------- reduction: z of every row, S of the owned rows [rank R, rank R + R) ----------------
+    if (warp > 0) {
+        // every load of this phase (stabilisers, z partials, S partials) is issued before the first
+        // use of any of them: one L2 round trip
+        float wgt[kMaxCluster];
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c) wgt[c] = c < T ? __ldcg(p.Stab + bh * kMaxCluster + c) : -INFINITY;
+        bool have_w = false;
+        auto weights = [&] {  // each partial's scale: exp(stab_c - largest stab)
+            if (have_w) return;
+            have_w = true;
+            float M = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kMaxCluster; ++c) M = fmaxf(M, wgt[c]);
+#pragma unroll
+            for (int c = 0; c < kMaxCluster; ++c) wgt[c] = c < T ? ex2((wgt[c] - M) * kLog2e) : 0.f;
+        };
+        // z (every CTA sums the head's z partials itself; thread ew * 32 + lane takes feature row
+        // fz, m_pad <= 512 threads) as operand columns 64 (hi) and 65 (lo) of the second MN region,
+        // columns 66..79 zero. Its loads are issued with those of the S rows below.
+        const int fz = ew * 32 + lane;
+        float zl[2 * kMaxCluster];
+        {
+            const float* zsrc = p.Zp + (size_t)bh * T * 2 * MP + fz;
+#pragma unroll
+            for (int c = 0; c < 2 * kMaxCluster; ++c) zl[c] = (fz < MP && c < 2 * T) ? __ldcg(zsrc + (size_t)c * MP) : 0.f;
+        }
+        const int c4 = ew;  // this warp's float4 column group: S columns [4 c4, 4 c4 + 4)
+        const float4* src = p.Pp + (size_t)bh * T * 16 * MP + (size_t)c4 * MP;
+        for (int i = lane; i < own_rows; i += 32) {
+            const int row = own_lo + i;
+            float4 a[kMaxCluster];
+#pragma unroll
+            for (int c = 0; c < kMaxCluster; ++c)  // all loads in flight
+                if (c < T) a[c] = __ldcg(src + (size_t)c * 16 * MP + row);
+            weights();
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int c = 0; c < kMaxCluster; ++c) {  // rank order
+                if (c < T) {
+                    acc[0] = fmaf(wgt[c], a[c].x, acc[0]);
+                    acc[1] = fmaf(wgt[c], a[c].y, acc[1]);
+                    acc[2] = fmaf(wgt[c], a[c].z, acc[2]);
+                    acc[3] = fmaf(wgt[c], a[c].w, acc[3]);
+                }
+            }
+            if (row >= p.m) {  // padding features contribute nothing
+#pragma unroll
+                for (int k = 0; k < 4; ++k) acc[k] = 0.f;
+            }
+            *reinterpret_cast<uint2*>(sS + sw128_offset(row, c4 >> 1) + 8 * (c4 & 1)) =
+                make_uint2(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]));
+        }
+        if (fz < MP) {
+            weights();
+            float z = 0.f;
+#pragma unroll
+            for (int c = 0; c < kMaxCluster; ++c) z = fmaf(wgt[c], zl[2 * c] + zl[2 * c + 1], z);
+            if (fz >= p.m) z = 0.f;  // padding features contribute nothing
+            const float zh = __bfloat162float(__float2bfloat16_rn(z));
+            uint8_t* zrow = sS + (size_t)MP * 128 + (size_t)fz * 128;
+            *reinterpret_cast<uint4*>(zrow + ((0u ^ (fz & 7u)) << 4)) = make_uint4(pack_bf16(zh, z - zh), 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(zrow + ((1u ^ (fz & 7u)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_async_smem();  // the rows are read by the bulk-copy engine and the tensor cores
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_own);
+        named_bar(1, 32 * kEpiWarps);  // the owned rows are complete
+        if (ew == 0 && lane == 0 && own_rows > 0) {
+            // the owned rows are one contiguous block of the operand: copy it into every peer
+            const uint32_t off = (uint32_t)own_lo * 128;
+            for (int c = 0; c < T; ++c)
+                if (c != rank)
+                    bulk_copy_to_peer(mapa(smem_u32(sS + off), c), sS + off, (uint32_t)own_rows * 128,
+                                      mapa(smem_u32(&bar_img), c));
+        }
+        __syncwarp();
+    }
+    if (warp == 0) {
+        if (lane == 0) {
+            // [num | den] = phi(Q) [S | z] (A = phi(Q) packed in TMEM, B = the operand, MN-major,
+            // N = 80: the S region and the first 16 columns of the z region)
+            constexpr uint32_t id_n = idesc_bf16(128, kD + 16, false, true);
+            const bool ok = mbar_wait(&bar_own, 0, &abort_flag) && mbar_wait(&bar_img, 0, &abort_flag) &&
+                            mbar_wait(&bar_phiq, 0, &abort_flag);
+            tc_fence_after();
+            if (ok) {
+                for (int ks = 0; ks < MP / 16; ++ks) {
+                    uint64_t bd = sdesc_sw128(smem_u32(sS + ks * 2048), (uint32_t)MP * 128, 1024);
+                    mma_ts(tbase, tbase + 256 + ks * 8, bd, id_n, ks > 0);
+                }
+            }
+            mma_commit(&bar_num);
+        }
+        __syncwarp();
+        // every peer's bulk copy into this CTA has landed (bar_img); arrive for the closing barrier
+        cluster_arrive();
+    }
+
+    // ---------------- the output ----------------
+    if (warp > 0) {
         failed |= !mbar_wait(&bar_num, 0, &abort_flag);
         __syncwarp();
+        cluster_arrive();  // the MMA has consumed the peers' rows: this CTA needs nothing more from them
         tc_fence_after();
-        uint32_t nv[16];
+        uint32_t nv[16], d0, d1;
         tmem_ld16(tbase + lane_off + 16 * cg4, nv);
+        tmem_ld2(tbase + lane_off + kD, d0, d1);
         tmem_ld_wait();
         if (r < nvalid) {
-            const float inv = 1.f / den;
+            const float inv = 1.f / (__uint_as_float(d0) + __uint_as_float(d1));
             uint4* dst = reinterpret_cast<uint4*>(p.Y + ((size_t)bh * p.n + j0 + r) * kD + 16 * cg4);
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
@@ -410,7 +455,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tbase, 512);
     }
-    cluster_sync();  // no CTA leaves while a peer may still read its shared memory
+    // no CTA leaves while a bulk copy out of its shared memory may still be running: every CTA
+    // arrives only once all copies into it have landed
+    cluster_wait();
 }
 
 }  // namespace tcfu
