@@ -14,6 +14,7 @@
 #include "simt_kernels.cuh"
 #include "tc_noncausal.cuh"
 #include "tc_causal.cuh"
+#include "tc_causal_wide.cuh"
 #include "tc_features.cuh"
 #include "tc_fused.cuh"
 #include "tma_host.h"
@@ -182,16 +183,17 @@ size_t noncausal_ws_bytes(int B, int H, int n, int d, int m, favor_dtype_t dt) {
     return tc_noncausal_ok(d, m, dt) ? tc_noncausal_ws(B, H, n, d, m).total : noncausal_ws(B, H, n, d, m).total;
 }
 
-// The tensor-core causal scan takes bf16 with d = 64; a head's 128-feature groups are spread over a
-// cluster of 1, 2 or 4 CTAs (each holding at most two groups in TMEM).
+// The tensor-core causal scan takes bf16 with d = 64. Heads of up to 256 features run the pipelined
+// scan (one 128-feature group per CTA, a cluster of 1 or 2 CTAs per head); wider heads (up to 512)
+// run the one-tile-at-a-time scan with up to two groups per CTA.
 bool tc_causal_ok(int d, int m, favor_dtype_t dt) { return dt == FAVOR_BF16 && d == 64 && m_padded(m) <= 512; }
 
-// Cluster size for the causal scan: with fewer heads than SMs, one group per CTA (more CTAs per
-// head); otherwise the fewest CTAs whose two-group TMEM budget holds the head's features.
-int causal_cluster(int BH, int m) {
+// Cluster size of the wide-head scan: with fewer heads than SMs, one group per CTA (three groups take
+// a cluster of four, the last CTA holding only padding features); otherwise two groups per CTA.
+int causal_wide_cluster(int BH, int m) {
     const int groups = m_padded(m) / 128;
-    int cs = groups == 3 ? 4 : groups;                 // one group per CTA
-    if (BH >= kNumSMs) cs = groups <= 2 ? 1 : 2;       // two groups per CTA
+    int cs = groups == 3 ? 4 : groups;
+    if (BH >= kNumSMs) cs = groups <= 2 ? 1 : 2;
     return cs;
 }
 
@@ -399,30 +401,46 @@ favor_status_t tc_noncausal(const void* Q, const void* K, const void* V, const v
 favor_status_t tc_causal(const void* Q, const void* K, const void* V, const void* Om, void* Y, int B, int H, int n,
                          int m, int kind, float eps, cudaStream_t s) {
     const int BH = B * H;
-    CUtensorMap mQ, mK, mV, mOm;
-    if (!tma::encode_bf16_3d(&mQ, Q, 64, n, BH, 64, tcc::kTile) || !tma::encode_bf16_3d(&mK, K, 64, n, BH, 64, tcc::kTile) ||
-        !tma::encode_bf16_3d(&mV, V, 64, n, BH, 64, tcc::kTile) || !tma::encode_bf16_2d(&mOm, Om, 64, m, 64, 128))
-        return FAVOR_ERR_CUDA;
-    const int cs = causal_cluster(BH, m);
     const int groups = m_padded(m) / 128;
-    const int m_cta = ((groups + cs - 1) / cs) * 128;  // features per CTA
-    tcc::CausalParams cp{n, m, m_cta, kind, eps * std::sqrt((float)m), qk_scale(64), static_cast<__nv_bfloat16*>(Y)};
-    const size_t smem = tcc::CausalSmem::bytes(m_cta);
-    FAVOR_TRY(set_smem(tcc::causal_tc, smem));
+    const bool wide = groups > 2;
+    CUtensorMap mQ, mK, mV, mOm;
+    const int tile = wide ? tccw::kTile : tcc::kTile;
+    if (!tma::encode_bf16_3d(&mQ, Q, 64, n, BH, 64, tile) || !tma::encode_bf16_3d(&mK, K, 64, n, BH, 64, tile) ||
+        !tma::encode_bf16_3d(&mV, V, 64, n, BH, 64, tile) || !tma::encode_bf16_2d(&mOm, Om, 64, m, 64, 128))
+        return FAVOR_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(BH * cs, 1, 1);
-    cfg.blockDim = dim3(tcc::kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    cfg.stream = s;
     cudaError_t lerr = cudaSuccess;
-    FAVOR_TRY(traced(FAVOR_KERNEL_CAUSAL, s, [&] { lerr = cudaLaunchKernelEx(&cfg, tcc::causal_tc, mQ, mK, mV, mOm, cp); }));
+    if (!wide) {
+        const int cs = groups;  // one 128-feature group per CTA
+        tcc::CausalParams cp{n,   m, kind, eps * std::sqrt((float)m), qk_scale(64), static_cast<const __nv_bfloat16*>(K),
+                             static_cast<__nv_bfloat16*>(Y)};
+        const size_t smem = tcc::CausalSmem::bytes(cs);
+        FAVOR_TRY(set_smem(tcc::causal_tc, smem));
+        cfg.gridDim = dim3(BH * cs, 1, 1);
+        cfg.blockDim = dim3(tcc::kThreads, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        attr[0].val.clusterDim.x = cs;
+        FAVOR_TRY(traced(FAVOR_KERNEL_CAUSAL, s, [&] { lerr = cudaLaunchKernelEx(&cfg, tcc::causal_tc, mQ, mK, mV, mOm, cp); }));
+    } else {
+        const int cs = causal_wide_cluster(BH, m);
+        const int m_cta = ((groups + cs - 1) / cs) * 128;  // features per CTA
+        tccw::CausalParams cp{n, m, m_cta, kind, eps * std::sqrt((float)m), qk_scale(64), static_cast<__nv_bfloat16*>(Y)};
+        const size_t smem = tccw::CausalSmem::bytes(m_cta);
+        FAVOR_TRY(set_smem(tccw::causal_tc_wide, smem));
+        cfg.gridDim = dim3(BH * cs, 1, 1);
+        cfg.blockDim = dim3(tccw::kThreads, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        attr[0].val.clusterDim.x = cs;
+        FAVOR_TRY(traced(FAVOR_KERNEL_CAUSAL, s,
+                         [&] { lerr = cudaLaunchKernelEx(&cfg, tccw::causal_tc_wide, mQ, mK, mV, mOm, cp); }));
+    }
     return lerr == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;
 }
 

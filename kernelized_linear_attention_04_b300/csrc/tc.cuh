@@ -312,6 +312,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
+// x0 = x0 * s + c, x1 = x1 * s + c in one packed fp32x2 FMA.
+__device__ __forceinline__ void fma2(float& x0, float& x1, float s, float c) {
+    asm("{\n\t.reg .b64 x, m, a;\n\t"
+        "mov.b64 x, {%0, %1};\n\tmov.b64 m, {%2, %2};\n\tmov.b64 a, {%3, %3};\n\t"
+        "fma.rn.f32x2 x, x, m, a;\n\t"
+        "mov.b64 {%0, %1}, x;\n\t}"
+        : "+f"(x0), "+f"(x1)
+        : "f"(s), "f"(c));
+}
 __device__ __forceinline__ void tmem_ld2(uint32_t taddr, uint32_t& r0, uint32_t& r1) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(taddr));
 }

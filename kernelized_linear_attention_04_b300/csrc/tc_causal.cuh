@@ -7,67 +7,74 @@
 // The prefix state is carried at every tile boundary (128 tokens); within a tile the keys are
 // masked by j <= i, which for two 64-token chunks is exactly their chunked prefix-sum result.
 //
-// Features are processed in 128-feature groups g; a head's groups are split over the CTAs of a
-// thread-block cluster (1, 2 or 4 CTAs, at most two groups each), which add their partial
-// numerators and denominators through distributed shared memory once per tile. Per group:
-//   U = Q_t Omega_g^T -> phi_g(Q) (tokens on TMEM lanes) -> shared memory (K-major);
-//   U = K_t Omega_g^T -> phi_g(K) -> shared memory;
-//   scores D_sc += phi_g(Q) phi_g(K)^T, inter D_num += phi_g(Q) S_g (the state as taken at the tile
-//   start, split into hi + lo bf16 images so that it keeps about 16 significant bits), state S_g += phi_g(K)^T V_t and z_g += phi_g(K)^T 1 (MMA with a block
-//   of ones), all on the tensor cores with fp32 accumulation in TMEM.
-// After the groups: the masked scores A~ are split into two bf16 operands (hi + lo, about 16
-// significant bits) for D_num += A~ V_t; den takes phi(q) . z_<t on the CUDA cores plus the fp32
-// row sums of the masked scores.
+// Each CTA holds one 128-feature group of the head; a head with more features is spread over a
+// thread-block cluster (2 or 4 CTAs) whose partial numerators and denominators are summed through
+// distributed shared memory once per tile.
+//
+// The tiles run as a software pipeline over four roles:
+//   warp 0      TMA producer: Q, K (single buffers) and V (two buffers) of the coming tiles;
+//   warp 1      MMA issuer, in the order [scores(t), inter(t), state(t)] [proj Q(t+1), proj K(t+1)]
+//               [intra(t)], so that the next tile's projections run while tile t's masked scores
+//               are formed;
+//   warps 2-9   feature team: phi(Q_t), phi(K_t) from the projections (TMEM) into shared memory, and
+//               the inter-tile part of the denominator, phi(q) . z_<t;
+//   warps 10-17 output team: the masked scores A~ (converted in place in TMEM into bf16 hi + lo, the
+//               A operand of the intra MMA), the bf16 hi + lo snapshot of the state for the next
+//               tile, and the output (cluster sum, num / den, Y).
+// The numerator has two TMEM buffers, so the inter MMA of tile t+1 need not wait for the output of
+// tile t. Tensor-core work per tile: U = X Omega^T (two projections), scores phi(Q) phi(K)^T, inter
+// phi(Q) (S_hi + S_lo), state S += phi(K)^T V and z += phi(K)^T 1, intra (A~hi + A~lo) V.
 //
 // Stabilisers: a query row uses c_i = W |q^_i| (W = largest row norm of Omega; Cauchy-Schwarz bounds
-// every w_r . q^_i by it), the same in every feature group; keys use one running per-head constant
-// raised (with a rescale of S and z) when a tile's bound W |k^| - |k^|^2/2 exceeds it by more than
-// kStabSlackHi. Both cancel in num / den; the common 1/sqrt(m) is dropped.
+// every w_r . q^_i by it). Keys use one constant per head, 12 nats below the largest bound
+// W |k^_j| - |k^_j|^2 / 2 over all of the head's keys, found by a pass over K before the scan. Both
+// cancel in num / den; the common 1/sqrt(m) is dropped.
 #pragma once
 
 #include "tc.cuh"
-#include "tc_noncausal.cuh"  // shared helpers: ex2, tile_row_sqnorm, slack constants
+#include "tc_noncausal.cuh"  // shared helpers: ex2, tile_row_sqnorm, sq_acc_bf16x2, slack constant
 
 namespace favor {
 namespace tcc {
 
 using namespace favor::tc;
 using tcnc::ex2;
-using tcnc::kStabSlackHi;
 using tcnc::kStabSlackLo;
+using tcnc::sq_acc_bf16x2;
 using tcnc::tile_row_sqnorm;
 
 constexpr int kTile = 128;
-constexpr int kD = 64;                 // head dimension handled by this kernel
-constexpr int kEpiWarps = 16;  // four column groups x four TMEM lane quarters
-constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr int kTileBytes = kTile * kD * 2;  // 16 KB: one [128 x 64] bf16 tile
-constexpr int kPhiBytes = kTile * 128 * 2;  // 32 KB: [128 tokens x 128 features] bf16, two K atoms
-constexpr int kXStride = 84;                // floats per row of the cluster exchange buffer (64 + den + pad)
+constexpr int kD = 64;                       // head dimension handled by this kernel
+constexpr int kFeat = 128;                   // features per CTA
+constexpr int kTeamWarps = 8;                // warps of the feature team and of the output team
+constexpr int kThreads = 64 + 2 * 32 * kTeamWarps;
+constexpr int kTileBytes = kTile * kD * 2;   // 16 KB: one [128 x 64] bf16 tile
+constexpr int kPhiBytes = kTile * 128 * 2;   // 32 KB: [128 tokens x 128 features] bf16, two K atoms
+constexpr int kXStride = 84;                 // floats per row of the cluster exchange buffer (64 + den + pad)
 
 // TMEM columns
-constexpr uint32_t kColS = 0;      // S_g at g * 80: 64 columns of S, 16 of z (all equal)
-constexpr uint32_t kColU = 160;    // projection output, 128 columns
-constexpr uint32_t kColSc = 288;   // scores, 128 columns
-constexpr uint32_t kColNum = 416;  // numerator, 64 columns
+constexpr uint32_t kColS = 0;      // S: 64 columns, z: 16 (all equal)
+constexpr uint32_t kColU = 128;    // projection output, 128 columns
+constexpr uint32_t kColSc = 256;   // scores; then A~ in place: keys [16 s, 16 s + 16) -> hi at 16 s, lo at 16 s + 8
+constexpr uint32_t kColNum = 384;  // numerator, two buffers of 64 columns
 
 struct CausalParams {
     int n;
     int m;
-    int m_pad;   // features handled by one CTA, a multiple of 128 (at most 256)
     int kind;
     float relu_eps_s;
     float scale;
+    const __nv_bfloat16* K;  // [BH][n][64] keys, read directly by the stabiliser pass
     __nv_bfloat16* Y;
 };
 
 struct CausalSmem {
-    // Omega (m_pad x 64, K-major), Q, K and V tiles, phi(Q) / A~lo, phi(K) / A~hi, the state snapshot
-    // as hi and lo bf16 images (m_pad x 64 each, MN-major), ones block (16 x 128 bf16, K-major), z
-    // snapshot (m_pad fp32).
-    static size_t bytes(int m_pad) {
-        return 1024 + (size_t)m_pad * 128 + 3 * kTileBytes + 2 * kPhiBytes + 2 * (size_t)m_pad * 128 + 4096 +
-               (size_t)m_pad * 4;
+    // Omega rows of the CTA (128 x 64, K-major), Q, K, two V tiles, the state snapshot as hi and lo
+    // bf16 images (128 x 64, MN-major), phi(Q), phi(K), ones block (16 x 128 bf16, K-major), z
+    // snapshots (2 x 128 fp32), denominator shares (6 x 128 fp32), cluster exchange buffer.
+    static size_t x_bytes(int cs) { return cs > 1 ? (size_t)(cs - 1) * (kTile / cs) * kXStride * 4 : 0; }
+    static size_t bytes(int cs) {
+        return 1024 + 7 * (size_t)kTileBytes + 2 * (size_t)kPhiBytes + 4096 + 8 * 128 * 4 + x_bytes(cs);
     }
 };
 
@@ -76,38 +83,40 @@ __global__ void __launch_bounds__(kThreads, 1)
               const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mOm, CausalParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];  // aligned to 1024 by hand below
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int MP = p.m_pad;  // this CTA's features
-    const int G = MP / 128;
     // A head's features are split over the CS CTAs of a cluster: CTA `rank` owns features
-    // [rank * MP, (rank + 1) * MP). Partial numerators and denominators are summed across the
-    // cluster once per tile; CTA `rank` finalises the rows [rank * RP, (rank + 1) * RP).
+    // [rank * 128, rank * 128 + 128). The partial numerators and denominators of a tile are summed
+    // in the CTA that finalises the row: CTA `rank` owns the rows [rank * RP, (rank + 1) * RP).
     const int CS = (int)cluster_size();
     const int rank = (int)cluster_rank();
     const int RP = kTile / CS;
-    const int feat0 = rank * MP;
-    uint8_t* sOm = smem;                          // G regions of 128 rows x 128 B
-    uint8_t* sQ = sOm + (size_t)MP * 128;
+    const int feat0 = rank * kFeat;
+    uint8_t* sOm = smem;                       // 128 rows x 128 B
+    uint8_t* sQ = sOm + kTileBytes;
     uint8_t* sK = sQ + kTileBytes;
-    uint8_t* sV = sK + kTileBytes;
-    uint8_t* sPQ = sV + kTileBytes;               // phi(Q): 2 K-atom regions of 128 rows x 128 B; later A~lo
-    uint8_t* sPK = sPQ + kPhiBytes;               // phi(K); later A~hi
-    uint8_t* sS = sPK + kPhiBytes;                // S snapshot hi: MP rows x 128 B (MN-major, d contiguous)
-    uint8_t* sSl = sS + (size_t)MP * 128;         // S snapshot lo (S - hi, rounded)
-    uint8_t* sOnes = sSl + (size_t)MP * 128;      // 2 K-atom regions of 16 rows x 128 B
-    float* sZ = reinterpret_cast<float*>(sOnes + 4096);  // [MP] z snapshot
-    __shared__ uint64_t bar_om, bar_qfull, bar_kfull, bar_qkempty, bar_vfull, bar_vempty;
-    __shared__ uint64_t bar_snap, bar_ufull, bar_ufree, bar_phq, bar_phk, bar_grp, bar_atil, bar_num, bar_dfree;
+    uint8_t* sV0 = sK + kTileBytes;            // V of even tiles, then V of odd tiles
+    uint8_t* sS = sV0 + 2 * kTileBytes;        // state snapshot hi: 128 feature rows x 128 B (MN-major)
+    uint8_t* sSl = sS + kTileBytes;            // state snapshot lo (S - hi, rounded)
+    uint8_t* sPQ = sSl + kTileBytes;           // phi(Q): 2 K-atom regions of 128 rows x 128 B
+    uint8_t* sPK = sPQ + kPhiBytes;            // phi(K)
+    uint8_t* sOnes = sPK + kPhiBytes;          // 2 K-atom regions of 16 rows x 128 B
+    float* sZ = reinterpret_cast<float*>(sOnes + 4096);  // [2][128] z snapshot by tile parity
+    float* sDenF = sZ + 2 * 128;               // [2 parity][2 half][128] phi(q) . z_<t shares
+    float* sDenO = sDenF + 4 * 128;            // [2 half][128] masked score row sums
+    float* sX = sDenO + 2 * 128;               // [CS - 1][RP][kXStride] partial sums from the peers
+    __shared__ uint64_t bar_om, bar_qfull, bar_kfull, bar_qkempty, bar_vfull[2], bar_vempty[2];
+    __shared__ uint64_t bar_ufull, bar_ufree, bar_phq, bar_phk, bar_snap, bar_grp, bar_atil, bar_num;
+    __shared__ uint64_t bar_dfree[2], bar_den[2];
     __shared__ uint64_t bar_xfree, bar_xfull;  // cluster exchange of the partial sums
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
-    __shared__ float red[2][kEpiWarps];
-    __shared__ float sW[4];  // per-rank largest squared row norm of Omega
     __shared__ float sWred[kThreads / 32];
-    __shared__ float sDen[4 * 128];
+    __shared__ float sW[4];   // per-rank largest squared row norm of Omega
+    __shared__ float sKB[4];  // per-rank largest key bound
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int bh = blockIdx.x / CS;
     const int T = (p.n + kTile - 1) / kTile;
+    const bool exp_kind = p.kind == kKindExp;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -115,22 +124,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bar_qfull, 1);
         mbar_init(&bar_kfull, 1);
         mbar_init(&bar_qkempty, 1);
-        mbar_init(&bar_vfull, 1);
-        mbar_init(&bar_vempty, 1);
-        mbar_init(&bar_snap, kEpiWarps);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bar_vfull[b], 1);
+            mbar_init(&bar_vempty[b], 1);
+            mbar_init(&bar_dfree[b], kTeamWarps);
+            mbar_init(&bar_den[b], kTeamWarps);
+        }
         mbar_init(&bar_ufull, 1);
-        mbar_init(&bar_ufree, kEpiWarps);
-        mbar_init(&bar_phq, kEpiWarps);
-        mbar_init(&bar_phk, kEpiWarps);
+        mbar_init(&bar_ufree, kTeamWarps);
+        mbar_init(&bar_phq, kTeamWarps);
+        mbar_init(&bar_phk, kTeamWarps);
+        mbar_init(&bar_snap, kTeamWarps);
         mbar_init(&bar_grp, 1);
-        mbar_init(&bar_atil, kEpiWarps);
+        mbar_init(&bar_atil, kTeamWarps);
         mbar_init(&bar_num, 1);
-        mbar_init(&bar_dfree, kEpiWarps);
         mbar_init(&bar_xfree, CS > 1 ? CS - 1 : 1);
-        mbar_init(&bar_xfull, CS > 1 ? (CS - 1) * (RP / 32) * 4 : 1);
+        mbar_init(&bar_xfull, CS > 1 ? (CS - 1) * (RP / 32) * 2 : 1);
         fence_mbar_init();
     }
-    // ones block (K-major, every element 1.0): z_g = phi_g(K)^T 1 via the tensor cores
+    // ones block (K-major, every element 1.0): z = phi(K)^T 1 via the tensor cores
     for (int i = threadIdx.x; i < 4096 / 16; i += blockDim.x)
         reinterpret_cast<uint4*>(sOnes)[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
     fence_async_smem();
@@ -144,15 +156,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // stabiliser c_i = W |q^_i| and the key bound must be the same in every CTA of the cluster.
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&mOm);
-        mbar_arrive_expect_tx(&bar_om, (uint32_t)MP * 128);
-        for (int r0 = 0; r0 < MP; r0 += 128) tma_load_2d(sOm + (size_t)r0 * 128, &mOm, &bar_om, 0, feat0 + r0);
+        mbar_arrive_expect_tx(&bar_om, (uint32_t)kTileBytes);
+        tma_load_2d(sOm, &mOm, &bar_om, 0, feat0);
     }
     bool om_ok = mbar_wait(&bar_om, 0, &abort_flag);
     {
         float w2 = 0.f;
-        if (p.kind == kKindExp)
-            for (int row = threadIdx.x; row < MP; row += blockDim.x)
-                w2 = fmaxf(w2, tile_row_sqnorm<64>(sOm + (size_t)(row >> 7) * 16384, row & 127));
+        if (exp_kind && threadIdx.x < kFeat) w2 = tile_row_sqnorm<64>(sOm, threadIdx.x);
         w2 = warp_max(w2);
         if (lane == 0) sWred[warp] = w2;
         __syncthreads();
@@ -163,10 +173,68 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         cluster_sync();
     }
-    float W_all = 0.f;
-    for (int c = 0; c < CS; ++c) W_all = fmaxf(W_all, sW[c]);
-    W_all = sqrtf(W_all);
+    float W = 0.f;
+    for (int c = 0; c < CS; ++c) W = fmaxf(W, sW[c]);
+    W = sqrtf(W);
     (void)om_ok;
+
+    // Key stabiliser of the head: the CTAs of the cluster take the tiles t = rank (mod CS) and read
+    // the keys straight from global memory (four tiles of loads in flight per thread), then
+    // exchange their maxima.
+    float stab = 0.f;
+    const float s2 = p.scale * p.scale;
+    if (exp_kind) {
+        float kb = -INFINITY;
+        if (warp >= 2) {
+            const int e = threadIdx.x - 64;
+            const int sub = e & 7, rr = e >> 3;  // 16-byte chunk of the row, row within a 64-row step
+            const uint4* Kh = reinterpret_cast<const uint4*>(p.K + (size_t)bh * p.n * kD);
+            constexpr int kU = 4;
+            for (int t0 = rank; t0 < T; t0 += kU * CS) {
+                uint4 v[2 * kU];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+#pragma unroll
+                    for (int s = 0; s < 2; ++s) {
+                        const int tt = t0 + u * CS;
+                        const int j = tt * kTile + s * 64 + rr;
+                        v[2 * u + s] = (tt < T && j < p.n) ? __ldg(Kh + (size_t)j * 8 + sub) : make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+#pragma unroll
+                    for (int s = 0; s < 2; ++s) {
+                        const int tt = t0 + u * CS;
+                        const int j = tt * kTile + s * 64 + rr;
+                        float a0 = 0.f, a1 = 0.f;
+                        sq_acc_bf16x2(v[2 * u + s].x, a0, a1);
+                        sq_acc_bf16x2(v[2 * u + s].y, a0, a1);
+                        sq_acc_bf16x2(v[2 * u + s].z, a0, a1);
+                        sq_acc_bf16x2(v[2 * u + s].w, a0, a1);
+                        float ss = a0 + a1;  // the 8 lanes of a row hold its 8 chunks
+                        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+                        ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+                        const float kn2 = s2 * ss;
+                        if (tt < T && j < p.n) kb = fmaxf(kb, W * sqrtf(kn2) - 0.5f * kn2);
+                    }
+                }
+            }
+        }
+        kb = warp_max(kb);
+        if (lane == 0) sWred[warp] = kb;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float mx = -INFINITY;
+            for (int i = 0; i < kThreads / 32; ++i) mx = fmaxf(mx, sWred[i]);
+            for (int c = 0; c < CS; ++c) st_cluster_f32(mapa(smem_u32(&sKB[rank]), c), mx);
+        }
+        cluster_sync();
+        float Bk = -INFINITY;
+        for (int c = 0; c < CS; ++c) Bk = fmaxf(Bk, sKB[c]);
+        stab = Bk - kStabSlackLo;
+    }
 
     if (warp == 0) {
         // ---------------- TMA producer (lane 0) ----------------
@@ -176,209 +244,317 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&mV);
             bool ok = true;
             for (int t = 0; t < T && ok; ++t) {
-                // Q and K of tile t once tile t-1 is projected; V of tile t once tile t-1's intra MMA is done.
+                const int b = t & 1;
+                // Q and K of tile t once both projections of tile t-1 are done; V of tile t once the
+                // intra MMA of tile t-2 (the last reader of its buffer) is done.
                 if (!(ok = mbar_wait(&bar_qkempty, (t & 1) ^ 1, &abort_flag))) break;
                 mbar_arrive_expect_tx(&bar_qfull, kTileBytes);
                 tma_load_3d(sQ, &mQ, &bar_qfull, 0, t * kTile, bh);
                 mbar_arrive_expect_tx(&bar_kfull, kTileBytes);
                 tma_load_3d(sK, &mK, &bar_kfull, 0, t * kTile, bh);
-                if (!(ok = mbar_wait(&bar_vempty, (t & 1) ^ 1, &abort_flag))) break;
-                mbar_arrive_expect_tx(&bar_vfull, kTileBytes);
-                tma_load_3d(sV, &mV, &bar_vfull, 0, t * kTile, bh);
+                if (!(ok = mbar_wait(&bar_vempty[b], ((t >> 1) & 1) ^ 1, &abort_flag))) break;
+                mbar_arrive_expect_tx(&bar_vfull[b], kTileBytes);
+                tma_load_3d(sV0 + b * kTileBytes, &mV, &bar_vfull[b], 0, t * kTile, bh);
             }
             // Drain the loads in flight before the CTA may exit.
             volatile int never = 0;
             if (T > 0) {
                 mbar_wait(&bar_qfull, (T - 1) & 1, &never);
                 mbar_wait(&bar_kfull, (T - 1) & 1, &never);
-                mbar_wait(&bar_vfull, (T - 1) & 1, &never);
+                mbar_wait(&bar_vfull[(T - 1) & 1], ((T - 1) >> 1) & 1, &never);
             }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer (lane 0) ----------------
         if (lane == 0) {
-            constexpr uint32_t id_proj = idesc_bf16(128, 128, false, false);  // U = X Om_g^T
+            constexpr uint32_t id_proj = idesc_bf16(128, 128, false, false);  // U = X Om^T
             constexpr uint32_t id_sc = idesc_bf16(128, 128, false, false);    // phi(Q) phi(K)^T
-            constexpr uint32_t id_num = idesc_bf16(128, kD, false, true);     // phi(Q) S_g, A~ V
+            constexpr uint32_t id_num = idesc_bf16(128, kD, false, true);     // phi(Q) S, A~ V
             constexpr uint32_t id_st = idesc_bf16(128, kD, true, true);       // phi(K)^T V
             constexpr uint32_t id_z = idesc_bf16(128, 16, true, false);       // phi(K)^T 1
-            bool ok = mbar_wait(&bar_om, 0, &abort_flag);
-            tc_fence_after();
-            int uuse = 0;  // uses of the U slot so far
-            auto proj = [&](const uint8_t* x, int g) {
+            bool ok = true;
+            int pu = 0;  // projections issued into the one U slot
+            auto proj = [&](const uint8_t* x, uint64_t* full, uint32_t parity) -> bool {
+                if (!mbar_wait(full, parity, &abort_flag)) return false;
+                if (pu > 0 && !mbar_wait(&bar_ufree, (pu - 1) & 1, &abort_flag)) return false;
+                tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < kD / 16; ++ks) {
                     uint64_t ad = sdesc_sw128(smem_u32(x + ks * 32), 16, 1024);
-                    uint64_t bd = sdesc_sw128(smem_u32(sOm + (size_t)g * 16384 + ks * 32), 16, 1024);
+                    uint64_t bd = sdesc_sw128(smem_u32(sOm + ks * 32), 16, 1024);
                     mma_ss(tbase + kColU, ad, bd, id_proj, ks > 0);
                 }
                 mma_commit(&bar_ufull);
+                ++pu;
+                return true;
             };
+            if (T > 0) {
+                ok = proj(sQ, &bar_qfull, 0) && proj(sK, &bar_kfull, 0);
+                if (ok) mma_commit(&bar_qkempty);
+            }
             for (int t = 0; t < T && ok; ++t) {
-                ok = ok && mbar_wait(&bar_qfull, t & 1, &abort_flag) && mbar_wait(&bar_kfull, t & 1, &abort_flag);
-                ok = ok && mbar_wait(&bar_snap, t & 1, &abort_flag);
-                ok = ok && mbar_wait(&bar_dfree, (t & 1) ^ 1, &abort_flag);
+                const int b = t & 1;
+                const uint8_t* vt = sV0 + b * kTileBytes;
+                const uint32_t nb = tbase + kColNum + 64 * b;
+                ok = mbar_wait(&bar_phq, t & 1, &abort_flag) && mbar_wait(&bar_phk, t & 1, &abort_flag) &&
+                     mbar_wait(&bar_snap, t & 1, &abort_flag) &&
+                     mbar_wait(&bar_dfree[b], ((t >> 1) & 1) ^ 1, &abort_flag) &&
+                     mbar_wait(&bar_vfull[b], (t >> 1) & 1, &abort_flag);
                 if (!ok) break;
                 tc_fence_after();
-                const uint8_t* vt = sV;
-                bool have_v = false;
-                for (int g = 0; g < G && ok; ++g) {
-                    // projections: Q then K into the one U slot
-                    ok = mbar_wait(&bar_ufree, (uuse & 1) ^ 1, &abort_flag);
-                    if (!ok) break;
-                    tc_fence_after();
-                    proj(sQ, g);
-                    ++uuse;
-                    ok = mbar_wait(&bar_ufree, (uuse & 1) ^ 1, &abort_flag);
-                    if (!ok) break;
-                    tc_fence_after();
-                    proj(sK, g);
-                    ++uuse;
-                    if (g == G - 1) mma_commit(&bar_qkempty);
-                    const int gu = t * G + g;  // group use count
-                    ok = mbar_wait(&bar_phq, gu & 1, &abort_flag) && mbar_wait(&bar_phk, gu & 1, &abort_flag);
-                    if (ok && !have_v) ok = have_v = mbar_wait(&bar_vfull, t & 1, &abort_flag);
-                    if (!ok) break;
-                    tc_fence_after();
-                    // scores and inter numerator (K = 128 features of group g, two K atoms)
+                // scores (K = 128 features, two K atoms)
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const int a = ks / 4, w = ks % 4;
+                    uint64_t ad = sdesc_sw128(smem_u32(sPQ + a * 16384 + w * 32), 16, 1024);
+                    uint64_t bd = sdesc_sw128(smem_u32(sPK + a * 16384 + w * 32), 16, 1024);
+                    mma_ss(tbase + kColSc, ad, bd, id_sc, ks > 0);
+                }
+                // inter numerator: phi(Q) (S_hi + S_lo), the state as taken at the tile start
+                for (int part = 0; part < 2; ++part) {
+                    const uint8_t* sp = part == 0 ? sS : sSl;
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         const int a = ks / 4, w = ks % 4;
                         uint64_t ad = sdesc_sw128(smem_u32(sPQ + a * 16384 + w * 32), 16, 1024);
-                        uint64_t bd = sdesc_sw128(smem_u32(sPK + a * 16384 + w * 32), 16, 1024);
-                        mma_ss(tbase + kColSc, ad, bd, id_sc, (g > 0 || ks > 0));
+                        uint64_t bd = sdesc_sw128(smem_u32(sp + ks * 16 * 128), 16, 1024);
+                        mma_ss(nb, ad, bd, id_num, part > 0 || ks > 0);
                     }
-                    for (int part = 0; part < 2; ++part) {  // state snapshot hi, then lo
-                        const uint8_t* sp = part == 0 ? sS : sSl;
-#pragma unroll
-                        for (int ks = 0; ks < 8; ++ks) {
-                            const int a = ks / 4, w = ks % 4;
-                            uint64_t ad = sdesc_sw128(smem_u32(sPQ + a * 16384 + w * 32), 16, 1024);
-                            uint64_t bd = sdesc_sw128(smem_u32(sp + (size_t)(g * 128 + ks * 16) * 128), 16, 1024);
-                            mma_ss(tbase + kColNum, ad, bd, id_num, (g > 0 || part > 0 || ks > 0));
-                        }
-                    }
-                    // state update: S_g += phi_g(K)^T V_t, z_g += phi_g(K)^T 1 (K = 128 tokens)
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        uint64_t ad = sdesc_sw128(smem_u32(sPK + ks * 2048), 16384, 1024);
-                        uint64_t bd = sdesc_sw128(smem_u32(vt + ks * 2048), 16, 1024);
-                        mma_ss(tbase + kColS + g * 80, ad, bd, id_st, (t > 0 || ks > 0));
-                    }
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const int a = ks / 4, w = ks % 4;
-                        uint64_t ad = sdesc_sw128(smem_u32(sPK + ks * 2048), 16384, 1024);
-                        uint64_t bd = sdesc_sw128(smem_u32(sOnes + a * 2048 + w * 32), 16, 1024);
-                        mma_ss(tbase + kColS + g * 80 + 64, ad, bd, id_z, (t > 0 || ks > 0));
-                    }
-                    mma_commit(&bar_grp);
                 }
-                if (!ok) break;
-                // intra-tile numerator: D_num += (A~hi + A~lo) V_t (hi in the phi(K) buffer, lo in the
-                // phi(Q) buffer; K = 128 tokens)
-                ok = mbar_wait(&bar_atil, t & 1, &abort_flag);
-                if (!ok) break;
+                // state update: S += phi(K)^T V_t, z += phi(K)^T 1 (K = 128 tokens)
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    uint64_t ad = sdesc_sw128(smem_u32(sPK + ks * 2048), 16384, 1024);
+                    uint64_t bd = sdesc_sw128(smem_u32(vt + ks * 2048), 16, 1024);
+                    mma_ss(tbase + kColS, ad, bd, id_st, t > 0 || ks > 0);
+                }
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const int a = ks / 4, w = ks % 4;
+                    uint64_t ad = sdesc_sw128(smem_u32(sPK + ks * 2048), 16384, 1024);
+                    uint64_t bd = sdesc_sw128(smem_u32(sOnes + a * 2048 + w * 32), 16, 1024);
+                    mma_ss(tbase + kColS + 64, ad, bd, id_z, t > 0 || ks > 0);
+                }
+                mma_commit(&bar_grp);
+                // projections of the next tile while the output team forms A~
+                if (t + 1 < T) {
+                    ok = proj(sQ, &bar_qfull, (t + 1) & 1) && proj(sK, &bar_kfull, (t + 1) & 1);
+                    if (!ok) break;
+                    mma_commit(&bar_qkempty);
+                }
+                // intra numerator: Num += (A~hi + A~lo) V_t, A from TMEM (K = 128 keys)
+                if (!(ok = mbar_wait(&bar_atil, t & 1, &abort_flag))) break;
                 tc_fence_after();
                 for (int part = 0; part < 2; ++part) {
-                    const uint8_t* at = part == 0 ? sPK : sPQ;
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
-                        const int a = ks / 4, w = ks % 4;
-                        uint64_t ad = sdesc_sw128(smem_u32(at + a * 16384 + w * 32), 16, 1024);
                         uint64_t bd = sdesc_sw128(smem_u32(vt + ks * 2048), 16, 1024);
-                        mma_ss(tbase + kColNum, ad, bd, id_num, 1);
+                        mma_ts(nb, tbase + kColSc + 16 * ks + 8 * part, bd, id_num, 1);
                     }
                 }
                 mma_commit(&bar_num);
-                mma_commit(&bar_vempty);
+                mma_commit(&bar_vempty[b]);
             }
         }
-    } else {
-        // ---------------- epilogue: 16 warps ----------------
-        // Warp ew = warp - 2 reads TMEM lane quarter q = warp % 4 (a hardware rule) and takes column
-        // group cg = ew / 4 of every row it handles. Its lane is a token row for the projections,
-        // the scores and the numerator, and a feature row for the state.
-        constexpr int NT = 32 * kEpiWarps;
-        const int ew = warp - 2;
-        const int q = warp & 3, cg = ew >> 2;
+    } else if (warp < 2 + kTeamWarps) {
+        // ---------------- feature team: 8 warps ----------------
+        // Warp w reads TMEM lane quarter q = w % 4 (a hardware rule) and features [64 h, 64 h + 64)
+        // of the projection; its lane is token row r of the tile.
+        const int fw = warp - 2;
+        const int q = warp & 3, h = fw >> 2;
         const int r = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         const float A2 = p.scale * kLog2e;
-        const bool exp_kind = p.kind == kKindExp;
-        bool failed = !mbar_wait(&bar_om, 0, &abort_flag);
-        __syncwarp();
-        const float W = W_all;
-        float stab = 0.f;
-        int guse = 0;    // feature groups whose MMAs have been committed (bar_grp phases)
-        int uuse_e = 0;  // projections consumed (bar_ufull phases)
+        bool failed = false;
+        int pu = 0;  // projections consumed
+        const int fvalid = p.m - (feat0 + 64 * h);  // real (not padding) features among this warp's 64
+        // phi of the 64 projections in v into row r of `dst` (K-major, atom region h). For exp
+        // features a row that must be zero gets cst = +inf (ex2(-inf) = 0); the per-feature padding
+        // test is skipped when all 64 features are real (a warp-uniform branch).
+        auto write_phi = [&](uint8_t* dst, const uint32_t (&v)[64], float cst, bool zero_row) {
+            if (exp_kind && fvalid >= 64) {
+                const float c = zero_row ? INFINITY : cst;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        float x0 = __uint_as_float(v[8 * ch + 2 * k]), x1 = __uint_as_float(v[8 * ch + 2 * k + 1]);
+                        fma2(x0, x1, A2, -c);
+                        w[k] = pack_bf16(ex2(x0), ex2(x1));
+                    }
+                    *reinterpret_cast<uint4*>(dst + h * 16384 + sw128_offset(r, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                return;
+            }
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                float ph[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float a = __uint_as_float(v[8 * ch + k]);
+                    float x = exp_kind ? ex2(fmaf(a, A2, -cst)) : fmaxf(a * p.scale, 0.f) + p.relu_eps_s;
+                    if (zero_row || 8 * ch + k >= fvalid) x = 0.f;
+                    ph[k] = x;
+                }
+                uint4 o;
+                o.x = pack_bf16(ph[0], ph[1]);
+                o.y = pack_bf16(ph[2], ph[3]);
+                o.z = pack_bf16(ph[4], ph[5]);
+                o.w = pack_bf16(ph[6], ph[7]);
+                *reinterpret_cast<uint4*>(dst + h * 16384 + sw128_offset(r, ch)) = o;
+            }
+        };
+        auto load_u = [&](uint32_t (&v)[64]) {
+            tmem_ld32(tbase + lane_off + kColU + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(v));
+            tmem_ld32(tbase + lane_off + kColU + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_ufree);  // U has been read: the next projection may overwrite it
+            ++pu;
+        };
         for (int t = 0; t < T; ++t) {
-            const int i_tok = t * kTile + r;  // this thread's token (query row / key row)
-            const bool valid = i_tok < p.n;
+            const int b = t & 1;
+            const bool valid = t * kTile + r < p.n;
+            // ---- phi(Q_t); the norms of row r first (Q and K of tile t stay in shared memory until
+            // both projections of the tile are done)
+            failed |= !mbar_wait(&bar_ufull, pu & 1, &abort_flag);
             failed |= !mbar_wait(&bar_qfull, t & 1, &abort_flag);
             failed |= !mbar_wait(&bar_kfull, t & 1, &abort_flag);
             __syncwarp();
-            // norms of this row's query and key (each column group recomputes them: 64 elements)
-            const float qn2 = exp_kind ? p.scale * p.scale * tile_row_sqnorm<64>(sQ, r) : 0.f;
-            const float kn2 = exp_kind ? p.scale * p.scale * tile_row_sqnorm<64>(sK, r) : 0.f;
-            const float cq = exp_kind ? W * sqrtf(qn2) * kLog2e : 0.f;
-            float f = 1.f;
+            tc_fence_after();
+            float cq = 0.f, ck = 0.f;
             if (exp_kind) {
-                const float b = valid ? W * sqrtf(kn2) - 0.5f * kn2 : -INFINITY;
-                const float bm = warp_max(b);
-                if (lane == 0) red[t & 1][ew] = bm;
-                named_bar(1, NT);
-                float Bt = -INFINITY;
-#pragma unroll
-                for (int i = 0; i < kEpiWarps; ++i) Bt = fmaxf(Bt, red[t & 1][i]);
-                if (t == 0) {
-                    stab = Bt - kStabSlackLo;
-                } else if (Bt > stab + kStabSlackHi) {
-                    const float nst = Bt - kStabSlackLo;
-                    f = ex2((stab - nst) * kLog2e);
-                    stab = nst;
-                }
+                const float qn2 = s2 * tile_row_sqnorm<64>(sQ, r);
+                const float kn2 = s2 * tile_row_sqnorm<64>(sK, r);
+                cq = W * sqrtf(qn2) * kLog2e;
+                ck = (0.5f * kn2 + stab) * kLog2e;
             }
-            const float ck = valid ? (exp_kind ? (0.5f * kn2 + stab) * kLog2e : 0.f) : INFINITY;
-            // ---- state snapshot for this tile (lane = feature r of each group; 16 columns per warp) ----
-            if (t > 0) {
-                // every state MMA of the previous tile has completed once its last group committed
-                failed |= !mbar_wait(&bar_grp, (guse - 1) & 1, &abort_flag);
+            uint32_t v[64];
+            load_u(v);
+            if (t > 0) {  // the MMAs of tile t-1 have read the phi buffers
+                failed |= !mbar_wait(&bar_grp, (t - 1) & 1, &abort_flag);
                 __syncwarp();
-                tc_fence_after();
             }
-            for (int g = 0; g < G; ++g) {
-                const int feat = g * 128 + r;
-                uint32_t v[16];
-                const uint32_t sa = tbase + lane_off + kColS + g * 80;
-                if (t > 0) {
-                    tmem_ld16(sa + 16 * cg, v);
-                    uint32_t zz[16];
-                    if (cg == 0) tmem_ld16(sa + 64, zz);
-                    tmem_ld_wait();
-                    if (f != 1.f) {  // the key stabiliser moved: rescale the accumulated state
+            write_phi(sPQ, v, cq, false);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_phq);
+            // ---- den share phi(q_r) . z_<t over this warp's features, with the bf16-rounded phi
+            // (both waits come before this tile's phi(K) is published, so neither barrier can have
+            // moved on by two phases)
+            failed |= !mbar_wait(&bar_snap, t & 1, &abort_flag);
+            failed |= !mbar_wait(&bar_dfree[b], ((t >> 1) & 1) ^ 1, &abort_flag);  // tile t-2's shares read
+            __syncwarp();
+            const float* zr = sZ + b * 128 + 64 * h;
+            float den = 0.f;
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
-                        tmem_st16(sa + 16 * cg, v);
-                        if (cg == 0) {
+            for (int c = 0; c < 8; ++c) {
+                const uint4 o = *reinterpret_cast<const uint4*>(sPQ + h * 16384 + sw128_offset(r, c));
+                const float4 za = *reinterpret_cast<const float4*>(zr + 8 * c);
+                const float4 zb = *reinterpret_cast<const float4*>(zr + 8 * c + 4);
+                den = fmaf(__uint_as_float(o.x << 16), za.x, den);
+                den = fmaf(__uint_as_float(o.x & 0xFFFF0000u), za.y, den);
+                den = fmaf(__uint_as_float(o.y << 16), za.z, den);
+                den = fmaf(__uint_as_float(o.y & 0xFFFF0000u), za.w, den);
+                den = fmaf(__uint_as_float(o.z << 16), zb.x, den);
+                den = fmaf(__uint_as_float(o.z & 0xFFFF0000u), zb.y, den);
+                den = fmaf(__uint_as_float(o.w << 16), zb.z, den);
+                den = fmaf(__uint_as_float(o.w & 0xFFFF0000u), zb.w, den);
+            }
+            sDenF[(b * 2 + h) * 128 + r] = den;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_den[b]);
+            // ---- phi(K_t)
+            failed |= !mbar_wait(&bar_ufull, pu & 1, &abort_flag);
+            __syncwarp();
+            tc_fence_after();
+            load_u(v);
+            write_phi(sPK, v, ck, !valid);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_phk);
+        }
+        (void)failed;
+    } else {
+        // ---------------- output team: 8 warps ----------------
+        // Warp w reads TMEM lane quarter q = w % 4 and half h of the columns: keys [64 h, 64 h + 64)
+        // of the scores, state columns [32 h, 32 h + 32) (lane = feature), output columns
+        // [32 h, 32 h + 32) (lane = token row).
+        const int ow = warp - 2 - kTeamWarps;
+        const int q = warp & 3, h = ow >> 2;
+        const int r = q * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        constexpr int NO = 32 * kTeamWarps;  // named barrier 2: the output team
+        bool failed = false;
+        // the state before tile 0 is zero
+        {
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) zz[i] = __float_as_uint(__uint_as_float(zz[i]) * f);
-                            tmem_st16(sa + 64, zz);
-                        }
-                        tmem_st_wait();
-                    }
-                    if (cg == 0) sZ[feat] = feat0 + feat < p.m ? __uint_as_float(zz[0]) : 0.f;
+            for (int c = 0; c < 4; ++c) {
+                *reinterpret_cast<uint4*>(sS + sw128_offset(r, 4 * h + c)) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(sSl + sw128_offset(r, 4 * h + c)) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            if (h == 0) sZ[r] = 0.f;
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_snap);
+        }
+        for (int t = 0; t < T; ++t) {
+            const int b = t & 1;
+            failed |= !mbar_wait(&bar_grp, t & 1, &abort_flag);
+            __syncwarp();
+            tc_fence_after();
+            // ---- A~ = scores masked by j <= i, as bf16 hi + lo, in place: the 16 columns of keys
+            // [16 s, 16 s + 16) become 8 columns of hi and 8 of lo
+            // Whether a 16-key chunk is wholly below, wholly above or across the diagonal is the same
+            // for the warp's 32 rows [32 q, 32 q + 32) unless the chunk meets them: warp-uniform branches.
+            float dO = 0.f;
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4) {
+                const int s = 4 * h + s4;
+                const uint32_t ca = tbase + lane_off + kColSc + 16 * s;
+                uint32_t w[16];
+                if (16 * s > 32 * q + 31) {  // every key of the chunk is after every row: A~ = 0
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) w[k] = 0u;
                 } else {
+                    const bool full = 16 * s + 15 <= 32 * q;  // every key at or before every row
+                    uint32_t v[16];
+                    tmem_ld16(ca, v);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] = 0u;
-                    if (cg == 0) sZ[feat] = 0.f;
+                    for (int k = 0; k < 16; k += 2) {
+                        const int j = 16 * s + k;
+                        const float a0 = (full || j <= r) ? __uint_as_float(v[k]) : 0.f;
+                        const float a1 = (full || j + 1 <= r) ? __uint_as_float(v[k + 1]) : 0.f;
+                        dO += a0 + a1;
+                        const uint32_t hw = pack_bf16(a0, a1);
+                        w[k / 2] = hw;
+                        w[8 + k / 2] = pack_bf16(a0 - __uint_as_float(hw << 16), a1 - __uint_as_float(hw & 0xFFFF0000u));
+                    }
                 }
-                // bf16 snapshot of S row `feat`, columns [16 cg, 16 cg + 16), as hi + lo
+                tmem_st16(ca, w);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_atil);
+            sDenO[h * 128 + r] = dO;
+            // ---- snapshot of the state after this tile's update, for the next tile (lane = feature r)
+            if (t + 1 < T) {
+                const int b1 = (t + 1) & 1;
+                uint32_t sv[32];
+                tmem_ld32(tbase + lane_off + kColS + 32 * h, sv);
+                uint32_t z0 = 0u, z1 = 0u;
+                if (h == 0) tmem_ld2(tbase + lane_off + kColS + 64, z0, z1);
+                tmem_ld_wait();
+                (void)z1;
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < 4; ++c) {
                     float x[8], l[8];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) x[k] = __uint_as_float(v[8 * c + k]);
+                    for (int k = 0; k < 8; ++k) x[k] = __uint_as_float(sv[8 * c + k]);
                     uint4 o;
                     o.x = pack_bf16(x[0], x[1]);
                     o.y = pack_bf16(x[2], x[3]);
@@ -395,179 +571,94 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ol.y = pack_bf16(l[2], l[3]);
                     ol.z = pack_bf16(l[4], l[5]);
                     ol.w = pack_bf16(l[6], l[7]);
-                    *reinterpret_cast<uint4*>(sS + sw128_offset(feat, 2 * cg + c)) = o;
-                    *reinterpret_cast<uint4*>(sSl + sw128_offset(feat, 2 * cg + c)) = ol;
+                    *reinterpret_cast<uint4*>(sS + sw128_offset(r, 4 * h + c)) = o;
+                    *reinterpret_cast<uint4*>(sSl + sw128_offset(r, 4 * h + c)) = ol;
                 }
+                if (h == 0) sZ[b1 * 128 + r] = feat0 + r < p.m ? __uint_as_float(z0) : 0.f;
+                tc_fence_before();
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_snap);
             }
-            tc_fence_before();
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar_snap);
-            named_bar(1, NT);  // z snapshot visible to every epilogue thread
-            // ---- per feature group: phi(Q), phi(K) into shared memory (32 features per warp) ----
-            float den = 0.f;  // this warp's share of the row's denominator
-            for (int g = 0; g < G; ++g) {
-                if (g > 0) {  // the previous group's MMAs have read the phi buffers
-                    failed |= !mbar_wait(&bar_grp, (guse - 1) & 1, &abort_flag);
-                    __syncwarp();
-                }
-                for (int which = 0; which < 2; ++which) {  // 0: queries, 1: keys
-                    failed |= !mbar_wait(&bar_ufull, uuse_e & 1, &abort_flag);
-                    __syncwarp();
-                    tc_fence_after();
-                    ++uuse_e;
-                    uint32_t v[32];
-                    tmem_ld32(tbase + lane_off + kColU + 32 * cg, v);
-                    tmem_ld_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bar_ufree);  // U has been read: the next projection may overwrite it
-                    uint8_t* dst = which == 0 ? sPQ : sPK;
-                    const float cst = which == 0 ? cq : ck;
-                    const bool zero_row = which == 1 && !valid;
-                    const int f0 = g * 128 + 32 * cg;  // this CTA's feature index
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        float ph[8];
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            const float a = __uint_as_float(v[8 * c + k]);
-                            float x = exp_kind ? ex2(fmaf(a, A2, -cst)) : fmaxf(a * p.scale, 0.f) + p.relu_eps_s;
-                            if (zero_row || feat0 + f0 + 8 * c + k >= p.m) x = 0.f;
-                            ph[k] = x;
-                        }
-                        uint4 o;
-                        o.x = pack_bf16(ph[0], ph[1]);
-                        o.y = pack_bf16(ph[2], ph[3]);
-                        o.z = pack_bf16(ph[4], ph[5]);
-                        o.w = pack_bf16(ph[6], ph[7]);
-                        *reinterpret_cast<uint4*>(dst + (cg >> 1) * 16384 + sw128_offset(r, (cg & 1) * 4 + c)) = o;
-                        if (which == 0) {  // den: phi(q) . z_<t with the bf16-rounded features
-                            const float4 za = *reinterpret_cast<const float4*>(sZ + f0 + 8 * c);
-                            const float4 zb = *reinterpret_cast<const float4*>(sZ + f0 + 8 * c + 4);
-                            den = fmaf(__uint_as_float(o.x << 16), za.x, den);
-                            den = fmaf(__uint_as_float(o.x & 0xFFFF0000u), za.y, den);
-                            den = fmaf(__uint_as_float(o.y << 16), za.z, den);
-                            den = fmaf(__uint_as_float(o.y & 0xFFFF0000u), za.w, den);
-                            den = fmaf(__uint_as_float(o.z << 16), zb.x, den);
-                            den = fmaf(__uint_as_float(o.z & 0xFFFF0000u), zb.y, den);
-                            den = fmaf(__uint_as_float(o.w << 16), zb.z, den);
-                            den = fmaf(__uint_as_float(o.w & 0xFFFF0000u), zb.w, den);
-                        }
-                    }
-                    fence_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(which == 0 ? &bar_phq : &bar_phk);
-                }
-                ++guse;
-            }
-            // ---- masked scores (keys [32 cg, 32 cg + 32) of row r) -> A~ hi (phi(K) buffer), lo (phi(Q) buffer) ----
-            failed |= !mbar_wait(&bar_grp, (guse - 1) & 1, &abort_flag);
-            __syncwarp();
-            tc_fence_after();
-            {
-                uint32_t v[32];
-                tmem_ld32(tbase + lane_off + kColSc + 32 * cg, v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float a[8];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        a[k] = (32 * cg + 8 * c + k <= r) ? __uint_as_float(v[8 * c + k]) : 0.f;
-                        den += a[k];
-                    }
-                    // A~ = hi + lo, both bf16: the intra-tile weights keep about 16 significant bits.
-                    uint4 o, ol;
-                    o.x = pack_bf16(a[0], a[1]);
-                    o.y = pack_bf16(a[2], a[3]);
-                    o.z = pack_bf16(a[4], a[5]);
-                    o.w = pack_bf16(a[6], a[7]);
-                    ol.x = pack_bf16(a[0] - __uint_as_float(o.x << 16), a[1] - __uint_as_float(o.x & 0xFFFF0000u));
-                    ol.y = pack_bf16(a[2] - __uint_as_float(o.y << 16), a[3] - __uint_as_float(o.y & 0xFFFF0000u));
-                    ol.z = pack_bf16(a[4] - __uint_as_float(o.z << 16), a[5] - __uint_as_float(o.z & 0xFFFF0000u));
-                    ol.w = pack_bf16(a[6] - __uint_as_float(o.w << 16), a[7] - __uint_as_float(o.w & 0xFFFF0000u));
-                    const uint32_t off = (cg >> 1) * 16384 + sw128_offset(r, (cg & 1) * 4 + c);
-                    *reinterpret_cast<uint4*>(sPK + off) = o;
-                    *reinterpret_cast<uint4*>(sPQ + off) = ol;
-                }
-            }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar_atil);
-            sDen[cg * 128 + r] = den;
-            named_bar(1, NT);  // denominator shares visible
-            const float den_row = ((sDen[r] + sDen[128 + r]) + sDen[256 + r]) + sDen[384 + r];
-            // ---- y = num / den, output columns [16 cg, 16 cg + 16) ----
+            // ---- output of tile t: columns [32 h, 32 h + 32) of row r
             failed |= !mbar_wait(&bar_num, t & 1, &abort_flag);
+            failed |= !mbar_wait(&bar_den[b], (t >> 1) & 1, &abort_flag);
             __syncwarp();
             tc_fence_after();
-            uint32_t v[16];
-            tmem_ld16(tbase + lane_off + kColNum + 16 * cg, v);
+            uint32_t nv[32];
+            tmem_ld32(tbase + lane_off + kColNum + 64 * b + 32 * h, nv);
             tmem_ld_wait();
+            named_bar(2, NO);  // both halves' score row sums are visible
+            const float den = ((sDenF[(b * 2) * 128 + r] + sDenF[(b * 2 + 1) * 128 + r]) + sDenO[r]) + sDenO[128 + r];
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar_dfree);
-            float num[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) num[i] = __uint_as_float(v[i]);
-            float dsum = den_row;
+            if (lane == 0) mbar_arrive(&bar_dfree[b]);  // numerator buffer b and its den shares are free
+            float dsum = den;
             const int owner = r / RP;
+            const int i_tok = t * kTile + r;
+            const bool valid = i_tok < p.n;
             if (CS > 1) {
-                // Partial sums of row r go to the CTA that finalises it, through its phi(Q) buffer
-                // (idle once this tile's intra MMA is done): slot [sender][row][kXStride floats]; the odd
-                // number of 16-byte groups per row keeps a warp's float4 accesses free of bank conflicts.
-                if (ew == 0 && lane == 0)
+                // Partial sums of row r go to the CTA that finalises it: slot [sender][row][kXStride
+                // floats]; the odd number of 16-byte groups per row keeps a warp's float4 accesses
+                // free of bank conflicts. Every output warp of this CTA is past its reads of the
+                // previous tile's slots (named barrier above), so its buffer may be refilled.
+                if (ow == 0 && lane == 0)
                     for (int c = 0; c < CS; ++c)
                         if (c != rank) mbar_arrive_cluster(mapa(smem_u32(&bar_xfree), c));
                 if (owner != rank) {
                     failed |= !mbar_wait_cluster(&bar_xfree, t & 1, &abort_flag);
                     __syncwarp();
                     const int slot = rank < owner ? rank : rank - 1;
-                    float* dstp = reinterpret_cast<float*>(sPQ) + ((size_t)slot * RP + (r - owner * RP)) * kXStride + 16 * cg;
-                    const uint32_t ca = mapa(smem_u32(dstp), owner);
+                    float* rowp = sX + ((size_t)slot * RP + (r - owner * RP)) * kXStride;
+                    const uint32_t ca = mapa(smem_u32(rowp + 32 * h), owner);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        st_cluster_v4(ca + 16 * c, make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]));
-                    if (cg == 0) st_cluster_f32(mapa(smem_u32(reinterpret_cast<float*>(sPQ) + ((size_t)slot * RP + (r - owner * RP)) * kXStride + 64), owner), den_row);
+                    for (int c = 0; c < 8; ++c)
+                        st_cluster_v4(ca + 16 * c, make_uint4(nv[4 * c], nv[4 * c + 1], nv[4 * c + 2], nv[4 * c + 3]));
+                    if (h == 0) st_cluster_f32(mapa(smem_u32(rowp + 64), owner), den);
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(mapa(smem_u32(&bar_xfull), owner));
                 } else {
                     failed |= !mbar_wait_cluster(&bar_xfull, t & 1, &abort_flag);
                     __syncwarp();
                     // sum the cluster's contributions in rank order (deterministic)
-                    float acc[16];
+                    float acc[32];
                     float dacc = 0.f;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+                    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
                     for (int c = 0; c < CS; ++c) {
                         if (c == rank) {
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) acc[i] += num[i];
-                            dacc += den_row;
+                            for (int i = 0; i < 32; ++i) acc[i] += __uint_as_float(nv[i]);
+                            dacc += den;
                         } else {
                             const int slot = c < rank ? c : c - 1;
-                            const float* src = reinterpret_cast<const float*>(sPQ) + ((size_t)slot * RP + (r - rank * RP)) * kXStride;
+                            const float* src = sX + ((size_t)slot * RP + (r - rank * RP)) * kXStride;
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) acc[i] += src[16 * cg + i];
+                            for (int i = 0; i < 32; i += 4) {
+                                const float4 x4 = *reinterpret_cast<const float4*>(src + 32 * h + i);
+                                acc[i] += x4.x;
+                                acc[i + 1] += x4.y;
+                                acc[i + 2] += x4.z;
+                                acc[i + 3] += x4.w;
+                            }
                             dacc += src[64];
                         }
                     }
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) num[i] = acc[i];
+                    for (int i = 0; i < 32; ++i) nv[i] = __float_as_uint(acc[i]);
                     dsum = dacc;
                 }
             }
             if (valid && owner == rank) {
                 const float inv = 1.f / dsum;
-                uint4* dst = reinterpret_cast<uint4*>(p.Y + ((size_t)bh * p.n + i_tok) * kD + 16 * cg);
+                uint4* dst = reinterpret_cast<uint4*>(p.Y + ((size_t)bh * p.n + i_tok) * kD + 32 * h);
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < 4; ++c) {
                     uint4 o;
-                    o.x = pack_bf16(num[8 * c + 0] * inv, num[8 * c + 1] * inv);
-                    o.y = pack_bf16(num[8 * c + 2] * inv, num[8 * c + 3] * inv);
-                    o.z = pack_bf16(num[8 * c + 4] * inv, num[8 * c + 5] * inv);
-                    o.w = pack_bf16(num[8 * c + 6] * inv, num[8 * c + 7] * inv);
+                    o.x = pack_bf16(__uint_as_float(nv[8 * c + 0]) * inv, __uint_as_float(nv[8 * c + 1]) * inv);
+                    o.y = pack_bf16(__uint_as_float(nv[8 * c + 2]) * inv, __uint_as_float(nv[8 * c + 3]) * inv);
+                    o.z = pack_bf16(__uint_as_float(nv[8 * c + 4]) * inv, __uint_as_float(nv[8 * c + 5]) * inv);
+                    o.w = pack_bf16(__uint_as_float(nv[8 * c + 6]) * inv, __uint_as_float(nv[8 * c + 7]) * inv);
                     dst[c] = o;
                 }
             }
