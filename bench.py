@@ -46,7 +46,11 @@ FP32_SIMT_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the committed ncu
 # captures, valid only while the kernel sources hash to `src`.
-NCU_TRAFFIC: dict[str, dict] = {}
+NCU_TRAFFIC: dict[str, dict] = {
+    # dram__bytes_read.sum + dram__bytes_write.sum of one launch (ncu --set full, see
+    # profiles/nc_fused_noncausal_bf16_B1H8n1024d64m256.md); "src" is kernel_source_hash("fused")
+    "noncausal_bf16_B1H8n1024d64m256:fused": {"bytes": 3258368 + 0, "src": "6deefdb29780a336"},
+}
 
 
 def load_peaks() -> tuple[dict, str]:
@@ -57,10 +61,20 @@ def load_peaks() -> tuple[dict, str]:
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
 
 
-def kernel_source_hash() -> str:
+# The source files each kernel is compiled from (its traffic figure is void once any of them changes).
+KERNEL_SOURCES = {
+    "fused": ["tc.cuh", "tc_noncausal.cuh", "tc_fused.cuh"],
+    "state": ["tc.cuh", "tc_noncausal.cuh"], "combine": ["tc.cuh", "tc_noncausal.cuh"],
+    "readout": ["tc.cuh", "tc_noncausal.cuh"],
+    "causal": ["tc.cuh", "tc_noncausal.cuh", "tc_causal.cuh", "tc_causal_wide.cuh"],
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "kernelized_linear_attention_04_b300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    names = KERNEL_SOURCES.get(kernel) or sorted(os.listdir(csrc))
+    for name in names:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -388,7 +402,7 @@ def run_ours(args, w):
         ach, peak, unit, bound, note = nbytes / (dom_ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s", "hbm", f"HBM copy, {peak_kind}"
     else:
         ach, peak, unit, bound, note = flops / (dom_ms * 1e-3) / 1e12, cmp_peak, cmp_unit, cmp_bound, cmp_note
-    src = kernel_source_hash()
+    src = kernel_source_hash(dom)
     tr_entry = NCU_TRAFFIC.get(f"{w.name}:{dom}")
     traffic = tr_entry["bytes"] if tr_entry and tr_entry.get("src") == src else None
     roofline = {"bound": bound, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,

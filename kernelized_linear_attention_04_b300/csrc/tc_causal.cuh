@@ -13,9 +13,9 @@
 //
 // The tiles run as a software pipeline over four roles:
 //   warp 0      TMA producer: Q, K (single buffers) and V (two buffers) of the coming tiles;
-//   warp 1      MMA issuer, in the order [scores(t), inter(t), state(t)] [proj Q(t+1), proj K(t+1)]
-//               [intra(t)], so that the next tile's projections run while tile t's masked scores
-//               are formed;
+//   warp 1      MMA issuer, in the order [proj Q(t+1)] [scores(t), inter(t), state(t)] [proj K(t+1)]
+//               [intra(t)], so that phi(Q_{t+1}) is computed while tile t's MMAs run and the next
+//               keys are projected while tile t's masked scores are formed;
 //   warps 2-9   feature team: phi(Q_t), phi(K_t) from the projections (TMEM) into shared memory, and
 //               the inter-tile part of the denominator, phi(q) . z_<t;
 //   warps 10-17 output team: the masked scores A~ (converted in place in TMEM into bf16 hi + lo, the
@@ -296,6 +296,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int b = t & 1;
                 const uint8_t* vt = sV0 + b * kTileBytes;
                 const uint32_t nb = tbase + kColNum + 64 * b;
+                // projection of the next tile's queries as soon as U is free (the feature team has read
+                // tile t's keys from it), so that phi(Q_{t+1}) is computed while tile t's MMAs run
+                if (t + 1 < T && !(ok = proj(sQ, &bar_qfull, (t + 1) & 1))) break;
                 ok = mbar_wait(&bar_phq, t & 1, &abort_flag) && mbar_wait(&bar_phk, t & 1, &abort_flag) &&
                      mbar_wait(&bar_snap, t & 1, &abort_flag) &&
                      mbar_wait(&bar_dfree[b], ((t >> 1) & 1) ^ 1, &abort_flag) &&
@@ -336,10 +339,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_ss(tbase + kColS + 64, ad, bd, id_z, t > 0 || ks > 0);
                 }
                 mma_commit(&bar_grp);
-                // projections of the next tile while the output team forms A~
+                // projection of the next tile's keys while the output team forms A~
                 if (t + 1 < T) {
-                    ok = proj(sQ, &bar_qfull, (t + 1) & 1) && proj(sK, &bar_kfull, (t + 1) & 1);
-                    if (!ok) break;
+                    if (!(ok = proj(sK, &bar_kfull, (t + 1) & 1))) break;
                     mma_commit(&bar_qkempty);
                 }
                 // intra numerator: Num += (A~hi + A~lo) V_t, A from TMEM (K = 128 keys)
@@ -368,42 +370,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool failed = false;
         int pu = 0;  // projections consumed
         const int fvalid = p.m - (feat0 + 64 * h);  // real (not padding) features among this warp's 64
-        // phi of the 64 projections in v into row r of `dst` (K-major, atom region h). For exp
-        // features a row that must be zero gets cst = +inf (ex2(-inf) = 0); the per-feature padding
-        // test is skipped when all 64 features are real (a warp-uniform branch).
-        auto write_phi = [&](uint8_t* dst, const uint32_t (&v)[64], float cst, bool zero_row) {
+        // phi of the 64 projections in v, as 32 packed bf16 pairs. For exp features a row that must
+        // be zero gets cst = +inf (ex2(-inf) = 0); the per-feature padding test is skipped when all 64
+        // features are real (a warp-uniform branch).
+        auto make_phi = [&](uint32_t (&w)[32], const uint32_t (&v)[64], float cst, bool zero_row) {
             if (exp_kind && fvalid >= 64) {
                 const float c = zero_row ? INFINITY : cst;
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        float x0 = __uint_as_float(v[8 * ch + 2 * k]), x1 = __uint_as_float(v[8 * ch + 2 * k + 1]);
-                        fma2(x0, x1, A2, -c);
-                        w[k] = pack_bf16(ex2(x0), ex2(x1));
-                    }
-                    *reinterpret_cast<uint4*>(dst + h * 16384 + sw128_offset(r, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
+                for (int k = 0; k < 32; ++k) {
+                    float x0 = __uint_as_float(v[2 * k]), x1 = __uint_as_float(v[2 * k + 1]);
+                    fma2(x0, x1, A2, -c);
+                    w[k] = pack_bf16(ex2(x0), ex2(x1));
                 }
                 return;
             }
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                float ph[8];
+            for (int k = 0; k < 32; ++k) {
+                float x[2];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float a = __uint_as_float(v[8 * ch + k]);
-                    float x = exp_kind ? ex2(fmaf(a, A2, -cst)) : fmaxf(a * p.scale, 0.f) + p.relu_eps_s;
-                    if (zero_row || 8 * ch + k >= fvalid) x = 0.f;
-                    ph[k] = x;
+                for (int e = 0; e < 2; ++e) {
+                    const float a = __uint_as_float(v[2 * k + e]);
+                    x[e] = exp_kind ? ex2(fmaf(a, A2, -cst)) : fmaxf(a * p.scale, 0.f) + p.relu_eps_s;
+                    if (zero_row || 2 * k + e >= fvalid) x[e] = 0.f;
                 }
-                uint4 o;
-                o.x = pack_bf16(ph[0], ph[1]);
-                o.y = pack_bf16(ph[2], ph[3]);
-                o.z = pack_bf16(ph[4], ph[5]);
-                o.w = pack_bf16(ph[6], ph[7]);
-                *reinterpret_cast<uint4*>(dst + h * 16384 + sw128_offset(r, ch)) = o;
+                w[k] = pack_bf16(x[0], x[1]);
             }
+        };
+        // row r of `dst` (K-major, atom region h)
+        auto store_phi = [&](uint8_t* dst, const uint32_t (&w)[32]) {
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+                *reinterpret_cast<uint4*>(dst + h * 16384 + sw128_offset(r, ch)) =
+                    make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
         };
         auto load_u = [&](uint32_t (&v)[64]) {
             tmem_ld32(tbase + lane_off + kColU + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(v));
@@ -433,11 +431,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             uint32_t v[64];
             load_u(v);
+            uint32_t pq[32];
+            make_phi(pq, v, cq, false);
             if (t > 0) {  // the MMAs of tile t-1 have read the phi buffers
                 failed |= !mbar_wait(&bar_grp, (t - 1) & 1, &abort_flag);
                 __syncwarp();
             }
-            write_phi(sPQ, v, cq, false);
+            store_phi(sPQ, pq);
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_phq);
@@ -471,7 +471,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             tc_fence_after();
             load_u(v);
-            write_phi(sPK, v, ck, !valid);
+            make_phi(pq, v, ck, !valid);
+            store_phi(sPK, pq);
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_phk);
