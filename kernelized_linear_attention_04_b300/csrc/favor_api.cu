@@ -272,7 +272,8 @@ favor_status_t simt_noncausal(const void* Q, const void* K, const void* V, const
             pS, pz, pst);
     }));
     FAVOR_TRY(traced(FAVOR_KERNEL_COMBINE, s, [&] {
-        combine_kernel<D><<<BH, kThreads, 0, s>>>(pS, pz, pst, splits, m, S, z);
+        combine_kernel<D><<<dim3(BH, (m * D + kCombineChunk - 1) / kCombineChunk), kThreads, 0, s>>>(pS, pz, pst, splits,
+                                                                                              m, S, z);
     }));
     size_t smem_read = sizeof(float) * (kTok * D + kOmChunk * (D + 1) + kTok * m + 2 * kTok);
     auto kread = readout_kernel<T, D>;

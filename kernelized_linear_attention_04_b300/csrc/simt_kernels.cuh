@@ -232,12 +232,16 @@ __global__ void __launch_bounds__(kThreads) state_kernel(const T* __restrict__ K
 }
 
 // Sums the partial states of one head: S = sum_s exp(stab_s - M) S_s (fixed order), same for z.
+// Grid: (head, chunk of kCombineChunk elements of S); chunk 0 also sums z.
+constexpr int kCombineChunk = 1024;
 template <int D>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const float* __restrict__ pS, const float* __restrict__ pz,
                                                            const float* __restrict__ pstab, int splits, int m,
                                                            float* __restrict__ S, float* __restrict__ z) {
     __shared__ float wts[64 * 8];             // splits * slices weights (<= 64 splits, <= 8 slices)
     const int64_t bh = blockIdx.x;
+    const int e0 = blockIdx.y * kCombineChunk;
+    const int e1 = min(m * D, e0 + kCombineChunk);
     const int slices = m / kSlice;
     const float* st = pstab + bh * splits * slices;
     float M = -INFINITY;
@@ -245,12 +249,13 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const float* __restri
     for (int i = threadIdx.x; i < splits * slices; i += kThreads)
         wts[i] = st[i] == -INFINITY ? 0.f : exp_shift(st[i], M);
     __syncthreads();
-    for (int e = threadIdx.x; e < m * D; e += kThreads) {
+    for (int e = e0 + threadIdx.x; e < e1; e += kThreads) {
         int r = e / D;
         float acc = 0.f;
         for (int s = 0; s < splits; ++s) acc = fmaf(wts[s * slices + r / kSlice], pS[((bh * splits + s) * m) * D + e], acc);
         S[bh * m * D + e] = acc;
     }
+    if (blockIdx.y != 0) return;
     for (int r = threadIdx.x; r < m; r += kThreads) {
         float acc = 0.f;
         for (int s = 0; s < splits; ++s) acc = fmaf(wts[s * slices + r / kSlice], pz[(bh * splits + s) * m + r], acc);
@@ -310,10 +315,17 @@ __global__ void __launch_bounds__(kThreads) readout_kernel(const T* __restrict__
     const int c = threadIdx.x % D;
     for (int t = threadIdx.x / D; t < kTok; t += kThreads / D) {
         int64_t row = t0 + t;
-        float acc = 0.f;
+        // four independent partial sums keep several loads of S in flight (m is a multiple of 64)
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
         const float* pr = ps + t * m;
-#pragma unroll 8
-        for (int r = 0; r < m; ++r) acc = fmaf(pr[r], S[(int64_t)r * D + c], acc);
+#pragma unroll 4
+        for (int r = 0; r < m; r += 4) {
+            a0 = fmaf(pr[r], S[(int64_t)r * D + c], a0);
+            a1 = fmaf(pr[r + 1], S[(int64_t)(r + 1) * D + c], a1);
+            a2 = fmaf(pr[r + 2], S[(int64_t)(r + 2) * D + c], a2);
+            a3 = fmaf(pr[r + 3], S[(int64_t)(r + 3) * D + c], a3);
+        }
+        const float acc = (a0 + a1) + (a2 + a3);
         if (row < n) store_elem(Y + row * D + c, acc / den[t]);
     }
 }

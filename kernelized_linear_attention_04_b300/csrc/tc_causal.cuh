@@ -370,31 +370,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool failed = false;
         int pu = 0;  // projections consumed
         const int fvalid = p.m - (feat0 + 64 * h);  // real (not padding) features among this warp's 64
-        // phi of the 64 projections in v, as 32 packed bf16 pairs. For exp features a row that must
-        // be zero gets cst = +inf (ex2(-inf) = 0); the per-feature padding test is skipped when all 64
+        // phi of this warp's 64 projections in U, as 32 packed bf16 pairs, read in two halves of 32
+        // columns (U is released once the second half is loaded). For exp features a row that must be
+        // zero gets cst = +inf (ex2(-inf) = 0); the per-feature padding test is skipped when all 64
         // features are real (a warp-uniform branch).
-        auto make_phi = [&](uint32_t (&w)[32], const uint32_t (&v)[64], float cst, bool zero_row) {
-            if (exp_kind && fvalid >= 64) {
-                const float c = zero_row ? INFINITY : cst;
+        auto phi_from_u = [&](uint32_t (&w)[32], float cst, bool zero_row) {
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    float x0 = __uint_as_float(v[2 * k]), x1 = __uint_as_float(v[2 * k + 1]);
-                    fma2(x0, x1, A2, -c);
-                    w[k] = pack_bf16(ex2(x0), ex2(x1));
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t v[32];
+                tmem_ld32(tbase + lane_off + kColU + 64 * h + 32 * hh, v);
+                tmem_ld_wait();
+                if (hh == 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar_ufree);  // the next projection may overwrite U
                 }
-                return;
-            }
+                if (exp_kind && fvalid >= 64) {
+                    const float c = zero_row ? INFINITY : cst;
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                float x[2];
+                    for (int k = 0; k < 16; ++k) {
+                        float x0 = __uint_as_float(v[2 * k]), x1 = __uint_as_float(v[2 * k + 1]);
+                        fma2(x0, x1, A2, -c);
+                        w[16 * hh + k] = pack_bf16(ex2(x0), ex2(x1));
+                    }
+                } else {
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float a = __uint_as_float(v[2 * k + e]);
-                    x[e] = exp_kind ? ex2(fmaf(a, A2, -cst)) : fmaxf(a * p.scale, 0.f) + p.relu_eps_s;
-                    if (zero_row || 2 * k + e >= fvalid) x[e] = 0.f;
+                    for (int k = 0; k < 16; ++k) {
+                        float x[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const float a = __uint_as_float(v[2 * k + e]);
+                            x[e] = exp_kind ? ex2(fmaf(a, A2, -cst)) : fmaxf(a * p.scale, 0.f) + p.relu_eps_s;
+                            if (zero_row || 32 * hh + 2 * k + e >= fvalid) x[e] = 0.f;
+                        }
+                        w[16 * hh + k] = pack_bf16(x[0], x[1]);
+                    }
                 }
-                w[k] = pack_bf16(x[0], x[1]);
             }
+            ++pu;
         };
         // row r of `dst` (K-major, atom region h)
         auto store_phi = [&](uint8_t* dst, const uint32_t (&w)[32]) {
@@ -402,15 +415,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int ch = 0; ch < 8; ++ch)
                 *reinterpret_cast<uint4*>(dst + h * 16384 + sw128_offset(r, ch)) =
                     make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
-        };
-        auto load_u = [&](uint32_t (&v)[64]) {
-            tmem_ld32(tbase + lane_off + kColU + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(v));
-            tmem_ld32(tbase + lane_off + kColU + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-            tmem_ld_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar_ufree);  // U has been read: the next projection may overwrite it
-            ++pu;
         };
         for (int t = 0; t < T; ++t) {
             const int b = t & 1;
@@ -429,10 +433,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 cq = W * sqrtf(qn2) * kLog2e;
                 ck = (0.5f * kn2 + stab) * kLog2e;
             }
-            uint32_t v[64];
-            load_u(v);
             uint32_t pq[32];
-            make_phi(pq, v, cq, false);
+            phi_from_u(pq, cq, false);
             if (t > 0) {  // the MMAs of tile t-1 have read the phi buffers
                 failed |= !mbar_wait(&bar_grp, (t - 1) & 1, &abort_flag);
                 __syncwarp();
@@ -470,8 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             failed |= !mbar_wait(&bar_ufull, pu & 1, &abort_flag);
             __syncwarp();
             tc_fence_after();
-            load_u(v);
-            make_phi(pq, v, ck, !valid);
+            phi_from_u(pq, ck, !valid);
             store_phi(sPK, pq);
             fence_async_smem();
             __syncwarp();
@@ -621,32 +622,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     failed |= !mbar_wait_cluster(&bar_xfull, t & 1, &abort_flag);
                     __syncwarp();
-                    // sum the cluster's contributions in rank order (deterministic)
-                    float acc[32];
-                    float dacc = 0.f;
+                    // add the peers' contributions to this CTA's own, peers in rank order (a fixed
+                    // order: the result is bitwise reproducible)
+                    float dacc = den;
+                    for (int slot = 0; slot < CS - 1; ++slot) {
+                        const float* src = sX + ((size_t)slot * RP + (r - rank * RP)) * kXStride;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-                    for (int c = 0; c < CS; ++c) {
-                        if (c == rank) {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) acc[i] += __uint_as_float(nv[i]);
-                            dacc += den;
-                        } else {
-                            const int slot = c < rank ? c : c - 1;
-                            const float* src = sX + ((size_t)slot * RP + (r - rank * RP)) * kXStride;
-#pragma unroll
-                            for (int i = 0; i < 32; i += 4) {
-                                const float4 x4 = *reinterpret_cast<const float4*>(src + 32 * h + i);
-                                acc[i] += x4.x;
-                                acc[i + 1] += x4.y;
-                                acc[i + 2] += x4.z;
-                                acc[i + 3] += x4.w;
-                            }
-                            dacc += src[64];
+                        for (int i = 0; i < 32; i += 4) {
+                            const float4 x4 = *reinterpret_cast<const float4*>(src + 32 * h + i);
+                            nv[i] = __float_as_uint(__uint_as_float(nv[i]) + x4.x);
+                            nv[i + 1] = __float_as_uint(__uint_as_float(nv[i + 1]) + x4.y);
+                            nv[i + 2] = __float_as_uint(__uint_as_float(nv[i + 2]) + x4.z);
+                            nv[i + 3] = __float_as_uint(__uint_as_float(nv[i + 3]) + x4.w);
                         }
+                        dacc += src[64];
                     }
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) nv[i] = __float_as_uint(acc[i]);
                     dsum = dacc;
                 }
             }

@@ -396,43 +396,37 @@ __global__ void __launch_bounds__(kStateThreads, 1)
                 __syncwarp();
                 tc_fence_after();
                 const uint32_t ua = tbase + lane_off + u_col(s) + 64 * cg;
-                uint32_t v[64];
-                tmem_ld32(ua, *reinterpret_cast<uint32_t(*)[32]>(v));
-                tmem_ld32(ua + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-                tmem_ld_wait();
                 float zs0 = 0.f, zs1 = 0.f;
+                // Two halves of 32 tokens: load, map, pack, store. The packed phi of half hh goes to
+                // columns [16 hh, 16 hh + 16) of this warp's own 64, which the loads of half 0 have
+                // already consumed: no other warp reads them.
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    float ph[32];
-                    const uint32_t* vv = v + 32 * hh;
+                    uint32_t vv[32];
+                    tmem_ld32(ua + 32 * hh, vv);
+                    tmem_ld_wait();
                     const float* cc = cj + 32 * hh;
-                    if (p.kind == kKindExp) {
-#pragma unroll
-                        for (int i = 0; i < 32; i += 4) {
-                            const float4 c4 = *reinterpret_cast<const float4*>(cc + i);
-                            ph[i + 0] = ex2(fmaf(__uint_as_float(vv[i + 0]), A2, -c4.x));
-                            ph[i + 1] = ex2(fmaf(__uint_as_float(vv[i + 1]), A2, -c4.y));
-                            ph[i + 2] = ex2(fmaf(__uint_as_float(vv[i + 2]), A2, -c4.z));
-                            ph[i + 3] = ex2(fmaf(__uint_as_float(vv[i + 3]), A2, -c4.w));
-                        }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; i += 4) {
-                            const float4 c4 = *reinterpret_cast<const float4*>(cc + i);
-                            ph[i + 0] = c4.x == 0.f ? fmaxf(__uint_as_float(vv[i + 0]) * p.scale, 0.f) + p.relu_eps_s : 0.f;
-                            ph[i + 1] = c4.y == 0.f ? fmaxf(__uint_as_float(vv[i + 1]) * p.scale, 0.f) + p.relu_eps_s : 0.f;
-                            ph[i + 2] = c4.z == 0.f ? fmaxf(__uint_as_float(vv[i + 2]) * p.scale, 0.f) + p.relu_eps_s : 0.f;
-                            ph[i + 3] = c4.w == 0.f ? fmaxf(__uint_as_float(vv[i + 3]) * p.scale, 0.f) + p.relu_eps_s : 0.f;
-                        }
-                    }
                     uint32_t pk[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        pk[i] = pack_bf16(ph[2 * i], ph[2 * i + 1]);
-                        zs0 += ph[2 * i];
-                        zs1 += ph[2 * i + 1];
+                    for (int i = 0; i < 32; i += 4) {
+                        const float4 c4 = *reinterpret_cast<const float4*>(cc + i);
+                        float f[4];
+                        if (p.kind == kKindExp) {
+                            f[0] = ex2(fmaf(__uint_as_float(vv[i + 0]), A2, -c4.x));
+                            f[1] = ex2(fmaf(__uint_as_float(vv[i + 1]), A2, -c4.y));
+                            f[2] = ex2(fmaf(__uint_as_float(vv[i + 2]), A2, -c4.z));
+                            f[3] = ex2(fmaf(__uint_as_float(vv[i + 3]), A2, -c4.w));
+                        } else {
+                            f[0] = c4.x == 0.f ? fmaxf(__uint_as_float(vv[i + 0]) * p.scale, 0.f) + p.relu_eps_s : 0.f;
+                            f[1] = c4.y == 0.f ? fmaxf(__uint_as_float(vv[i + 1]) * p.scale, 0.f) + p.relu_eps_s : 0.f;
+                            f[2] = c4.z == 0.f ? fmaxf(__uint_as_float(vv[i + 2]) * p.scale, 0.f) + p.relu_eps_s : 0.f;
+                            f[3] = c4.w == 0.f ? fmaxf(__uint_as_float(vv[i + 3]) * p.scale, 0.f) + p.relu_eps_s : 0.f;
+                        }
+                        pk[i / 2] = pack_bf16(f[0], f[1]);
+                        pk[i / 2 + 1] = pack_bf16(f[2], f[3]);
+                        zs0 += f[0] + f[2];
+                        zs1 += f[1] + f[3];
                     }
-                    // Packed phi goes to the first 32 columns of this warp's own 64: no other warp reads them.
                     tmem_st16(ua + 16 * hh, pk);
                 }
                 if (g == 0) zacc[0] += zs0 + zs1;
