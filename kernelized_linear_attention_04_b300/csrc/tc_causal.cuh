@@ -13,9 +13,10 @@
 //
 // The tiles run as a software pipeline over four roles:
 //   warp 0      TMA producer: Q, K (single buffers) and V (two buffers) of the coming tiles;
-//   warp 1      MMA issuer, in the order [proj Q(t+1)] [scores(t), inter(t), state(t)] [proj K(t+1)]
-//               [intra(t)], so that phi(Q_{t+1}) is computed while tile t's MMAs run and the next
-//               keys are projected while tile t's masked scores are formed;
+//   warp 1      MMA issuer, in the order [inter(t)] [intra(t-1)] [proj Q(t+1)] [scores(t), state(t)]
+//               [proj K(t+1)]: the inter numerator runs while phi(K_t) is formed, the previous
+//               tile's intra numerator as soon as its masked scores are in place, and phi(Q_{t+1})
+//               is computed while tile t's MMAs run;
 //   warps 2-9   feature team: phi(Q_t), phi(K_t) from the projections (TMEM) into shared memory, and
 //               the inter-tile part of the denominator, phi(q) . z_<t;
 //   warps 10-17 output team: the masked scores A~ (converted in place in TMEM into bf16 hi + lo, the
@@ -288,6 +289,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++pu;
                 return true;
             };
+            // intra numerator of tile u: Num += (A~hi + A~lo) V_u, A from TMEM (K = 128 keys); A~ must be
+            // consumed before the next scores MMA overwrites it
+            auto intra = [&](int u) -> bool {
+                if (!mbar_wait(&bar_atil, u & 1, &abort_flag)) return false;
+                tc_fence_after();
+                const uint8_t* vu = sV0 + (u & 1) * kTileBytes;
+                const uint32_t nu = tbase + kColNum + 64 * (u & 1);
+                for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        uint64_t bd = sdesc_sw128(smem_u32(vu + ks * 2048), 16, 1024);
+                        mma_ts(nu, tbase + kColSc + 16 * ks + 8 * part, bd, id_num, 1);
+                    }
+                }
+                mma_commit(&bar_num);
+                mma_commit(&bar_vempty[u & 1]);
+                return true;
+            };
             if (T > 0) {
                 ok = proj(sQ, &bar_qfull, 0) && proj(sK, &bar_kfull, 0);
                 if (ok) mma_commit(&bar_qkempty);
@@ -296,24 +315,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int b = t & 1;
                 const uint8_t* vt = sV0 + b * kTileBytes;
                 const uint32_t nb = tbase + kColNum + 64 * b;
-                // projection of the next tile's queries as soon as U is free (the feature team has read
-                // tile t's keys from it), so that phi(Q_{t+1}) is computed while tile t's MMAs run
-                if (t + 1 < T && !(ok = proj(sQ, &bar_qfull, (t + 1) & 1))) break;
-                ok = mbar_wait(&bar_phq, t & 1, &abort_flag) && mbar_wait(&bar_phk, t & 1, &abort_flag) &&
-                     mbar_wait(&bar_snap, t & 1, &abort_flag) &&
-                     mbar_wait(&bar_dfree[b], ((t >> 1) & 1) ^ 1, &abort_flag) &&
-                     mbar_wait(&bar_vfull[b], (t >> 1) & 1, &abort_flag);
+                // inter numerator phi(Q) (S_hi + S_lo) (the state as taken at the tile start) as soon
+                // as phi(Q) and the snapshot are in place: it runs while phi(K) is formed
+                ok = mbar_wait(&bar_phq, t & 1, &abort_flag) && mbar_wait(&bar_snap, t & 1, &abort_flag) &&
+                     mbar_wait(&bar_dfree[b], ((t >> 1) & 1) ^ 1, &abort_flag);
                 if (!ok) break;
                 tc_fence_after();
-                // scores (K = 128 features, two K atoms)
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const int a = ks / 4, w = ks % 4;
-                    uint64_t ad = sdesc_sw128(smem_u32(sPQ + a * 16384 + w * 32), 16, 1024);
-                    uint64_t bd = sdesc_sw128(smem_u32(sPK + a * 16384 + w * 32), 16, 1024);
-                    mma_ss(tbase + kColSc, ad, bd, id_sc, ks > 0);
-                }
-                // inter numerator: phi(Q) (S_hi + S_lo), the state as taken at the tile start
                 for (int part = 0; part < 2; ++part) {
                     const uint8_t* sp = part == 0 ? sS : sSl;
 #pragma unroll
@@ -323,6 +330,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint64_t bd = sdesc_sw128(smem_u32(sp + ks * 16 * 128), 16, 1024);
                         mma_ss(nb, ad, bd, id_num, part > 0 || ks > 0);
                     }
+                }
+                // the previous tile's intra numerator (its A~ is ready by now, or soon)
+                if (t > 0 && !(ok = intra(t - 1))) break;
+                // projection of the next tile's queries as soon as U is free (the feature team has read
+                // tile t's keys from it), so that phi(Q_{t+1}) is computed while tile t's MMAs run
+                if (t + 1 < T && !(ok = proj(sQ, &bar_qfull, (t + 1) & 1))) break;
+                ok = mbar_wait(&bar_phk, t & 1, &abort_flag) && mbar_wait(&bar_vfull[b], (t >> 1) & 1, &abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                // scores (K = 128 features, two K atoms)
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const int a = ks / 4, w = ks % 4;
+                    uint64_t ad = sdesc_sw128(smem_u32(sPQ + a * 16384 + w * 32), 16, 1024);
+                    uint64_t bd = sdesc_sw128(smem_u32(sPK + a * 16384 + w * 32), 16, 1024);
+                    mma_ss(tbase + kColSc, ad, bd, id_sc, ks > 0);
                 }
                 // state update: S += phi(K)^T V_t, z += phi(K)^T 1 (K = 128 tokens)
 #pragma unroll
@@ -344,19 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = proj(sK, &bar_kfull, (t + 1) & 1))) break;
                     mma_commit(&bar_qkempty);
                 }
-                // intra numerator: Num += (A~hi + A~lo) V_t, A from TMEM (K = 128 keys)
-                if (!(ok = mbar_wait(&bar_atil, t & 1, &abort_flag))) break;
-                tc_fence_after();
-                for (int part = 0; part < 2; ++part) {
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        uint64_t bd = sdesc_sw128(smem_u32(vt + ks * 2048), 16, 1024);
-                        mma_ts(nb, tbase + kColSc + 16 * ks + 8 * part, bd, id_num, 1);
-                    }
-                }
-                mma_commit(&bar_num);
-                mma_commit(&bar_vempty[b]);
             }
+            if (ok && T > 0) intra(T - 1);
         }
     } else if (warp < 2 + kTeamWarps) {
         // ---------------- feature team: 8 warps ----------------
@@ -507,43 +519,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             failed |= !mbar_wait(&bar_grp, t & 1, &abort_flag);
             __syncwarp();
             tc_fence_after();
-            // ---- A~ = scores masked by j <= i, as bf16 hi + lo, in place: the 16 columns of keys
-            // [16 s, 16 s + 16) become 8 columns of hi and 8 of lo
-            // Whether a 16-key chunk is wholly below, wholly above or across the diagonal is the same
-            // for the warp's 32 rows [32 q, 32 q + 32) unless the chunk meets them: warp-uniform branches.
-            float dO = 0.f;
-#pragma unroll
-            for (int s4 = 0; s4 < 4; ++s4) {
-                const int s = 4 * h + s4;
-                const uint32_t ca = tbase + lane_off + kColSc + 16 * s;
-                uint32_t w[16];
-                if (16 * s > 32 * q + 31) {  // every key of the chunk is after every row: A~ = 0
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) w[k] = 0u;
-                } else {
-                    const bool full = 16 * s + 15 <= 32 * q;  // every key at or before every row
-                    uint32_t v[16];
-                    tmem_ld16(ca, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int k = 0; k < 16; k += 2) {
-                        const int j = 16 * s + k;
-                        const float a0 = (full || j <= r) ? __uint_as_float(v[k]) : 0.f;
-                        const float a1 = (full || j + 1 <= r) ? __uint_as_float(v[k + 1]) : 0.f;
-                        dO += a0 + a1;
-                        const uint32_t hw = pack_bf16(a0, a1);
-                        w[k / 2] = hw;
-                        w[8 + k / 2] = pack_bf16(a0 - __uint_as_float(hw << 16), a1 - __uint_as_float(hw & 0xFFFF0000u));
-                    }
-                }
-                tmem_st16(ca, w);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar_atil);
-            sDenO[h * 128 + r] = dO;
-            // ---- snapshot of the state after this tile's update, for the next tile (lane = feature r)
+            // ---- snapshot of the state after this tile's update, for the next tile (lane = feature r);
+            // first, as the next tile's inter MMA and denominator wait for it
             if (t + 1 < T) {
                 const int b1 = (t + 1) & 1;
                 uint32_t sv[32];
@@ -582,6 +559,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar_snap);
             }
+            // ---- A~ = scores masked by j <= i, as bf16 hi + lo, in place: the 16 columns of keys
+            // [16 s, 16 s + 16) become 8 columns of hi and 8 of lo
+            // Whether a 16-key chunk is wholly below, wholly above or across the diagonal is the same
+            // for the warp's 32 rows [32 q, 32 q + 32) unless the chunk meets them: warp-uniform branches.
+            float dO = 0.f;
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4) {
+                const int s = 4 * h + s4;
+                const uint32_t ca = tbase + lane_off + kColSc + 16 * s;
+                uint32_t w[16];
+                if (16 * s > 32 * q + 31) {  // every key of the chunk is after every row: A~ = 0
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) w[k] = 0u;
+                } else {
+                    const bool full = 16 * s + 15 <= 32 * q;  // every key at or before every row
+                    uint32_t v[16];
+                    tmem_ld16(ca, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int k = 0; k < 16; k += 2) {
+                        const int j = 16 * s + k;
+                        const float a0 = (full || j <= r) ? __uint_as_float(v[k]) : 0.f;
+                        const float a1 = (full || j + 1 <= r) ? __uint_as_float(v[k + 1]) : 0.f;
+                        dO += a0 + a1;
+                        const uint32_t hw = pack_bf16(a0, a1);
+                        w[k / 2] = hw;
+                        w[8 + k / 2] = pack_bf16(a0 - __uint_as_float(hw << 16), a1 - __uint_as_float(hw & 0xFFFF0000u));
+                    }
+                }
+                tmem_st16(ca, w);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_atil);
+            sDenO[h * 128 + r] = dO;
             // ---- output of tile t: columns [32 h, 32 h + 32) of row r
             failed |= !mbar_wait(&bar_num, t & 1, &abort_flag);
             failed |= !mbar_wait(&bar_den[b], (t >> 1) & 1, &abort_flag);
