@@ -54,6 +54,31 @@ def test_workspace_sizes():
         favor.workspace_bytes("causal", 1, 8, 1024, 64, 256, bf, chunk=48)
 
 
+def test_workspace_sizes_per_path():
+    # Short bf16 sequences (n <= 8 tiles of 128, d = 64, m <= 256) run the single-launch kernel, whose
+    # workspace is the per-tile fp32 partial states: [BH][T][m_pad][64] S, [BH][T][2][m_pad] z and
+    # [BH][8] stabilisers, each piece rounded up to 256 bytes.
+    import kernelized_linear_attention_04_b300 as favor
+
+    bf, f32 = torch.bfloat16, torch.float32
+    BH, T, mp = 8, 8, 256
+    up = lambda b: (b + 255) // 256 * 256
+    fused = up(BH * T * mp * 64 * 4) + up(BH * T * 2 * mp * 4) + up(BH * 8 * 4)
+    assert favor.workspace_bytes("noncausal", 1, 8, 1024, 64, 256, bf) == fused
+    # m = 192 pads to 256 features
+    assert favor.workspace_bytes("noncausal", 1, 8, 1024, 64, 192, bf) == fused
+    # one tile per head
+    assert favor.workspace_bytes("noncausal", 1, 8, 100, 64, 256, bf) == up(BH * mp * 256) + up(BH * 2 * mp * 4) + up(BH * 32)
+    # longer sequences run the three-kernel path, whose workspace does not grow with n beyond the splits
+    assert favor.workspace_bytes("noncausal", 1, 8, 4096, 64, 256, bf) > 0
+    # the tensor-core causal scans keep the state in TMEM: no workspace
+    for m in (64, 192, 256, 384, 512):
+        assert favor.workspace_bytes("causal", 4, 16, 8192, 64, m, bf) == 0
+    # fp32, and bf16 with d = 128, take the CUDA-core scan, whose state lives in the workspace
+    assert favor.workspace_bytes("causal", 1, 2, 300, 64, 256, f32) >= 2 * (256 * 64 + 256) * 4
+    assert favor.workspace_bytes("causal", 1, 2, 300, 128, 256, bf) >= 2 * (256 * 128 + 256) * 4
+
+
 # Argument checks. Fake (never dereferenced) addresses are only passed where an earlier check
 # must fail; to keep even that off a real device these run only without a GPU.
 needs_no_gpu = pytest.mark.skipif(torch.cuda.is_available(), reason="host-only argument checks")

@@ -55,7 +55,7 @@ for dtype in ("f32", "bf16"):
         for kind in ("exp", "relu"):
             for n in (1, 3, 63, 65, 127, 129, 1000):
                 CASES.append((dtype, causal, kind, n, 64, 256))
-        for d, m in ((128, 256), (64, 64), (64, 512), (128, 192)):
+        for d, m in ((128, 256), (64, 64), (64, 512), (128, 192), (64, 192), (64, 384)):
             CASES.append((dtype, causal, "exp", 200, d, m))
 
 
