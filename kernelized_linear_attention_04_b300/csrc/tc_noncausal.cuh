@@ -134,6 +134,11 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     __shared__ uint64_t bar_kfull[NK], bar_kempty[NK], bar_vfull[NV], bar_vempty[NV], bar_om;
     __shared__ uint64_t bar_ufull[kStateSlots], bar_ufree[kStateSlots], bar_phi[kStateSlots];
     __shared__ uint64_t bar_nfull[2], bar_nempty[2];
+    // bar_rs: one completion per tile whose stabiliser moved, once every state MMA of the tiles
+    // before it has completed; bar_sdone: once, after the last state MMA. Every epilogue warp waits
+    // on every completion of both, so no wait can mistake an old phase for the one it wants (a wait
+    // on a slot barrier could: a team that does not use a slot may be two of its phases behind).
+    __shared__ uint64_t bar_rs, bar_sdone;
     __shared__ float sF[2];  // per-tile rescale factor of the accumulated state (1 = none)
     __shared__ float sRed[2][kStateNormWarps];
     __shared__ uint32_t tmem_base;
@@ -169,6 +174,10 @@ __global__ void __launch_bounds__(kStateThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar_nfull[i], kStateNormWarps);
             mbar_init(&bar_nempty[i], kStateEpiWarps);
+            if (i == 0) {
+                mbar_init(&bar_rs, 1);
+                mbar_init(&bar_sdone, 1);
+            }
         }
         fence_mbar_init();
     }
@@ -254,7 +263,16 @@ __global__ void __launch_bounds__(kStateThreads, 1)
                     mma_ts(tbase + (uint32_t)(g * D), tbase + u_col(s) + phi_col(ks), bd, idesc_s, (t > 0 || ks > 0));
                 }
                 mma_commit(&bar_ufree[s]);
-                if (u % UPT == UPT - 1) mma_commit(&bar_vempty[st]);
+                if (u % UPT == UPT - 1) {
+                    mma_commit(&bar_vempty[st]);
+                    // the next tile's rescale factor (the norm warps publish it with bar_nfull); if the
+                    // stabiliser moved, signal the epilogue once this tile's state MMAs have completed
+                    const int tn = t + 1;
+                    if (tn < T) {
+                        if (!mbar_wait(&bar_nfull[tn & 1], (tn >> 1) & 1, &abort_flag)) return false;
+                        if (sF[tn & 1] != 1.f) mma_commit(&bar_rs);
+                    }
+                }
                 return true;
             };
             // Order P(0), P(1), S(0), P(2), S(1), ...: the projection into a slot waits for the state
@@ -266,6 +284,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
                 }
                 if (!abort_flag && U > 0) issue_state(U - 1);
             }
+            mma_commit(&bar_sdone);  // every state MMA issued has completed
         }
     } else if (warp < kStateEpiWarp0) {
         // ---------------- norms and the key stabiliser (two warps) ----------------
@@ -349,6 +368,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
         const float A2 = p.scale * kLog2e;
         float zacc[4] = {0.f, 0.f, 0.f, 0.f};
         bool failed = false;
+        int nrs = 0;  // rescale events waited for (bar_rs completions)
         for (int t = 0; t < T; ++t) {
             const int b2 = t & 1;
             failed |= !mbar_wait(&bar_nfull[b2], (t >> 1) & 1, &abort_flag);
@@ -356,8 +376,8 @@ __global__ void __launch_bounds__(kStateThreads, 1)
             const float f = sF[b2];
             if (f != 1.f) {
                 // The key stabiliser moved: once every state MMA so far has completed, scale S and z.
-                const int ul = t * UPT - 1;
-                failed |= !mbar_wait(&bar_ufree[ul % kStateSlots], (ul / kStateSlots) & 1, &abort_flag);
+                failed |= !mbar_wait(&bar_rs, nrs & 1, &abort_flag);
+                ++nrs;
                 __syncwarp();
                 tc_fence_after();
                 const int part = tm * 2 + cg;  // this warp's quarter of the S columns
@@ -442,9 +462,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
             if (lane == 0) mbar_arrive(&bar_nempty[b2]);
         }
         // Final state: wait for the last state MMA, then write this CTA's partial S and z.
-        const int ul = U - 1;
-        const bool done =
-            __all_sync(0xffffffffu, U > 0 && mbar_wait(&bar_ufree[ul % kStateSlots], (ul / kStateSlots) & 1, &abort_flag));
+        const bool done = __all_sync(0xffffffffu, U > 0 && mbar_wait(&bar_sdone, 0, &abort_flag));
         tc_fence_after();
         const size_t part_idx = (size_t)bh * splits + split;
         // z partials of the two teams and two column groups meet in shared memory (the V ring is idle now).
