@@ -24,7 +24,7 @@
 //               tile, and the output (cluster sum, num / den, Y).
 // The numerator has two TMEM buffers, so the inter MMA of tile t+1 need not wait for the output of
 // tile t. Tensor-core work per tile: U = X Omega^T (two projections), scores phi(Q) phi(K)^T, inter
-// phi(Q) (S_hi + S_lo), state S += phi(K)^T V and z += phi(K)^T 1, intra (A~hi + A~lo) V.
+// phi(Q) (S_hi + S_lo), state [S | z] += phi(K)^T [V | 1], intra (A~hi + A~lo) V.
 //
 // Stabilisers: a query row uses c_i = W |q^_i| (W = largest row norm of Omega; Cauchy-Schwarz bounds
 // every w_r . q^_i by it). Keys use one constant per head, 12 nats below the largest bound
@@ -54,7 +54,7 @@ constexpr int kPhiBytes = kTile * 128 * 2;   // 32 KB: [128 tokens x 128 feature
 constexpr int kXStride = 84;                 // floats per row of the cluster exchange buffer (64 + den + pad)
 
 // TMEM columns
-constexpr uint32_t kColS = 0;      // S: 64 columns, z: 16 (all equal)
+constexpr uint32_t kColS = 0;      // S: 64 columns, then z (column 64) and 15 zero columns
 constexpr uint32_t kColU = 128;    // projection output, 128 columns
 constexpr uint32_t kColSc = 256;   // scores; then A~ in place: keys [16 s, 16 s + 16) -> hi at 16 s, lo at 16 s + 8
 constexpr uint32_t kColNum = 384;  // numerator, two buffers of 64 columns
@@ -71,11 +71,12 @@ struct CausalParams {
 
 struct CausalSmem {
     // Omega rows of the CTA (128 x 64, K-major), Q, K, two V tiles, the state snapshot as hi and lo
-    // bf16 images (128 x 64, MN-major), phi(Q), phi(K), ones block (16 x 128 bf16, K-major), z
-    // snapshots (2 x 128 fp32), denominator shares (6 x 128 fp32), cluster exchange buffer.
+    // bf16 images (128 x 64, MN-major), phi(Q), phi(K), the ones column (128 x 64 bf16, MN-major:
+    // the second N region of the state MMA's B operand [V | 1]), z snapshots (2 x 128 fp32),
+    // denominator shares (6 x 128 fp32), cluster exchange buffer.
     static size_t x_bytes(int cs) { return cs > 1 ? (size_t)(cs - 1) * (kTile / cs) * kXStride * 4 : 0; }
     static size_t bytes(int cs) {
-        return 1024 + 7 * (size_t)kTileBytes + 2 * (size_t)kPhiBytes + 4096 + 8 * 128 * 4 + x_bytes(cs);
+        return 1024 + 8 * (size_t)kTileBytes + 2 * (size_t)kPhiBytes + 8 * 128 * 4 + x_bytes(cs);
     }
 };
 
@@ -99,8 +100,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sSl = sS + kTileBytes;            // state snapshot lo (S - hi, rounded)
     uint8_t* sPQ = sSl + kTileBytes;           // phi(Q): 2 K-atom regions of 128 rows x 128 B
     uint8_t* sPK = sPQ + kPhiBytes;            // phi(K)
-    uint8_t* sOnes = sPK + kPhiBytes;          // 2 K-atom regions of 16 rows x 128 B
-    float* sZ = reinterpret_cast<float*>(sOnes + 4096);  // [2][128] z snapshot by tile parity
+    uint8_t* sOnes = sPK + kPhiBytes;          // 128 token rows x 128 B: column 0 = 1, the rest 0
+    float* sZ = reinterpret_cast<float*>(sOnes + kTileBytes);  // [2][128] z snapshot by tile parity
     float* sDenF = sZ + 2 * 128;               // [2 parity][2 half][128] phi(q) . z_<t shares
     float* sDenO = sDenF + 4 * 128;            // [2 half][128] masked score row sums
     float* sX = sDenO + 2 * 128;               // [CS - 1][RP][kXStride] partial sums from the peers
@@ -143,9 +144,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bar_xfull, CS > 1 ? (CS - 1) * (RP / 32) * 2 : 1);
         fence_mbar_init();
     }
-    // ones block (K-major, every element 1.0): z = phi(K)^T 1 via the tensor cores
-    for (int i = threadIdx.x; i < 4096 / 16; i += blockDim.x)
-        reinterpret_cast<uint4*>(sOnes)[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    // the ones column: z = phi(K)^T 1 comes out of the state MMA as its 65th output column. In the
+    // 128-byte-swizzled MN-major layout, column 0 of token row k sits in 16-byte chunk (k mod 8).
+    for (int i = threadIdx.x; i < kTileBytes / 16; i += blockDim.x) {
+        const int row = i >> 3, chunk = i & 7;
+        reinterpret_cast<uint4*>(sOnes)[i] = make_uint4(chunk == (row & 7) ? 0x00003F80u : 0u, 0u, 0u, 0u);
+    }
     fence_async_smem();
     if (warp == 1) tmem_alloc(&tmem_base, 512);
     __syncthreads();
@@ -271,8 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t id_proj = idesc_bf16(128, 128, false, false);  // U = X Om^T
             constexpr uint32_t id_sc = idesc_bf16(128, 128, false, false);    // phi(Q) phi(K)^T
             constexpr uint32_t id_num = idesc_bf16(128, kD, false, true);     // phi(Q) S, A~ V
-            constexpr uint32_t id_st = idesc_bf16(128, kD, true, true);       // phi(K)^T V
-            constexpr uint32_t id_z = idesc_bf16(128, 16, true, false);       // phi(K)^T 1
+            constexpr uint32_t id_st = idesc_bf16(128, kD + 16, true, true);  // phi(K)^T [V | 1]
             bool ok = true;
             int pu = 0;  // projections issued into the one U slot
             auto proj = [&](const uint8_t* x, uint64_t* full, uint32_t parity) -> bool {
@@ -347,19 +350,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint64_t bd = sdesc_sw128(smem_u32(sPK + a * 16384 + w * 32), 16, 1024);
                     mma_ss(tbase + kColSc, ad, bd, id_sc, ks > 0);
                 }
-                // state update: S += phi(K)^T V_t, z += phi(K)^T 1 (K = 128 tokens)
+                // state update: [S | z] += phi(K)^T [V_t | 1] (K = 128 tokens, N = 64 + 16; the ones
+                // column is the B operand's second N region, LBO bytes after the V tile)
+                const uint32_t lbo_ones = (uint32_t)(sOnes - vt);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     uint64_t ad = sdesc_sw128(smem_u32(sPK + ks * 2048), 16384, 1024);
-                    uint64_t bd = sdesc_sw128(smem_u32(vt + ks * 2048), 16, 1024);
+                    uint64_t bd = sdesc_sw128(smem_u32(vt + ks * 2048), lbo_ones, 1024);
                     mma_ss(tbase + kColS, ad, bd, id_st, t > 0 || ks > 0);
-                }
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const int a = ks / 4, w = ks % 4;
-                    uint64_t ad = sdesc_sw128(smem_u32(sPK + ks * 2048), 16384, 1024);
-                    uint64_t bd = sdesc_sw128(smem_u32(sOnes + a * 2048 + w * 32), 16, 1024);
-                    mma_ss(tbase + kColS + 64, ad, bd, id_z, t > 0 || ks > 0);
                 }
                 mma_commit(&bar_grp);
                 // projection of the next tile's keys while the output team forms A~
