@@ -90,6 +90,10 @@ favor_status_t favor_features(const void* X, const void* Omega, float* Phi, int 
  *   Q, K, V, Y [B, H, n, d] dtype dt; Omega [m, d] dtype dt. Y may not alias Q, K or V.
  * Stabilisers: queries use one constant per row, keys one constant per head (after rescaling of
  * partial sums); both cancel in the ratio, so Y does not depend on them.
+ * bf16 with d = 64, m <= 256 and n <= 1024 runs as one launch (a head's 128-token tiles are the
+ * CTAs of one thread-block cluster); other bf16 shapes with d = 64, or d = 128 and m <= 256, run a
+ * key-state pass, a combine and a query readout on the tensor cores; fp32 and the remaining shapes
+ * run on CUDA cores. The workspace holds the partial key states (favor_workspace_bytes).
  */
 favor_status_t favor_attn_noncausal(const void* Q, const void* K, const void* V, const void* Omega, void* Y,
                                     int B, int H, int n, int d, int m, favor_dtype_t dt, favor_kind_t kind,
@@ -101,10 +105,10 @@ favor_status_t favor_attn_noncausal(const void* Q, const void* K, const void* V,
  *   y_i = phi(q_i)^T S_i / phi(q_i)^T z_i,  S_i = sum_{j<=i} phi(k_j) v_j^T,  z_i = sum_{j<=i} phi(k_j).
  * Computed as a chunked scan: per chunk, an intra-chunk lower-triangular block plus the carried
  * prefix state. chunk: 0 (implementation default), 64 or 128; the result does not depend on it
- * beyond rounding. bf16 with d = 64 and m <= 256 runs the tensor-core scan, which carries the state
- * every 128 tokens and masks j <= i inside each 128-token tile (two 64-token chunks give exactly
- * that sum); other inputs run on CUDA cores in 16-token steps. Shapes and dtypes as above.
- * Workspace: 0 bytes on the tensor-core scan.
+ * beyond rounding. bf16 with d = 64 and m <= 512 runs a tensor-core scan (pipelined over tiles
+ * for m <= 256), which carries the state every 128 tokens and masks j <= i inside each 128-token
+ * tile (two 64-token chunks give exactly that sum); other inputs run on CUDA cores in 16-token
+ * steps. Shapes and dtypes as above. Workspace: 0 bytes on the tensor-core scans.
  */
 favor_status_t favor_attn_causal(const void* Q, const void* K, const void* V, const void* Omega, void* Y,
                                  int B, int H, int n, int d, int m, int chunk, favor_dtype_t dt,
@@ -119,7 +123,7 @@ favor_status_t favor_attn_causal(const void* Q, const void* K, const void* V, co
  * is fixed at start-up).
  *
  * It computes exactly what favor_attn_noncausal computes, with the same arguments minus the
- * workspace. Its scratch (the per-split partial key states) lives in one fixed device array of
+ * workspace. Its scratch (the partial key states) lives in one fixed device array of
  * FAVOR_NOALLOC_SCRATCH_BYTES compiled into the library, so every GPU that loads libfavor.so holds
  * that array until the process exits. Shapes whose scratch need (favor_workspace_bytes for
  * FAVOR_OP_NONCAUSAL) exceeds it are rejected with FAVOR_ERR_WORKSPACE before anything runs.
