@@ -457,6 +457,79 @@ def run_ours(args, w):
     return 0
 
 
+def run_decode(args, w):
+    """Streaming decode: one favor_decode_step per timed step, one new token for each of the
+    workload's B*H heads (its d, m, dtype and feature family; n is not used). Memory-bound: the
+    step reads and writes the fp32 state S [m x d] and z [m] of every head."""
+    import torch
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    import kernelized_linear_attention_04_b300 as favor
+
+    dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    g = torch.Generator(device="cpu").manual_seed(w.seed)
+    steps_tokens = args.warmup + args.steps
+    # one token per head per step, drawn once (synthetic, iid N(0, sigma^2)); Omega from the workload
+    toks = torch.randn(3, steps_tokens + args.steps, w.B, w.H, w.d, generator=g) * w.sigma
+    toks = toks.to(dt).to(dev)
+    om_store, _ = si.omega_for(w)
+    Om = (torch.from_numpy(om_store.view(np.int16)).view(torch.bfloat16) if om_store.dtype == np.uint16
+          else torch.from_numpy(om_store)).to(dev)
+    state = favor.decode_state(w.B, w.H, w.d, w.m)
+    y = torch.empty(w.B, w.H, w.d, dtype=dt, device=dev)
+
+    def step(i):
+        favor.favor_decode_step(toks[0, i], toks[1, i], toks[2, i], Om, state, kind=w.kind, relu_eps=w.relu_eps, out=y)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    assert favor.last_device_error() == 0
+    BH = w.B * w.H
+    s_el = 4 if dt == torch.float32 else 2
+    nbytes = BH * (2 * w.m * w.d * 4 + 2 * w.m * 4 + 4 * w.d * s_el) + w.m * w.d * s_el
+    # every timed step starts from a cold L2 (a 512 MB write) unless the state is larger than L2
+    flush = nbytes < 2 * L2_BYTES
+    fbuf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
+
+    def timed(n0):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for i, (a, b) in enumerate(evs):
+            if fbuf is not None:
+                fbuf.zero_()
+            a.record()
+            step(n0 + i)
+            b.record()
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in evs) / args.steps
+
+    sampler = ClockSampler(0)
+    with sampler:
+        ms = timed(args.warmup)
+    favor.trace_enable(True)
+    timed(args.warmup)
+    tr = favor.trace_read()
+    favor.trace_enable(False)
+    k_ms = tr["decode"][1] / tr["decode"][0]
+    peaks, peak_kind = load_peaks()
+    ach = nbytes / (k_ms * 1e-3) / 1e9
+    line = {
+        "metric": "FAVOR+ streaming decode tokens/s (B*H new tokens per s)", "value": BH / (ms * 1e-3),
+        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32" if dt == torch.float32 else "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"decode_{w.dtype}_B{w.B}H{w.H}d{w.d}m{w.m}", "form": "streaming decode step",
+                   "features": w.kind, "B": w.B, "H": w.H, "d": w.d, "m": w.m,
+                   "l2": "flushed before every timed step (512 MB write)" if flush else "state larger than L2"},
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": ach / peaks["hbm_gbs"], "traffic": None, "kernel": "decode", "kernel_ms": k_ms,
+                     "peak_source": f"HBM copy, {peak_kind}", "algorithmic_bytes": nbytes},
+        "gpu_launches": args.steps, "clocks": sampler.summary(),
+    }
+    print(json.dumps(line))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -465,6 +538,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=si.workloads.WORKLOAD_ORDER)
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the host-core oracle timing")
+    ap.add_argument("--decode", action="store_true",
+                    help="time the streaming decode step at the workload's B, H, d, m instead of the full call")
     ap.add_argument("--n", type=int, default=None,
                     help="override the sequence length (smaller cases for profiler captures; not a bench line)")
     args = ap.parse_args(argv)
@@ -478,6 +553,8 @@ def main(argv=None):
         w = w.with_(n=args.n, name=f"{w.name}@n={args.n}")
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.decode:
+        return run_decode(args, w)
     return run_ours(args, w)
 
 

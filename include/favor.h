@@ -140,6 +140,30 @@ favor_status_t favor_attn_noncausal_noalloc(const void* Q, const void* K, const 
                                             void* Y, int B, int H, int n, int d, int m, favor_dtype_t dt,
                                             favor_kind_t kind, float relu_eps, void* stream);
 
+/*
+ * Streaming decode ("Performer for vision", *What Is Performer?*, Key Feature 2: attention is
+ * accumulated incrementally, enabling streaming inference; *Why Performer Matters*, Streaming and
+ * Sampling: autoregressive decoding). The causal form one token at a time: per head a state
+ * (S = sum_j phi(k_j) v_j^T, z = sum_j phi(k_j) over the tokens seen so far) lives in a
+ * caller-owned device buffer, and each step appends one token and returns its output.
+ *
+ * favor_decode_state_bytes: size of the state for B*H heads (fp32 S [B*H][m][d], z [B*H][m] and one
+ *   key stabiliser per head, 256-byte aligned pieces); SIZE_MAX for an unsupported shape
+ *   (d in {64, 128}, m a multiple of 64 in [64, 512]).
+ * favor_decode_init: empties the state of every head (no token seen). Asynchronous on `stream`.
+ * favor_decode_step: q, k, v, y are [B, H, d] (the new token of every head), Omega [m, d], all of
+ *   dtype dt; state as initialised (256-byte aligned, at least favor_decode_state_bytes). Updates
+ *   S <- S + phi(k) v^T, z <- z + phi(k) and writes y = phi(q)^T S / phi(q)^T z, so that steps
+ *   t = 1..n give exactly the rows of favor_attn_causal over those n tokens (up to rounding).
+ *   The key stabiliser is carried in the state and the accumulated S, z are rescaled when it moves;
+ *   it cancels in the ratio. Errors as for the attention calls; nothing runs on an error.
+ */
+size_t favor_decode_state_bytes(int B, int H, int d, int m);
+favor_status_t favor_decode_init(void* state, size_t state_bytes, int B, int H, int d, int m, void* stream);
+favor_status_t favor_decode_step(const void* q, const void* k, const void* v, const void* Omega, void* y,
+                                 void* state, size_t state_bytes, int B, int H, int d, int m, favor_dtype_t dt,
+                                 favor_kind_t kind, float relu_eps, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* favor_status_string(favor_status_t status);
 
@@ -160,7 +184,9 @@ typedef enum {
     FAVOR_KERNEL_READOUT = 4,       /* non-causal query-side readout and divide              */
     FAVOR_KERNEL_CAUSAL = 5,        /* causal chunked scan                                    */
     FAVOR_KERNEL_FUSED = 6,         /* single-launch non-causal path for short sequences      */
-    FAVOR_KERNEL_COUNT = 7
+    FAVOR_KERNEL_DECODE = 7,        /* streaming decode step (favor_decode_step)              */
+    FAVOR_KERNEL_DECODE_INIT = 8,   /* decode state reset (favor_decode_init)                 */
+    FAVOR_KERNEL_COUNT = 9
 } favor_kernel_id_t;
 
 /* Starts (on != 0) or stops recording. Starting clears previous records. While recording, every

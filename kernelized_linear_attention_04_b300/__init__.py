@@ -8,6 +8,8 @@ path: if the library cannot be loaded, importing this package raises.
     Y = favor.favor_attn_noncausal(Q, K, V, Omega)            # [B, H, n, d] bf16/fp32 CUDA tensors
     Y = favor.favor_attn_causal(Q, K, V, Omega, chunk=64)
     Phi = favor.favor_features(X, Omega, stab="head")
+    state = favor.decode_state(B, H, d, m, device)             # streaming decode, one token per step
+    y = favor.favor_decode_step(q, k, v, Omega, state)         # q, k, v: [B, H, d]
 """
 from __future__ import annotations
 
@@ -21,6 +23,7 @@ from . import build as _build
 __all__ = [
     "FavorError", "favor_features", "favor_attn_noncausal", "favor_attn_causal", "favor_attn_noncausal_noalloc",
     "workspace_bytes", "NOALLOC_SCRATCH_BYTES",
+    "decode_state_bytes", "decode_state", "favor_decode_init", "favor_decode_step",
     "last_device_error", "trace_enable", "trace_read", "abi_version", "lib", "LIB_PATH",
     "KERNEL_NAMES", "EXPORTED_SYMBOLS",
 ]
@@ -33,7 +36,7 @@ _STABS = {"none": 0, "row": 1, "head": 2}
 _OPS = {"features": 0, "noncausal": 1, "causal": 2}
 _STATUS = {0: "FAVOR_OK", 1: "FAVOR_ERR_INVALID_ARG", 2: "FAVOR_ERR_UNSUPPORTED", 3: "FAVOR_ERR_MISALIGNED",
            4: "FAVOR_ERR_WORKSPACE", 5: "FAVOR_ERR_CUDA", 6: "FAVOR_ERR_TIMEOUT"}
-KERNEL_COUNT = 7
+KERNEL_COUNT = 9
 # Size of the library's fixed scratch array used by favor_attn_noncausal_noalloc.
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -42,6 +45,7 @@ EXPORTED_SYMBOLS = (
     "favor_workspace_bytes", "favor_features", "favor_attn_noncausal", "favor_attn_causal",
     "favor_status_string", "favor_last_device_error", "favor_abi_version", "favor_trace_enable",
     "favor_trace_read", "favor_kernel_name", "favor_attn_noncausal_noalloc",
+    "favor_decode_state_bytes", "favor_decode_init", "favor_decode_step",
 )
 
 
@@ -77,6 +81,12 @@ def _load() -> ctypes.CDLL:
     L.favor_trace_read.restype = i32
     L.favor_kernel_name.argtypes = [i32]
     L.favor_kernel_name.restype = ctypes.c_char_p
+    L.favor_decode_state_bytes.argtypes = [i32, i32, i32, i32]
+    L.favor_decode_state_bytes.restype = sz
+    L.favor_decode_init.argtypes = [vp, sz, i32, i32, i32, i32, vp]
+    L.favor_decode_init.restype = i32
+    L.favor_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, sz, i32, i32, i32, i32, i32, i32, f32, vp]
+    L.favor_decode_step.restype = i32
     return L
 
 
@@ -214,3 +224,47 @@ def trace_read() -> dict[str, tuple[int, float]]:
     _check(lib.favor_trace_read(ctypes.cast(launches, ctypes.c_void_p), ctypes.cast(total, ctypes.c_void_p)),
            "favor_trace_read")
     return {KERNEL_NAMES[i]: (int(launches[i]), float(total[i])) for i in range(KERNEL_COUNT)}
+
+
+# ---- streaming decode ------------------------------------------------------------------------------
+
+def decode_state_bytes(B: int, H: int, d: int, m: int) -> int:
+    """Bytes of the decode state of B*H heads (raises FavorError(UNSUPPORTED) for unsupported d, m)."""
+    v = lib.favor_decode_state_bytes(B, H, d, m)
+    if v == ctypes.c_size_t(-1).value:
+        raise FavorError(2, "favor_decode_state_bytes")
+    return int(v)
+
+
+def favor_decode_init(state: torch.Tensor, B: int, H: int, d: int, m: int, stream=None) -> torch.Tensor:
+    """Empties the decode state (no token seen) of every head."""
+    _check(lib.favor_decode_init(_ptr(state), state.numel() * state.element_size(), B, H, d, m,
+                                 _stream_handle(stream)), "favor_decode_init")
+    return state
+
+
+def decode_state(B: int, H: int, d: int, m: int, device="cuda", stream=None) -> torch.Tensor:
+    """A new, empty decode state (a uint8 device buffer owned by the caller)."""
+    state = torch.empty(decode_state_bytes(B, H, d, m), dtype=torch.uint8, device=device)
+    return favor_decode_init(state, B, H, d, m, stream)
+
+
+def favor_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, Omega: torch.Tensor, state: torch.Tensor,
+                      *, kind: str = "exp", relu_eps: float = 1e-3, out: torch.Tensor | None = None,
+                      stream=None) -> torch.Tensor:
+    """Appends one token per head (q, k, v: [B, H, d]) to `state` and returns its output y [B, H, d]."""
+    for t, name in ((q, "q"), (k, "k"), (v, "v")):
+        if t.dim() != 3 or not t.is_contiguous() or t.dtype not in _DTYPES:
+            raise ValueError(f"{name} must be a contiguous [B, H, d] float32/bfloat16 tensor")
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError("q, k and v must have the same shape and dtype")
+    B, H, d = (int(x) for x in q.shape)
+    if Omega.dim() != 2 or Omega.shape[1] != d or Omega.dtype != q.dtype or not Omega.is_contiguous():
+        raise ValueError("Omega must be a contiguous [m, d] tensor of the same dtype as q")
+    m = int(Omega.shape[0])
+    if out is None:
+        out = torch.empty_like(q)
+    _check(lib.favor_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(Omega), _ptr(out), _ptr(state),
+                                 state.numel() * state.element_size(), B, H, d, m, _DTYPES[q.dtype], _KINDS[kind],
+                                 relu_eps, _stream_handle(stream)), "favor_decode_step")
+    return out

@@ -17,6 +17,7 @@
 #include "tc_causal_wide.cuh"
 #include "tc_features.cuh"
 #include "tc_fused.cuh"
+#include "decode.cuh"
 #include "tma_host.h"
 
 namespace favor {
@@ -530,6 +531,8 @@ const char* favor_kernel_name(int kid) {
         case FAVOR_KERNEL_COMBINE: return "combine";
         case FAVOR_KERNEL_READOUT: return "readout";
         case FAVOR_KERNEL_CAUSAL: return "causal";
+        case FAVOR_KERNEL_DECODE: return "decode";
+        case FAVOR_KERNEL_DECODE_INIT: return "decode_init";
         case FAVOR_KERNEL_FUSED: return "fused";
     }
     return "unknown";
@@ -596,6 +599,83 @@ favor_status_t favor_attn_causal(const void* Q, const void* K, const void* V, co
 // ------------------------------------------------------------------------------------------------
 // favor_attn_noncausal_noalloc: the non-causal path with its scratch in a fixed device array.
 // ------------------------------------------------------------------------------------------------
+}  // extern "C"
+
+namespace favor {
+namespace {
+
+// ---- streaming decode state: S [BH][m][d], z [BH][m], stab [BH], fp32 ---------------------------
+struct DecodeLayout {
+    size_t off_z, off_stab, total;
+};
+DecodeLayout decode_layout(int B, int H, int d, int m) {
+    const size_t BH = (size_t)B * H;
+    DecodeLayout L{};
+    L.off_z = align_up(BH * m * d * sizeof(float), 256);
+    L.off_stab = L.off_z + align_up(BH * m * sizeof(float), 256);
+    L.total = L.off_stab + align_up(BH * sizeof(float), 256);
+    return L;
+}
+
+favor_status_t check_decode_state(const void* state, size_t state_bytes, int B, int H, int d, int m) {
+    if (!state) return FAVOR_ERR_INVALID_ARG;
+    if (!aligned(state, 256)) return FAVOR_ERR_MISALIGNED;
+    if (state_bytes < decode_layout(B, H, d, m).total) return FAVOR_ERR_WORKSPACE;
+    return FAVOR_OK;
+}
+
+template <typename T, int D>
+favor_status_t decode_launch(const void* q, const void* k, const void* v, const void* Om, void* y, void* state, int BH,
+                             int m, int kind, float eps, cudaStream_t s) {
+    const DecodeLayout L = decode_layout(BH, 1, D, m);
+    char* base = static_cast<char*>(state);
+    const size_t smem = sizeof(float) * dec::decode_smem_floats<D>(m);
+    FAVOR_TRY(traced(FAVOR_KERNEL_DECODE, s, [&] {
+        dec::decode_step<T, D><<<BH, dec::kThreads, smem, s>>>(
+            static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), static_cast<const T*>(Om),
+            static_cast<T*>(y), reinterpret_cast<float*>(base), reinterpret_cast<float*>(base + L.off_z),
+            reinterpret_cast<float*>(base + L.off_stab), m, kind, eps * std::sqrt((float)m), qk_scale(D));
+    }));
+    return cudaGetLastError() == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace favor
+
+extern "C" {
+
+size_t favor_decode_state_bytes(int B, int H, int d, int m) {
+    if (check_shape(B, H, 1, d, m, FAVOR_BF16, FAVOR_EXP) != FAVOR_OK) return SIZE_MAX;
+    return decode_layout(B, H, d, m).total;
+}
+
+favor_status_t favor_decode_init(void* state, size_t state_bytes, int B, int H, int d, int m, void* stream) {
+    FAVOR_TRY(check_shape(B, H, 1, d, m, FAVOR_BF16, FAVOR_EXP));
+    if ((int64_t)B * H == 0) return FAVOR_OK;
+    FAVOR_TRY(check_decode_state(state, state_bytes, B, H, d, m));
+    const DecodeLayout L = decode_layout(B, H, d, m);
+    char* base = static_cast<char*>(state);
+    const int64_t BH = (int64_t)B * H;
+    const int64_t nS = BH * m * d;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int blocks = (int)std::min<int64_t>((nS + 255) / 256, 4 * kNumSMs);
+    FAVOR_TRY(traced(FAVOR_KERNEL_DECODE_INIT, s, [&] {
+        dec::decode_init<<<blocks, 256, 0, s>>>(reinterpret_cast<float*>(base), reinterpret_cast<float*>(base + L.off_z),
+                                               reinterpret_cast<float*>(base + L.off_stab), nS, BH * m, BH);
+    }));
+    return cudaGetLastError() == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;
+}
+
+favor_status_t favor_decode_step(const void* q, const void* k, const void* v, const void* Omega, void* y, void* state,
+                                 size_t state_bytes, int B, int H, int d, int m, favor_dtype_t dt, favor_kind_t kind,
+                                 float relu_eps, void* stream) {
+    FAVOR_TRY(check_attn_args(q, k, v, Omega, y, B, H, 1, d, m, dt, kind, relu_eps));
+    if ((int64_t)B * H == 0) return FAVOR_OK;
+    FAVOR_TRY(check_decode_state(state, state_bytes, B, H, d, m));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return FAVOR_DISPATCH(dt, d, decode_launch, q, k, v, Omega, y, state, B * H, m, (int)kind, relu_eps, s);
+}
+
 }  // extern "C"
 
 namespace favor {

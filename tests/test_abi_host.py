@@ -74,6 +74,11 @@ def test_workspace_sizes_per_path():
     # the tensor-core causal scans keep the state in TMEM: no workspace
     for m in (64, 192, 256, 384, 512):
         assert favor.workspace_bytes("causal", 4, 16, 8192, 64, m, bf) == 0
+    # streaming decode state: fp32 S [BH][m][d], z [BH][m], one stabiliser per head, 256-byte pieces
+    assert favor.decode_state_bytes(2, 3, 64, 256) == 6 * 256 * 64 * 4 + 6 * 256 * 4 + 256
+    assert favor.decode_state_bytes(1, 1, 128, 512) == 512 * 128 * 4 + 512 * 4 + 256
+    with pytest.raises(favor.FavorError):
+        favor.decode_state_bytes(1, 1, 96, 256)
     # fp32, and bf16 with d = 128, take the CUDA-core scan, whose state lives in the workspace
     assert favor.workspace_bytes("causal", 1, 2, 300, 64, 256, f32) >= 2 * (256 * 64 + 256) * 4
     assert favor.workspace_bytes("causal", 1, 2, 300, 128, 256, bf) >= 2 * (256 * 128 + 256) * 4
@@ -121,6 +126,19 @@ def test_argument_checks_reject_before_launch():
     assert ft(P, P, N, 1, 1, 16, 64, 64, 1, 0, 0.0, 1, N, 0, S) == 1
     assert ft(P, P, P, 1, 1, 16, 64, 64, 1, 0, 0.0, 9, N, 0, S) == 1
     assert ft(P, P, P, 1, 1, 16, 64, 64, 1, 0, 0.0, 2, N, 0, S) == 1       # head stab needs workspace
+    # streaming decode: state checks come after the tensor checks; empty batches are no-ops
+    ds = L.favor_decode_step
+    need = L.favor_decode_state_bytes(1, 1, 64, 64)
+    assert ds(P, N, P, P, P, P, need, 1, 1, 64, 64, 1, 0, 0.0, S) == 1           # null k
+    assert ds(P, P, P, P, P, N, need, 1, 1, 64, 64, 1, 0, 0.0, S) == 1           # null state
+    assert ds(P, P, P, P, P, ctypes.c_void_p(0x10010), need, 1, 1, 64, 64, 1, 0, 0.0, S) == 3  # state alignment
+    assert ds(P, P, P, P, P, P, need - 1, 1, 1, 64, 64, 1, 0, 0.0, S) == 4       # state too small
+    assert ds(P, P, P, P, P, P, need, 1, 1, 96, 64, 1, 0, 0.0, S) == 2           # unsupported d
+    assert ds(N, N, N, N, N, N, 0, 0, 4, 64, 64, 1, 0, 0.0, S) == 0              # no heads
+    di = L.favor_decode_init
+    assert di(N, need, 1, 1, 64, 64, S) == 1
+    assert di(P, need - 1, 1, 1, 64, 64, S) == 4
+    assert di(N, 0, 0, 1, 64, 64, S) == 0
 
 
 def test_python_binding_validates_shapes():
