@@ -7,9 +7,10 @@
 // The prefix state is carried at every tile boundary (128 tokens); within a tile the keys are
 // masked by j <= i, which for two 64-token chunks is exactly their chunked prefix-sum result.
 //
-// Each CTA holds one 128-feature group of the head; a head with more features is spread over a
-// thread-block cluster (2 or 4 CTAs) whose partial numerators and denominators are summed through
-// distributed shared memory once per tile.
+// Each CTA holds one 128-feature group of the head; a head of 256 features is spread over a
+// thread-block cluster of 2 CTAs whose partial numerators and denominators are summed through
+// distributed shared memory once per tile (wider heads run the one-tile-at-a-time scan of
+// tc_causal_wide.cuh).
 //
 // The tiles run as a software pipeline over four roles:
 //   warp 0      TMA producer: Q, K (single buffers) and V (two buffers) of the coming tiles;
