@@ -147,9 +147,10 @@ favor_status_t favor_attn_noncausal_noalloc(const void* Q, const void* K, const 
  * (S = sum_j phi(k_j) v_j^T, z = sum_j phi(k_j) over the tokens seen so far) lives in a
  * caller-owned device buffer, and each step appends one token and returns its output.
  *
- * favor_decode_state_bytes: size of the state for B*H heads (fp32 S [B*H][m][d], z [B*H][m] and one
- *   key stabiliser per head, 256-byte aligned pieces); SIZE_MAX for an unsupported shape
- *   (d in {64, 128}, m a multiple of 64 in [64, 512]).
+ * favor_decode_state_bytes: size of the state for B*H heads (fp32 S [B*H][m][d], z [B*H][m], a key
+ *   stabiliser per head and 64-feature block, the blocks' partial sums of the current step, and a
+ *   per-head counter; 256-byte aligned pieces); SIZE_MAX for an unsupported shape (d in {64, 128},
+ *   m a multiple of 64 in [64, 512]).
  * favor_decode_init: empties the state of every head (no token seen). Asynchronous on `stream`.
  * favor_decode_step: q, k, v, y are [B, H, d] (the new token of every head), Omega [m, d], all of
  *   dtype dt; state as initialised (256-byte aligned, at least favor_decode_state_bytes). Updates

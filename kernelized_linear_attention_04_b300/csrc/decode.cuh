@@ -5,14 +5,17 @@
 //   S <- f S + phi(k) v^T,   z <- f z + phi(k),   y = phi(q)^T S / phi(q)^T z,
 // one step of the causal recurrence (the new token attends to itself and every earlier token).
 //
-// Stabilisers (both cancel in the ratio; the common 1/sqrt(m) is dropped, so the ReLU family's
-// epsilon is scaled by sqrt(m)): the key stabiliser is a running constant per head kept in the
-// state. A new key whose largest exponent max_r (w_r . k^) - |k^|^2 / 2 exceeds it raises it to
-// that exponent, and f = exp(old - new) rescales the accumulated S and z (f = 1 otherwise, f = 0
-// for the first token), so no key feature exceeds 1. A query uses its own largest exponent.
+// The m features are processed in blocks of 64, one CTA per (head, block), each block with its own
+// stabilisers (all cancel in the ratio; the common 1/sqrt(m) is dropped, so the ReLU family's
+// epsilon is scaled by sqrt(m)). Block b of a head keeps a running key constant st_b in the state: a
+// new key whose largest exponent over the block, max_r (w_r . k^) - |k^|^2 / 2, exceeds it raises
+// it, and f = exp(old - new) rescales the block's S and z (f = 0 for the first token). The query
+// uses its largest exponent over the block, c_b. With num_b = phi_b(q)^T S_b and den_b = phi_b(q)^T z_b,
+//   y = sum_b w_b num_b / sum_b w_b den_b,   w_b = exp(c_b + st_b - max_b' (c_b' + st_b')),
+// which the last block of the head to finish computes (a per-head counter in the state, no waits).
 //
-// One CTA per head on the CUDA cores: the step reads and writes the head's m x d fp32 state once
-// (a memory-bound update) and reads Omega from L2.
+// Each CTA reads and writes its 64 x d fp32 block of the state once (a memory-bound update) and
+// reads its 64 rows of Omega from L2.
 #pragma once
 
 #include "common.cuh"
@@ -46,22 +49,24 @@ __device__ __forceinline__ float block_reduce_sum(float v, float* red) {
     return r;
 }
 
-// State of every head: S [BH][m][D], z [BH][m], stab [BH] (fp32; -inf before the first token).
-__global__ void decode_init(float* __restrict__ S, float* __restrict__ z, float* __restrict__ stab, int64_t nS,
-                            int64_t nz, int64_t nh) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nS; i += (int64_t)gridDim.x * blockDim.x)
-        S[i] = 0.f;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nz; i += (int64_t)gridDim.x * blockDim.x)
-        z[i] = 0.f;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nh; i += (int64_t)gridDim.x * blockDim.x)
-        stab[i] = -INFINITY;
+constexpr int kBlk = 64;  // features per CTA
+
+// State of every head: S [BH][m][D], z [BH][m], stab [BH][m/64] (fp32; -inf before the first
+// token), partials [BH][m/64][D + 2], counter [BH] (u32; 0 between steps).
+__global__ void decode_init(float* __restrict__ S, float* __restrict__ z, float* __restrict__ stab,
+                            unsigned* __restrict__ cnt, int64_t nS, int64_t nz, int64_t nst, int64_t nh) {
+    const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x, di = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = i0; i < nS; i += di) S[i] = 0.f;
+    for (int64_t i = i0; i < nz; i += di) z[i] = 0.f;
+    for (int64_t i = i0; i < nst; i += di) stab[i] = -INFINITY;
+    for (int64_t i = i0; i < nh; i += di) cnt[i] = 0u;
 }
 
-// Shared memory: q^, k^, v (D each), phi(q), phi(k) (m each), numerator partials (4 kThreads),
+// Shared memory: q^, k^, v (D each), phi(q), phi(k) (64 each), numerator partials (4 kThreads),
 // reduction scratch (kThreads / 32).
 template <int D>
-constexpr size_t decode_smem_floats(int m) {
-    return 3 * (size_t)D + 2 * (size_t)m + 4 * kThreads + kThreads / 32;
+constexpr size_t decode_smem_floats() {
+    return 3 * (size_t)D + 2 * kBlk + 4 * kThreads + kThreads / 32;
 }
 
 // 8 consecutive elements of a row of Omega as fp32 (one 16-byte load for bf16, two for fp32).
@@ -80,29 +85,47 @@ __device__ __forceinline__ void load8(const float* p, float (&x)[8]) {
     x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 
+// Grid (B*H heads, m / 64 blocks), kThreads threads.
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads)
     decode_step(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v, const T* __restrict__ Om,
-                T* __restrict__ y, float* __restrict__ S, float* __restrict__ z, float* __restrict__ stabs, int m,
-                int kind, float relu_eps_s, float scale) {
-    static_assert(kThreads % (D / 4) == 0 && D % 64 == 0, "rows of D/4 float4 columns; Omega rows of 8 x 16 bytes");
+                T* __restrict__ y, float* __restrict__ S, float* __restrict__ z, float* __restrict__ stabs,
+                float* __restrict__ part, unsigned* __restrict__ cnt, int m, int kind, float relu_eps_s, float scale) {
+    static_assert(kThreads % (D / 4) == 0 && D % 64 == 0 && kBlk % (kThreads / (D / 4)) == 0 && kBlk <= kThreads,
+                  "rows of D/4 float4 columns; Omega rows of 8 x 16 bytes; one z entry per thread");
     extern __shared__ float sm[];
-    float* sq = sm;           // scale * q
-    float* sk = sq + D;       // scale * k
-    float* sv = sk + D;       // v
-    float* pq = sv + D;       // phi(q), m
-    float* pk = pq + m;       // phi(k), m
-    float* nump = pk + m;     // [kThreads / (D / 4)][D] = 4 kThreads numerator partials
+    float* sq = sm;            // scale * q
+    float* sk = sq + D;        // scale * k
+    float* sv = sk + D;        // v
+    float* pq = sv + D;        // phi(q) of the block's 64 features
+    float* pk = pq + kBlk;     // phi(k)
+    float* nump = pk + kBlk;   // [kThreads / (D / 4)][D] = 4 kThreads numerator partials
     float* red = nump + 4 * kThreads;
+    __shared__ bool s_last;
+    const int nb = m / kBlk;
+    const int blk = blockIdx.y;
     const int64_t bh = blockIdx.x;
     const int tid = threadIdx.x;
     const bool exp_kind = kind == kKindExp;
+    const int f0 = blk * kBlk;  // first feature of this block
     q += bh * D;
     k += bh * D;
     v += bh * D;
     y += bh * D;
-    S += bh * (int64_t)m * D;
-    z += bh * (int64_t)m;
+    S += (bh * (int64_t)m + f0) * D;
+    z += bh * (int64_t)m + f0;
+
+    // the block's state does not depend on the new token: its loads go out first, so that their
+    // latency overlaps the token and Omega loads and the projections. Thread tid keeps columns
+    // c4 .. c4 + 3 (c4 = 4 (tid mod D/4)) of the rows tid / (D/4) + i kThreads / (D/4).
+    constexpr int kTpr = D / 4;
+    constexpr int kRows = kThreads / kTpr;
+    constexpr int kPer = kBlk / kRows;
+    const int c4 = 4 * (tid % kTpr), r0s = tid / kTpr;
+    float4 xs[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) xs[i] = *reinterpret_cast<const float4*>(S + (int64_t)(r0s + i * kRows) * D + c4);
+    const float zold = tid < kBlk ? z[tid] : 0.f;
 
     for (int c = tid; c < D; c += kThreads) {
         sq[c] = scale * to_f32(q[c]);
@@ -110,20 +133,20 @@ __global__ void __launch_bounds__(kThreads)
         sv[c] = to_f32(v[c]);
     }
     __syncthreads();
-    // |k^|^2 / 2 (every thread needs it; one pass over D in shared memory)
+    // |k^|^2 / 2 (every warp computes it from shared memory)
     float hk = 0.f;
     for (int c = tid % 32; c < D; c += 32) hk = fmaf(sk[c], sk[c], hk);
     hk = 0.5f * warp_sum(hk);
 
-    // projections u_r = w_r . x^ of the query and the key: a row of Omega per group of 8 lanes, D / 8
-    // consecutive elements per lane (coalesced 16-byte loads), summed across the group by shuffles
-    constexpr int kLpr = 8;               // lanes per row
-    constexpr int kEl = D / kLpr;         // elements per lane
+    // projections u_r = w_r . x^ of the query and the key for the block's rows: a row of Omega per
+    // group of 8 lanes, D / 8 consecutive elements per lane (coalesced 16-byte loads), shuffle sums
+    constexpr int kLpr = 8;
+    constexpr int kEl = D / kLpr;
     const int lr = (tid % 32) / kLpr, lc = tid % kLpr;
     float qmax = -INFINITY, kmax = -INFINITY;
-    for (int r0 = (tid / 32) * (32 / kLpr); r0 < m; r0 += kThreads / kLpr) {
+    for (int r0 = (tid / 32) * (32 / kLpr); r0 < kBlk; r0 += kThreads / kLpr) {
         const int r = r0 + lr;
-        const T* w = Om + (int64_t)r * D + lc * kEl;
+        const T* w = Om + (int64_t)(f0 + r) * D + lc * kEl;
         float uq = 0.f, uk = 0.f;
 #pragma unroll
         for (int e = 0; e < kEl; e += 8) {
@@ -148,16 +171,15 @@ __global__ void __launch_bounds__(kThreads)
         kmax = fmaxf(kmax, uk);
     }
     __syncthreads();
-    float f = 1.f;
-    float new_stab = 0.f;
+    float f = 1.f, new_stab = 0.f;
     if (exp_kind) {
         qmax = block_reduce_max(qmax, red);
-        kmax = block_reduce_max(kmax, red) - hk;  // the new key's largest exponent
-        const float old = stabs[bh];
+        kmax = block_reduce_max(kmax, red) - hk;  // the new key's largest exponent in this block
+        const float old = stabs[bh * nb + blk];
         new_stab = fmaxf(old, kmax);
         f = old == -INFINITY ? 0.f : exp_shift(old, new_stab);
     }
-    for (int r = tid; r < m; r += kThreads) {
+    for (int r = tid; r < kBlk; r += kThreads) {
         if (exp_kind) {
             pq[r] = exp_shift(pq[r], qmax);
             pk[r] = exp_shift(pk[r] - hk, new_stab);
@@ -168,18 +190,14 @@ __global__ void __launch_bounds__(kThreads)
     }
     __syncthreads();
 
-    // state update and the numerator: thread tid keeps the 4 columns c4 .. c4 + 3 (c4 = 4 (tid mod D/4))
-    // of the rows tid / (D/4) + i kThreads / (D/4): float4 loads and stores, 256 contiguous bytes per
-    // row and warp, four rows in flight per thread
-    constexpr int kTpr = D / 4;          // threads per row
-    constexpr int kRows = kThreads / kTpr;  // rows per pass
-    const int c4 = 4 * (tid % kTpr);
+    // state update and the block's numerator (float4 stores)
     const float4 v4 = make_float4(sv[c4], sv[c4 + 1], sv[c4 + 2], sv[c4 + 3]);
     float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int r = tid / kTpr; r < m; r += kRows) {
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int r = r0s + i * kRows;
         float4* sp = reinterpret_cast<float4*>(S + (int64_t)r * D + c4);
-        float4 x = *sp;
+        float4 x = xs[i];
         const float p = pk[r], g = pq[r];
         x.x = fmaf(f, x.x, p * v4.x);
         x.y = fmaf(f, x.y, p * v4.y);
@@ -192,20 +210,45 @@ __global__ void __launch_bounds__(kThreads)
         num.w = fmaf(g, x.w, num.w);
     }
     float den = 0.f;
-    for (int r = tid; r < m; r += kThreads) {
-        const float zr = fmaf(f, z[r], pk[r]);
-        z[r] = zr;
-        den = fmaf(pq[r], zr, den);
+    if (tid < kBlk) {
+        const float zr = fmaf(f, zold, pk[tid]);
+        z[tid] = zr;
+        den = pq[tid] * zr;
     }
     *reinterpret_cast<float4*>(nump + (tid / kTpr) * D + c4) = num;
     den = block_reduce_sum(den, red);  // its barriers also publish nump
+    float* mine = part + (bh * nb + blk) * (int64_t)(D + 2);
     if (tid < D) {
         float acc = 0.f;
 #pragma unroll 8
         for (int g = 0; g < kRows; ++g) acc += nump[g * D + tid];  // fixed order
-        store_elem(y + tid, acc / den);
+        mine[tid] = acc;
     }
-    if (tid == 0 && exp_kind) stabs[bh] = new_stab;
+    if (tid == 0) {
+        mine[D] = den;
+        mine[D + 1] = exp_kind ? qmax + new_stab : 0.f;  // log of the block's weight, up to a common constant
+        if (exp_kind) stabs[bh * nb + blk] = new_stab;
+    }
+    // the last block of the head to finish combines the partials
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(cnt + bh, 1u) == (unsigned)(nb - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const float* hp = part + bh * nb * (int64_t)(D + 2);
+    float M = -INFINITY;
+    for (int b = 0; b < nb; ++b) M = fmaxf(M, __ldcg(hp + b * (D + 2) + D + 1));
+    if (tid < D) {
+        float nsum = 0.f, dsum = 0.f;
+        for (int b = 0; b < nb; ++b) {  // fixed order
+            const float wb = exp_shift(__ldcg(hp + b * (D + 2) + D + 1), M);
+            nsum = fmaf(wb, __ldcg(hp + b * (D + 2) + tid), nsum);
+            dsum = fmaf(wb, __ldcg(hp + b * (D + 2) + D), dsum);
+        }
+        store_elem(y + tid, nsum / dsum);
+    }
+    if (tid == 0) cnt[bh] = 0u;  // ready for the next step (launches on a stream run in order)
 }
 
 }  // namespace dec

@@ -604,16 +604,19 @@ favor_status_t favor_attn_causal(const void* Q, const void* K, const void* V, co
 namespace favor {
 namespace {
 
-// ---- streaming decode state: S [BH][m][d], z [BH][m], stab [BH], fp32 ---------------------------
+// ---- streaming decode state: S [BH][m][d], z [BH][m], stab [BH][m/64], partials [BH][m/64][d+2]
+// (fp32), counter [BH] (u32) ---------------------------------------------------------------------
 struct DecodeLayout {
-    size_t off_z, off_stab, total;
+    size_t off_z, off_stab, off_part, off_cnt, total;
 };
 DecodeLayout decode_layout(int B, int H, int d, int m) {
-    const size_t BH = (size_t)B * H;
+    const size_t BH = (size_t)B * H, nb = (size_t)m / dec::kBlk;
     DecodeLayout L{};
     L.off_z = align_up(BH * m * d * sizeof(float), 256);
     L.off_stab = L.off_z + align_up(BH * m * sizeof(float), 256);
-    L.total = L.off_stab + align_up(BH * sizeof(float), 256);
+    L.off_part = L.off_stab + align_up(BH * nb * sizeof(float), 256);
+    L.off_cnt = L.off_part + align_up(BH * nb * (d + 2) * sizeof(float), 256);
+    L.total = L.off_cnt + align_up(BH * sizeof(unsigned), 256);
     return L;
 }
 
@@ -629,12 +632,13 @@ favor_status_t decode_launch(const void* q, const void* k, const void* v, const 
                              int m, int kind, float eps, cudaStream_t s) {
     const DecodeLayout L = decode_layout(BH, 1, D, m);
     char* base = static_cast<char*>(state);
-    const size_t smem = sizeof(float) * dec::decode_smem_floats<D>(m);
+    const size_t smem = sizeof(float) * dec::decode_smem_floats<D>();
     FAVOR_TRY(traced(FAVOR_KERNEL_DECODE, s, [&] {
-        dec::decode_step<T, D><<<BH, dec::kThreads, smem, s>>>(
+        dec::decode_step<T, D><<<dim3(BH, m / dec::kBlk), dec::kThreads, smem, s>>>(
             static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), static_cast<const T*>(Om),
             static_cast<T*>(y), reinterpret_cast<float*>(base), reinterpret_cast<float*>(base + L.off_z),
-            reinterpret_cast<float*>(base + L.off_stab), m, kind, eps * std::sqrt((float)m), qk_scale(D));
+            reinterpret_cast<float*>(base + L.off_stab), reinterpret_cast<float*>(base + L.off_part),
+            reinterpret_cast<unsigned*>(base + L.off_cnt), m, kind, eps * std::sqrt((float)m), qk_scale(D));
     }));
     return cudaGetLastError() == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;
 }
@@ -661,7 +665,9 @@ favor_status_t favor_decode_init(void* state, size_t state_bytes, int B, int H, 
     const int blocks = (int)std::min<int64_t>((nS + 255) / 256, 4 * kNumSMs);
     FAVOR_TRY(traced(FAVOR_KERNEL_DECODE_INIT, s, [&] {
         dec::decode_init<<<blocks, 256, 0, s>>>(reinterpret_cast<float*>(base), reinterpret_cast<float*>(base + L.off_z),
-                                               reinterpret_cast<float*>(base + L.off_stab), nS, BH * m, BH);
+                                               reinterpret_cast<float*>(base + L.off_stab),
+                                               reinterpret_cast<unsigned*>(base + L.off_cnt), nS, BH * m,
+                                               BH * (m / dec::kBlk), BH);
     }));
     return cudaGetLastError() == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;
 }

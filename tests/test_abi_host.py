@@ -74,9 +74,13 @@ def test_workspace_sizes_per_path():
     # the tensor-core causal scans keep the state in TMEM: no workspace
     for m in (64, 192, 256, 384, 512):
         assert favor.workspace_bytes("causal", 4, 16, 8192, 64, m, bf) == 0
-    # streaming decode state: fp32 S [BH][m][d], z [BH][m], one stabiliser per head, 256-byte pieces
-    assert favor.decode_state_bytes(2, 3, 64, 256) == 6 * 256 * 64 * 4 + 6 * 256 * 4 + 256
-    assert favor.decode_state_bytes(1, 1, 128, 512) == 512 * 128 * 4 + 512 * 4 + 256
+    # streaming decode state: fp32 S [BH][m][d], z [BH][m], stabilisers [BH][m/64], block partials
+    # [BH][m/64][d+2], u32 counter [BH]; 256-byte pieces
+    up = lambda b: (b + 255) // 256 * 256
+    assert favor.decode_state_bytes(2, 3, 64, 256) == (6 * 256 * 64 * 4 + 6 * 256 * 4 + up(6 * 4 * 4)
+                                                       + up(6 * 4 * 66 * 4) + up(6 * 4))
+    assert favor.decode_state_bytes(1, 1, 128, 512) == (512 * 128 * 4 + 512 * 4 + up(8 * 4) + up(8 * 130 * 4)
+                                                        + up(4))
     with pytest.raises(favor.FavorError):
         favor.decode_state_bytes(1, 1, 96, 256)
     # fp32, and bf16 with d = 128, take the CUDA-core scan, whose state lives in the workspace
