@@ -345,12 +345,14 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream()
 
     def call():
+        # on the current stream: the bench's stream, or the side stream of a graph capture
+        st = torch.cuda.current_stream()
         if w.causal:
             favor.favor_attn_causal(Q, K, V, Om, chunk=w.chunk, kind=w.kind, relu_eps=w.relu_eps, out=Y,
-                                    workspace=wsp, stream=stream)
+                                    workspace=wsp, stream=st)
         else:
             favor.favor_attn_noncausal(Q, K, V, Om, kind=w.kind, relu_eps=w.relu_eps, out=Y, workspace=wsp,
-                                       stream=stream)
+                                       stream=st)
 
     step_bytes = path_work(w)[1]
     flush = step_bytes < 2 * L2_BYTES
@@ -369,6 +371,24 @@ def run_ours(args, w):
         torch.cuda.synchronize()
         return [a.elapsed_time(b) for a, b in evs]
 
+    def timed_graph(n_steps, body):
+        # the steps (each behind its L2 flush, bracketed by event-record nodes) captured into one
+        # CUDA graph and launched once: no host work can fall between a step's two events
+        evs = [(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
+               for _ in range(n_steps)]
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for a, b in evs:
+                if fbuf is not None:
+                    fbuf.zero_()
+                a.record()
+                body()
+                b.record()
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
     # -- device-resident throughput (clocks sampled from the warm-up on, so the GPU is under load) --
     sampler = ClockSampler(local)
     with sampler:
@@ -378,7 +398,12 @@ def run_ours(args, w):
         assert favor.last_device_error() == 0
         barrier()
         torch.cuda.synchronize()
-        ms = timed_loop(args.steps, call)
+        try:
+            ms, timing = timed_graph(args.steps, call), "one CUDA graph of the timed steps"
+        except RuntimeError as e:  # capture unsupported here: eager launches, queued ahead of the device
+            torch.cuda.synchronize()
+            ms, timing = timed_loop(args.steps, call), f"eager launches (graph capture failed: {str(e)[:80]})"
+        assert favor.last_device_error() == 0
         barrier()
         torch.cuda.synchronize()
     ms_per_step = max_over_ranks(sum(ms) / len(ms), dev)
@@ -392,7 +417,11 @@ def run_ours(args, w):
     launched = {k: v for k, v in tr.items() if v[0] > 0}
     launches_per_step = sum(v[0] for v in launched.values()) / args.steps
     dom = max(launched, key=lambda k: launched[k][1])
-    dom_ms = launched[dom][1] / launched[dom][0]
+    dom_ms = eager_ms = launched[dom][1] / launched[dom][0]
+    dur_src = "events around each launch, eager"
+    if timing.startswith("one CUDA graph") and launches_per_step == 1:
+        # the step is this one launch: its graph-timed duration carries no host launch latency
+        dom_ms, dur_src = sum(ms) / len(ms), "graph-timed step (the step is this one launch)"
     flops, nbytes = kernel_work(w, dom)
     peaks, peak_kind = load_peaks()
     t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
@@ -411,7 +440,8 @@ def run_ours(args, w):
     tr_entry = NCU_TRAFFIC.get(f"{w.name}:{dom}")
     traffic = tr_entry["bytes"] if tr_entry and tr_entry.get("src") == src else None
     roofline = {"bound": bound, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
-                "traffic": traffic, "kernel": dom, "kernel_ms": dom_ms, "peak_source": note,
+                "traffic": traffic, "kernel": dom, "kernel_ms": dom_ms, "duration_source": dur_src,
+                "kernel_ms_eager": eager_ms, "peak_source": note,
                 "algorithmic_flops": flops, "algorithmic_bytes": nbytes,
                 "kernels_ms": {k: v[1] / v[0] for k, v in launched.items()}}
     # whole-path roofline fraction (the slower of flops at the tensor peak and bytes at HBM)
@@ -444,7 +474,7 @@ def run_ours(args, w):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
-            "config": workload_config(w, l2_note),
+            "config": {**workload_config(w, l2_note), "timing": timing},
             "path_roofline_frac": (t_roof * 1e3) / ms_per_step,
             "roofline": roofline,
             "e2e": {"value": world * w.tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -487,10 +517,6 @@ def run_decode(args, w):
     def step(i):
         favor.favor_decode_step(toks[0, i], toks[1, i], toks[2, i], Om, state, kind=w.kind, relu_eps=w.relu_eps, out=y)
 
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    assert favor.last_device_error() == 0
     BH = w.B * w.H
     s_el = 4 if dt == torch.float32 else 2
     nbytes = BH * (2 * w.m * w.d * 4 + 2 * w.m * 4 + 4 * w.d * s_el) + w.m * w.d * s_el
@@ -508,28 +534,65 @@ def run_decode(args, w):
             step(n0 + i)
             b.record()
         torch.cuda.synchronize()
-        return sum(a.elapsed_time(b) for a, b in evs) / args.steps
+        return [a.elapsed_time(b) for a, b in evs]
 
+    def timed_graph(n0):
+        # the K steps (each behind its L2 flush, bracketed by event-record nodes) captured into one
+        # CUDA graph and launched once: no host work can fall between a step's two events
+        evs = [(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
+               for _ in range(args.steps)]
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i, (a, b) in enumerate(evs):
+                if fbuf is not None:
+                    fbuf.zero_()
+                a.record()
+                step(n0 + i)
+                b.record()
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    # clocks sampled from the warm-up on, so that the timed steps start on a busy GPU
     sampler = ClockSampler(0)
     with sampler:
-        ms = timed(args.warmup)
+        for i in range(args.warmup):
+            if fbuf is not None:
+                fbuf.zero_()
+            step(i)
+        torch.cuda.synchronize()
+        assert favor.last_device_error() == 0
+        try:
+            per_step, timing = timed_graph(args.warmup), "one CUDA graph of the timed steps"
+        except RuntimeError as e:  # capture unsupported here: eager launches, queued ahead of the device
+            per_step, timing = timed(args.warmup), f"eager launches (graph capture failed: {str(e)[:80]})"
+        assert favor.last_device_error() == 0
+    ms = sum(per_step) / len(per_step)
     favor.trace_enable(True)
     timed(args.warmup)
     tr = favor.trace_read()
     favor.trace_enable(False)
-    k_ms = tr["decode"][1] / tr["decode"][0]
+    k_ms = eager_ms = tr["decode"][1] / tr["decode"][0]
+    dur_src = "events around each launch, eager"
+    if timing.startswith("one CUDA graph"):
+        # a decode step is exactly one launch of the kernel
+        k_ms, dur_src = ms, "graph-timed step (the step is this one launch)"
     peaks, peak_kind = load_peaks()
     ach = nbytes / (k_ms * 1e-3) / 1e9
     line = {
         "metric": "FAVOR+ streaming decode tokens/s (B*H new tokens per s)", "value": BH / (ms * 1e-3),
         "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "ms_per_step_median": float(np.median(per_step)), "ms_per_step_max": max(per_step),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32" if dt == torch.float32 else "bf16",
         "data": "synthetic",
         "config": {"workload": f"decode_{w.dtype}_B{w.B}H{w.H}d{w.d}m{w.m}", "form": "streaming decode step",
                    "features": w.kind, "B": w.B, "H": w.H, "d": w.d, "m": w.m,
-                   "l2": "flushed before every timed step (512 MB write)" if flush else "state larger than L2"},
+                   "l2": "flushed before every timed step (512 MB write)" if flush else "state larger than L2",
+                   "timing": timing},
         "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": ach / peaks["hbm_gbs"], "traffic": None, "kernel": "decode", "kernel_ms": k_ms,
+                     "duration_source": dur_src, "kernel_ms_eager": eager_ms,
                      "peak_source": f"HBM copy, {peak_kind}", "algorithmic_bytes": nbytes},
         "gpu_launches": args.steps, "clocks": sampler.summary(),
     }
