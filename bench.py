@@ -47,6 +47,8 @@ QUEUE_AHEAD_CYCLES = 5_000_000
 # Nominal unit counts used where a kernel is bound by plain CUDA-core arithmetic:
 # 148 SMs x 128 fp32 FMA lanes x 2 flop x 2.032 GHz.
 FP32_SIMT_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
+# Nominal dense FP64 rate of a B300 (far below its low-precision tensor rates).
+FP64_PEAK_TFLOPS = 1.25
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the committed ncu
 # captures, valid only while the kernel sources hash to `src`.
@@ -599,6 +601,73 @@ def run_decode(args, w):
     print(json.dumps(line))
 
 
+def omega_flops(m: int, d: int) -> float:
+    """fp64 flops of one Omega build: per block of r rows, the projections (a dot product and an
+    update, 4d each, for every pair of rows) and the normalisations and chi lengths (5d per row).
+    The Box-Muller draws (2 d^2 logarithms and cosines per block) are not counted."""
+    total = 0.0
+    for b in range(-(-m // d)):
+        r = min(d, m - b * d)
+        total += 2.0 * d * r * (r - 1) + 5.0 * d * r
+    return total
+
+
+def run_omega(args, w):
+    """On-device Omega builder: one favor_omega per timed step for the workload's m and d, the
+    steps captured in one CUDA graph with the L2 flush between them."""
+    import torch
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    import kernelized_linear_attention_04_b300 as favor
+
+    dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    Om = torch.empty(w.m, w.d, dtype=dt, device=dev)
+    fbuf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(i):
+        favor.favor_omega(w.omega_seed + i, w.m, w.d, dtype=dt, out=Om)
+
+    sampler = ClockSampler(0)
+    with sampler:
+        for i in range(args.warmup):
+            fbuf.zero_()
+            step(i)
+        torch.cuda.synchronize()
+        assert favor.last_device_error() == 0
+        evs = [(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
+               for _ in range(args.steps)]
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i, (a, b) in enumerate(evs):
+                fbuf.zero_()
+                a.record()
+                step(args.warmup + i)
+                b.record()
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        per_step = [a.elapsed_time(b) for a, b in evs]
+    ms = sum(per_step) / len(per_step)
+    flops = omega_flops(w.m, w.d)
+    ach = flops / (ms * 1e-3) / 1e12
+    line = {
+        "metric": "FAVOR+ random projection rows built per s (orthogonal, on device)", "value": w.m / (ms * 1e-3),
+        "unit": "rows/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "ms_per_step_median": float(np.median(per_step)), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"omega_{w.dtype}_m{w.m}d{w.d}", "form": "orthogonal random features",
+                   "m": w.m, "d": w.d, "output": w.dtype, "l2": "flushed before every timed step (512 MB write)",
+                   "timing": "one CUDA graph of the timed steps"},
+        "roofline": {"bound": "alu", "achieved": ach, "peak": FP64_PEAK_TFLOPS, "unit": "TFLOP/s",
+                     "frac": ach / FP64_PEAK_TFLOPS, "traffic": None, "kernel": "omega", "kernel_ms": ms,
+                     "duration_source": "graph-timed step (the step is this one launch)",
+                     "peak_source": "nominal dense FP64 of a B300", "algorithmic_flops": flops},
+        "gpu_launches": args.steps, "clocks": sampler.summary(),
+    }
+    print(json.dumps(line))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -609,6 +678,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the host-core oracle timing")
     ap.add_argument("--decode", action="store_true",
                     help="time the streaming decode step at the workload's B, H, d, m instead of the full call")
+    ap.add_argument("--omega", action="store_true",
+                    help="time the on-device Omega builder at the workload's m and d instead of the full call")
     ap.add_argument("--n", type=int, default=None,
                     help="override the sequence length (smaller cases for profiler captures; not a bench line)")
     args = ap.parse_args(argv)
@@ -624,6 +695,8 @@ def main(argv=None):
         return run_reference(args, w)
     if args.decode:
         return run_decode(args, w)
+    if args.omega:
+        return run_omega(args, w)
     return run_ours(args, w)
 
 

@@ -165,6 +165,25 @@ favor_status_t favor_decode_step(const void* q, const void* k, const void* v, co
                                  void* state, size_t state_bytes, int B, int H, int d, int m, favor_dtype_t dt,
                                  favor_kind_t kind, float relu_eps, void* stream);
 
+/*
+ * Random projection Omega built on the device ("Performer for vision", *What Is Performer?*,
+ * Orthogonal Features; the "Performer" paper note, FAVOR+ section: positive orthogonal random
+ * features). Writes Omega [m, d] (row-major, dtype dt, 16-byte aligned, caller-owned) for `seed`:
+ *   orthogonal != 0: for every block of d rows, a d x d matrix of iid N(0, 1) draws whose rows are
+ *     orthonormalised in order (modified Gram-Schmidt, fp64), each row then scaled to the length of
+ *     an independent N(0, I_d) vector (a chi_d sample); the last block keeps its first m mod d rows;
+ *   orthogonal == 0: m rows of iid N(0, 1) draws.
+ * Draws: element i of stream s of the seed is the cosine branch of Box-Muller applied to two
+ * uniforms from SplitMix64's finaliser (key = splitmix64(splitmix64(seed) ^ s * 0xD1B54A32D192ED03),
+ * u1 = ((splitmix64(key + 2i) >> 11) + 1) 2^-53, u2 = (splitmix64(key + 2i + 1) >> 11) 2^-53); the
+ * Gaussian blocks are stream 4 (element (b d + r) d + c for row r, column c of block b), the chi
+ * lengths stream 5 (elements r d .. r d + d - 1 for row r of Omega). Values are computed in fp64 and
+ * rounded to fp32 (to nearest) and then, for bf16, to bf16 (to nearest even). Redrawing the features
+ * is a call with a new seed. d in {64, 128}, m >= 0 (m == 0: nothing runs). Asynchronous on
+ * `stream`; errors as for the attention calls.
+ */
+favor_status_t favor_omega(uint64_t seed, int m, int d, int orthogonal, favor_dtype_t dt, void* Omega, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* favor_status_string(favor_status_t status);
 
@@ -187,7 +206,8 @@ typedef enum {
     FAVOR_KERNEL_FUSED = 6,         /* single-launch non-causal path for short sequences      */
     FAVOR_KERNEL_DECODE = 7,        /* streaming decode step (favor_decode_step)              */
     FAVOR_KERNEL_DECODE_INIT = 8,   /* decode state reset (favor_decode_init)                 */
-    FAVOR_KERNEL_COUNT = 9
+    FAVOR_KERNEL_OMEGA = 9,         /* random projection builder (favor_omega)                */
+    FAVOR_KERNEL_COUNT = 10
 } favor_kernel_id_t;
 
 /* Starts (on != 0) or stops recording. Starting clears previous records. While recording, every

@@ -23,7 +23,7 @@ from . import build as _build
 __all__ = [
     "FavorError", "favor_features", "favor_attn_noncausal", "favor_attn_causal", "favor_attn_noncausal_noalloc",
     "workspace_bytes", "NOALLOC_SCRATCH_BYTES",
-    "decode_state_bytes", "decode_state", "favor_decode_init", "favor_decode_step",
+    "decode_state_bytes", "decode_state", "favor_decode_init", "favor_decode_step", "favor_omega",
     "last_device_error", "trace_enable", "trace_read", "abi_version", "lib", "LIB_PATH",
     "KERNEL_NAMES", "EXPORTED_SYMBOLS",
 ]
@@ -36,7 +36,7 @@ _STABS = {"none": 0, "row": 1, "head": 2}
 _OPS = {"features": 0, "noncausal": 1, "causal": 2}
 _STATUS = {0: "FAVOR_OK", 1: "FAVOR_ERR_INVALID_ARG", 2: "FAVOR_ERR_UNSUPPORTED", 3: "FAVOR_ERR_MISALIGNED",
            4: "FAVOR_ERR_WORKSPACE", 5: "FAVOR_ERR_CUDA", 6: "FAVOR_ERR_TIMEOUT"}
-KERNEL_COUNT = 9
+KERNEL_COUNT = 10
 # Size of the library's fixed scratch array used by favor_attn_noncausal_noalloc.
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -45,7 +45,7 @@ EXPORTED_SYMBOLS = (
     "favor_workspace_bytes", "favor_features", "favor_attn_noncausal", "favor_attn_causal",
     "favor_status_string", "favor_last_device_error", "favor_abi_version", "favor_trace_enable",
     "favor_trace_read", "favor_kernel_name", "favor_attn_noncausal_noalloc",
-    "favor_decode_state_bytes", "favor_decode_init", "favor_decode_step",
+    "favor_decode_state_bytes", "favor_decode_init", "favor_decode_step", "favor_omega",
 )
 
 
@@ -87,6 +87,8 @@ def _load() -> ctypes.CDLL:
     L.favor_decode_init.restype = i32
     L.favor_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, sz, i32, i32, i32, i32, i32, i32, f32, vp]
     L.favor_decode_step.restype = i32
+    L.favor_omega.argtypes = [ctypes.c_uint64, i32, i32, i32, i32, vp, vp]
+    L.favor_omega.restype = i32
     return L
 
 
@@ -267,4 +269,21 @@ def favor_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, Omega: 
     _check(lib.favor_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(Omega), _ptr(out), _ptr(state),
                                  state.numel() * state.element_size(), B, H, d, m, _DTYPES[q.dtype], _KINDS[kind],
                                  relu_eps, _stream_handle(stream)), "favor_decode_step")
+    return out
+
+
+# ---- random projection -------------------------------------------------------------------------------
+
+def favor_omega(seed: int, m: int, d: int, *, dtype=torch.bfloat16, orthogonal: bool = True, out=None,
+                device="cuda", stream=None) -> torch.Tensor:
+    """Omega [m, d] for `seed`, built on the device: orthogonal random features (Gaussian blocks of
+    d rows orthonormalised in order, each row scaled to a chi_d length), or iid Gaussian rows."""
+    if dtype not in _DTYPES:
+        raise TypeError("dtype must be torch.float32 or torch.bfloat16")
+    if out is None:
+        out = torch.empty(m, d, dtype=dtype, device=device)
+    elif out.shape != (m, d) or out.dtype != dtype or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous [{m}, {d}] {dtype} tensor")
+    _check(lib.favor_omega(ctypes.c_uint64(int(seed) & (2**64 - 1)), m, d, 1 if orthogonal else 0, _DTYPES[dtype],
+                           _ptr(out), _stream_handle(stream)), "favor_omega")
     return out

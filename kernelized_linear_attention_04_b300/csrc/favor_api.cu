@@ -18,6 +18,7 @@
 #include "tc_features.cuh"
 #include "tc_fused.cuh"
 #include "decode.cuh"
+#include "omega.cuh"
 #include "tma_host.h"
 
 namespace favor {
@@ -533,6 +534,7 @@ const char* favor_kernel_name(int kid) {
         case FAVOR_KERNEL_CAUSAL: return "causal";
         case FAVOR_KERNEL_DECODE: return "decode";
         case FAVOR_KERNEL_DECODE_INIT: return "decode_init";
+        case FAVOR_KERNEL_OMEGA: return "omega";
         case FAVOR_KERNEL_FUSED: return "fused";
     }
     return "unknown";
@@ -643,6 +645,19 @@ favor_status_t decode_launch(const void* q, const void* k, const void* v, const 
     return cudaGetLastError() == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;
 }
 
+template <typename T, int D>
+favor_status_t omega_launch(uint64_t seed, int m, bool orthogonal, void* Om, cudaStream_t s) {
+    const size_t smem = omg::omega_smem_bytes<D>();
+    FAVOR_TRY(set_smem(omg::omega_build<T, D>, smem));
+    const int blocks = (m + D - 1) / D;
+    FAVOR_TRY(traced(FAVOR_KERNEL_OMEGA, s, [&] {
+        omg::omega_build<T, D><<<blocks, omg::kThreads, smem, s>>>(omg::stream_key(seed, omg::kStreamGauss),
+                                                                    omg::stream_key(seed, omg::kStreamChi), m,
+                                                                    orthogonal ? 1 : 0, static_cast<T*>(Om));
+    }));
+    return cudaGetLastError() == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace favor
 
@@ -680,6 +695,16 @@ favor_status_t favor_decode_step(const void* q, const void* k, const void* v, co
     FAVOR_TRY(check_decode_state(state, state_bytes, B, H, d, m));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return FAVOR_DISPATCH(dt, d, decode_launch, q, k, v, Omega, y, state, B * H, m, (int)kind, relu_eps, s);
+}
+
+favor_status_t favor_omega(uint64_t seed, int m, int d, int orthogonal, favor_dtype_t dt, void* Omega, void* stream) {
+    if (m < 0 || (dt != FAVOR_F32 && dt != FAVOR_BF16)) return FAVOR_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FAVOR_ERR_UNSUPPORTED;
+    if (m == 0) return FAVOR_OK;
+    if (!Omega) return FAVOR_ERR_INVALID_ARG;
+    if (!aligned(Omega, 16)) return FAVOR_ERR_MISALIGNED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return FAVOR_DISPATCH(dt, d, omega_launch, seed, m, orthogonal != 0, Omega, s);
 }
 
 }  // extern "C"

@@ -157,3 +157,35 @@ def softmax_attention(Q, K, V, *, causal: bool = False):
     s = s - s.max(axis=-1, keepdims=True)
     e = np.exp(s)
     return (e / e.sum(axis=-1, keepdims=True)) @ V
+
+
+def omega_orf(seed: int, m: int, d: int, *, orthogonal: bool = True) -> np.ndarray:
+    """The random projection Omega [m, d] in fp64, as the device builder defines it.
+
+    Orthogonal random features ("Performer for vision", *What Is Performer?*, Orthogonal Features;
+    the "Performer" paper note, FAVOR+ section): for each block b of d rows, G_b is a d x d matrix of
+    N(0, 1) draws (element (b d + r) d + c of the generator's stream 4); its rows are orthonormalised
+    in order (row r minus its components along the already finished rows 0 .. r-1, one at a time,
+    then divided by its length); row r of Omega is that unit row times chi_r, the length of the
+    d draws r d .. r d + d - 1 of stream 5, so that it is again marginally N(0, I_d). The last block
+    keeps its first m - b d rows. orthogonal=False: the m iid Gaussian rows themselves.
+    The draws come from ``seeded_inputs.normal``; everything else is written out here.
+    """
+    import seeded_inputs as si
+
+    if m < 0 or d <= 0:
+        raise ValueError("m must be >= 0 and d > 0")
+    nblk = -(-m // d)
+    G = si.normal(seed, 4, nblk * d * d).reshape(nblk, d, d)
+    if not orthogonal:
+        return np.ascontiguousarray(G.reshape(nblk * d, d)[:m])
+    E = np.empty_like(G)
+    for b in range(nblk):
+        for r in range(d):
+            v = G[b, r].copy()
+            for j in range(r):
+                v = v - np.dot(v, E[b, j]) * E[b, j]
+            E[b, r] = v / np.sqrt(np.dot(v, v))
+    x = si.normal(seed, 5, m * d).reshape(m, d)
+    chi = np.sqrt(np.einsum("rc,rc->r", x, x))
+    return np.ascontiguousarray(E.reshape(nblk * d, d)[:m] * chi[:, None])

@@ -37,6 +37,7 @@ def test_status_strings_and_kernel_names():
     for code in range(7):
         assert favor.lib.favor_status_string(code).decode().startswith("FAVOR_")
     assert favor.KERNEL_NAMES[0] == "features"
+    assert favor.KERNEL_NAMES[-1] == "omega"
 
 
 def test_workspace_sizes():
@@ -143,6 +144,14 @@ def test_argument_checks_reject_before_launch():
     assert di(N, need, 1, 1, 64, 64, S) == 1
     assert di(P, need - 1, 1, 1, 64, 64, S) == 4
     assert di(N, 0, 0, 1, 64, 64, S) == 0
+    # random projection builder: every failing check comes before the launch; m = 0 is a no-op
+    om = L.favor_omega
+    assert om(1, 64, 96, 1, 1, P, S) == 2          # unsupported d
+    assert om(1, 64, 64, 1, 1, N, S) == 1          # null output
+    assert om(1, 64, 64, 1, 1, Mis, S) == 3        # misaligned output
+    assert om(1, -1, 64, 1, 1, P, S) == 1          # negative m
+    assert om(1, 64, 64, 1, 7, P, S) == 1          # bad dtype
+    assert om(1, 0, 64, 1, 1, N, S) == 0           # nothing to build
 
 
 def test_python_binding_validates_shapes():
