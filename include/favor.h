@@ -20,7 +20,10 @@
  *     Callers pass RAW q and k: the d^(-1/4) scaling is applied inside.
  *   - All device pointers must be 16-byte aligned; workspace must be 256-byte aligned.
  *   - Supported shapes: d in {64, 128}; m a multiple of 64 with 64 <= m <= 512; n >= 0; B, H >= 0.
- *     B*H*n == 0 is a valid empty call that returns FAVOR_OK and touches no memory.
+ *     B*H*n == 0 is a valid empty call that returns FAVOR_OK and touches no memory. Head count:
+ *     B*H <= 65535 for favor_features and the non-causal calls (heads index a grid dimension of
+ *     that size), B*H <= 2^24 for the causal and decode calls; larger counts return
+ *     FAVOR_ERR_UNSUPPORTED (favor_workspace_bytes and favor_decode_state_bytes: SIZE_MAX).
  *   - Arithmetic: fp32 inputs are computed in fp32 on CUDA cores; bf16 inputs run on the tensor
  *     cores with fp32 accumulation (features rounded to bf16 between the two contractions).
  *   - Ownership: the caller owns every buffer. The library allocates no device memory; it keeps only

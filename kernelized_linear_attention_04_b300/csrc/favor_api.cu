@@ -102,6 +102,12 @@ favor_status_t check_shape(int B, int H, int n, int d, int m, favor_dtype_t dt, 
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Head-count limits of the launches: B*H heads index gridDim.y of the feature-map and non-causal
+// kernels (at most 65535), and gridDim.x (with up to 4 CTAs per head) everywhere else.
+constexpr int64_t kMaxHeadsGridY = 65535;
+constexpr int64_t kMaxHeads = int64_t(1) << 24;
+bool heads_ok(int B, int H, int64_t limit) { return (int64_t)B * H <= limit; }
+
 constexpr int kMaxSplits = 64;
 
 // Token splits of the non-causal state pass: enough CTAs to fill the GPU about twice, at least
@@ -544,6 +550,7 @@ size_t favor_workspace_bytes(favor_op_t op, int B, int H, int n, int d, int m, f
                              favor_stab_t stab, int chunk) {
     if (check_shape(B, H, n, d, m, dt, kind) != FAVOR_OK) return (size_t)-1;
     if ((int64_t)B * H * n == 0) return 0;
+    if (!heads_ok(B, H, op == FAVOR_OP_CAUSAL ? kMaxHeads : kMaxHeadsGridY)) return (size_t)-1;
     switch (op) {
         case FAVOR_OP_FEATURES: return features_ws_bytes(B, H, kind, stab);
         case FAVOR_OP_NONCAUSAL: return noncausal_ws_bytes(B, H, n, d, m, dt);
@@ -561,6 +568,7 @@ favor_status_t favor_features(const void* X, const void* Omega, float* Phi, int 
     if (stab != FAVOR_STAB_NONE && stab != FAVOR_STAB_ROW && stab != FAVOR_STAB_HEAD) return FAVOR_ERR_INVALID_ARG;
     if (!(relu_eps >= 0.f) || !std::isfinite(relu_eps)) return FAVOR_ERR_INVALID_ARG;
     if ((int64_t)B * H * n == 0) return FAVOR_OK;
+    if (!heads_ok(B, H, kMaxHeadsGridY)) return FAVOR_ERR_UNSUPPORTED;
     if (!X || !Omega || !Phi) return FAVOR_ERR_INVALID_ARG;
     if (!aligned(X, 16) || !aligned(Omega, 16) || !aligned(Phi, 16)) return FAVOR_ERR_MISALIGNED;
     FAVOR_TRY(check_ws(workspace, ws_bytes, features_ws_bytes(B, H, kind, stab)));
@@ -577,6 +585,7 @@ favor_status_t favor_attn_noncausal(const void* Q, const void* K, const void* V,
                                     void* workspace, size_t ws_bytes, void* stream) {
     FAVOR_TRY(check_attn_args(Q, K, V, Omega, Y, B, H, n, d, m, dt, kind, relu_eps));
     if ((int64_t)B * H * n == 0) return FAVOR_OK;
+    if (!heads_ok(B, H, kMaxHeadsGridY)) return FAVOR_ERR_UNSUPPORTED;
     FAVOR_TRY(check_ws(workspace, ws_bytes, noncausal_ws_bytes(B, H, n, d, m, dt)));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (tc_fused_ok(n, d, m, dt)) return tc_fused(Q, K, V, Omega, Y, B, H, n, m, (int)kind, relu_eps, workspace, s);
@@ -592,6 +601,7 @@ favor_status_t favor_attn_causal(const void* Q, const void* K, const void* V, co
     FAVOR_TRY(check_attn_args(Q, K, V, Omega, Y, B, H, n, d, m, dt, kind, relu_eps));
     if (chunk != 0 && chunk != 64 && chunk != 128) return FAVOR_ERR_UNSUPPORTED;
     if ((int64_t)B * H * n == 0) return FAVOR_OK;
+    if (!heads_ok(B, H, kMaxHeads)) return FAVOR_ERR_UNSUPPORTED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (tc_causal_ok(d, m, dt)) return tc_causal(Q, K, V, Omega, Y, B, H, n, m, (int)kind, relu_eps, s);
     FAVOR_TRY(check_ws(workspace, ws_bytes, causal_ws_bytes(B, H, d, m)));
@@ -665,12 +675,14 @@ extern "C" {
 
 size_t favor_decode_state_bytes(int B, int H, int d, int m) {
     if (check_shape(B, H, 1, d, m, FAVOR_BF16, FAVOR_EXP) != FAVOR_OK) return SIZE_MAX;
+    if (!heads_ok(B, H, kMaxHeads)) return SIZE_MAX;
     return decode_layout(B, H, d, m).total;
 }
 
 favor_status_t favor_decode_init(void* state, size_t state_bytes, int B, int H, int d, int m, void* stream) {
     FAVOR_TRY(check_shape(B, H, 1, d, m, FAVOR_BF16, FAVOR_EXP));
     if ((int64_t)B * H == 0) return FAVOR_OK;
+    if (!heads_ok(B, H, kMaxHeads)) return FAVOR_ERR_UNSUPPORTED;
     FAVOR_TRY(check_decode_state(state, state_bytes, B, H, d, m));
     const DecodeLayout L = decode_layout(B, H, d, m);
     char* base = static_cast<char*>(state);
@@ -692,6 +704,7 @@ favor_status_t favor_decode_step(const void* q, const void* k, const void* v, co
                                  float relu_eps, void* stream) {
     FAVOR_TRY(check_attn_args(q, k, v, Omega, y, B, H, 1, d, m, dt, kind, relu_eps));
     if ((int64_t)B * H == 0) return FAVOR_OK;
+    if (!heads_ok(B, H, kMaxHeads)) return FAVOR_ERR_UNSUPPORTED;
     FAVOR_TRY(check_decode_state(state, state_bytes, B, H, d, m));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return FAVOR_DISPATCH(dt, d, decode_launch, q, k, v, Omega, y, state, B * H, m, (int)kind, relu_eps, s);
@@ -744,6 +757,7 @@ favor_status_t favor_attn_noncausal_noalloc(const void* Q, const void* K, const 
                                             float relu_eps, void* stream) {
     FAVOR_TRY(check_attn_args(Q, K, V, Omega, Y, B, H, n, d, m, dt, kind, relu_eps));
     if ((int64_t)B * H * n == 0) return FAVOR_OK;
+    if (!heads_ok(B, H, kMaxHeadsGridY)) return FAVOR_ERR_UNSUPPORTED;
     const size_t need = favor_workspace_bytes(FAVOR_OP_NONCAUSAL, B, H, n, d, m, dt, kind, FAVOR_STAB_NONE, 0);
     if (need > FAVOR_NOALLOC_SCRATCH_BYTES) return FAVOR_ERR_WORKSPACE;
     void* scratch = nullptr;

@@ -84,6 +84,15 @@ def test_workspace_sizes_per_path():
                                                         + up(4))
     with pytest.raises(favor.FavorError):
         favor.decode_state_bytes(1, 1, 96, 256)
+    # head-count limits (see include/favor.h): grid-y paths take at most 65535 heads
+    assert favor.workspace_bytes("noncausal", 1, 65535, 16, 64, 64, bf) > 0
+    with pytest.raises(favor.FavorError):
+        favor.workspace_bytes("noncausal", 1, 65536, 16, 64, 64, bf)
+    with pytest.raises(favor.FavorError):
+        favor.workspace_bytes("features", 2, 40000, 16, 64, 64, bf, stab="head")
+    assert favor.workspace_bytes("causal", 1, 65536, 16, 64, 64, bf) == 0
+    with pytest.raises(favor.FavorError):
+        favor.decode_state_bytes(1 << 13, 1 << 12, 64, 64)
     # fp32, and bf16 with d = 128, take the CUDA-core scan, whose state lives in the workspace
     assert favor.workspace_bytes("causal", 1, 2, 300, 64, 256, f32) >= 2 * (256 * 64 + 256) * 4
     assert favor.workspace_bytes("causal", 1, 2, 300, 128, 256, bf) >= 2 * (256 * 128 + 256) * 4
@@ -144,6 +153,15 @@ def test_argument_checks_reject_before_launch():
     assert di(N, need, 1, 1, 64, 64, S) == 1
     assert di(P, need - 1, 1, 1, 64, 64, S) == 4
     assert di(N, 0, 0, 1, 64, 64, S) == 0
+    # head-count limits: rejected before anything is launched (empty calls stay no-ops)
+    assert nc(P, P, P, P, P, 65536, 1, 16, 64, 64, 1, 0, 0.0, P, 1 << 30, S) == 2
+    assert nc(P, P, P, P, P, 256, 256, 16, 64, 64, 1, 0, 0.0, P, 1 << 30, S) == 2
+    assert nc(N, N, N, N, N, 65536, 1, 0, 64, 64, 1, 0, 0.0, N, 0, S) == 0
+    assert L.favor_attn_noncausal_noalloc(P, P, P, P, P, 65536, 1, 16, 64, 64, 1, 0, 0.0, S) == 2
+    assert ft(P, P, P, 65536, 1, 16, 64, 64, 1, 0, 0.0, 1, N, 0, S) == 2
+    assert ca(P, P, P, P, P, 1 << 13, 1 << 12, 16, 64, 64, 64, 1, 0, 0.0, P, 1 << 20, S) == 2
+    assert ds(P, P, P, P, P, P, need, 1 << 13, 1 << 12, 64, 64, 1, 0, 0.0, S) == 2
+    assert di(P, need, 1 << 13, 1 << 12, 64, 64, S) == 2
     # random projection builder: every failing check comes before the launch; m = 0 is a no-op
     om = L.favor_omega
     assert om(1, 64, 96, 1, 1, P, S) == 2          # unsupported d
