@@ -115,6 +115,23 @@ def _ptr(t) -> ctypes.c_void_p:
     return ctypes.c_void_p(0 if t is None else t.data_ptr())
 
 
+def _require_cuda(**tensors) -> None:
+    """Every given tensor must live on the current CUDA device: the kernels launch there and take
+    raw pointers, so a host tensor or another GPU's memory is rejected here, before any launch."""
+    dev = None
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor, got one on {t.device}")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, the other tensors on {dev}")
+    if dev is not None and dev.index != torch.cuda.current_device():
+        raise ValueError(f"the tensors are on {dev} but the current CUDA device is {torch.cuda.current_device()}")
+
+
 def _dims(X: torch.Tensor, name: str) -> tuple[int, int, int, int]:
     if X.dim() != 4:
         raise ValueError(f"{name} must be [B, H, n, d], got shape {tuple(X.shape)}")
@@ -151,6 +168,7 @@ def favor_features(X: torch.Tensor, Omega: torch.Tensor, *, kind: str = "exp", r
     if out is None:
         out = torch.empty((B, H, n, m), dtype=torch.float32, device=X.device)
     ws, wsb = _workspace(workspace_bytes("features", B, H, n, d, m, X.dtype, kind=kind, stab=stab), X, workspace)
+    _require_cuda(X=X, Omega=Omega, out=out, workspace=ws)
     _check(lib.favor_features(_ptr(X), _ptr(Omega), _ptr(out), B, H, n, d, m, _DTYPES[X.dtype], _KINDS[kind],
                               relu_eps, _STABS[stab], _ptr(ws), wsb, _stream_handle(stream)), "favor_features")
     return out
@@ -175,6 +193,7 @@ def favor_attn_noncausal(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, Omeg
     """Y = Phi(Q)(Phi(K)^T V) / Phi(Q)(Phi(K)^T 1), all keys."""
     B, H, n, d, m, out = _attn_prep(Q, K, V, Omega, out)
     ws, wsb = _workspace(workspace_bytes("noncausal", B, H, n, d, m, Q.dtype, kind=kind), Q, workspace)
+    _require_cuda(Q=Q, K=K, V=V, Omega=Omega, out=out, workspace=ws)
     _check(lib.favor_attn_noncausal(_ptr(Q), _ptr(K), _ptr(V), _ptr(Omega), _ptr(out), B, H, n, d, m,
                                     _DTYPES[Q.dtype], _KINDS[kind], relu_eps, _ptr(ws), wsb, _stream_handle(stream)),
            "favor_attn_noncausal")
@@ -187,6 +206,7 @@ def favor_attn_causal(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, Omega: 
     """Causal FAVOR+ attention (keys j <= i) as a chunked prefix-sum scan."""
     B, H, n, d, m, out = _attn_prep(Q, K, V, Omega, out)
     ws, wsb = _workspace(workspace_bytes("causal", B, H, n, d, m, Q.dtype, kind=kind, chunk=chunk), Q, workspace)
+    _require_cuda(Q=Q, K=K, V=V, Omega=Omega, out=out, workspace=ws)
     _check(lib.favor_attn_causal(_ptr(Q), _ptr(K), _ptr(V), _ptr(Omega), _ptr(out), B, H, n, d, m, chunk,
                                  _DTYPES[Q.dtype], _KINDS[kind], relu_eps, _ptr(ws), wsb, _stream_handle(stream)),
            "favor_attn_causal")
@@ -204,6 +224,7 @@ def favor_attn_noncausal_noalloc(Q: torch.Tensor, K: torch.Tensor, V: torch.Tens
     outside stream capture (it looks up the array's address).
     """
     B, H, n, d, m, out = _attn_prep(Q, K, V, Omega, out)
+    _require_cuda(Q=Q, K=K, V=V, Omega=Omega, out=out)
     _check(lib.favor_attn_noncausal_noalloc(_ptr(Q), _ptr(K), _ptr(V), _ptr(Omega), _ptr(out), B, H, n, d, m,
                                             _DTYPES[Q.dtype], _KINDS[kind], relu_eps, _stream_handle(stream)),
            "favor_attn_noncausal_noalloc")
@@ -240,6 +261,7 @@ def decode_state_bytes(B: int, H: int, d: int, m: int) -> int:
 
 def favor_decode_init(state: torch.Tensor, B: int, H: int, d: int, m: int, stream=None) -> torch.Tensor:
     """Empties the decode state (no token seen) of every head."""
+    _require_cuda(state=state)
     _check(lib.favor_decode_init(_ptr(state), state.numel() * state.element_size(), B, H, d, m,
                                  _stream_handle(stream)), "favor_decode_init")
     return state
@@ -266,6 +288,7 @@ def favor_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, Omega: 
     m = int(Omega.shape[0])
     if out is None:
         out = torch.empty_like(q)
+    _require_cuda(q=q, k=k, v=v, Omega=Omega, state=state, out=out)
     _check(lib.favor_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(Omega), _ptr(out), _ptr(state),
                                  state.numel() * state.element_size(), B, H, d, m, _DTYPES[q.dtype], _KINDS[kind],
                                  relu_eps, _stream_handle(stream)), "favor_decode_step")
@@ -284,6 +307,7 @@ def favor_omega(seed: int, m: int, d: int, *, dtype=torch.bfloat16, orthogonal: 
         out = torch.empty(m, d, dtype=dtype, device=device)
     elif out.shape != (m, d) or out.dtype != dtype or not out.is_contiguous():
         raise ValueError(f"out must be a contiguous [{m}, {d}] {dtype} tensor")
+    _require_cuda(out=out)
     _check(lib.favor_omega(ctypes.c_uint64(int(seed) & (2**64 - 1)), m, d, 1 if orthogonal else 0, _DTYPES[dtype],
                            _ptr(out), _stream_handle(stream)), "favor_omega")
     return out

@@ -182,3 +182,25 @@ def test_python_binding_validates_shapes():
         favor.favor_attn_noncausal(q, q, q, torch.zeros(64, 64, dtype=torch.bfloat16))
     with pytest.raises(ValueError):
         favor.favor_attn_noncausal(q[0], q[0], q[0], torch.zeros(64, 64))
+
+
+def test_python_binding_rejects_host_tensors_before_any_launch():
+    # a host pointer handed to a kernel would be an illegal address on the GPU: the binding refuses
+    # tensors that are not on the current CUDA device (checked after the shape and dtype checks)
+    import kernelized_linear_attention_04_b300 as favor
+
+    q = torch.zeros(1, 1, 4, 64)
+    om = torch.zeros(64, 64)
+    for fn in (favor.favor_attn_noncausal, favor.favor_attn_causal, favor.favor_attn_noncausal_noalloc):
+        with pytest.raises(ValueError, match="CUDA tensor"):
+            fn(q, q, q, om)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        favor.favor_features(q, om)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        favor.favor_omega(1, 64, 64, device="cpu")
+    t = torch.zeros(1, 1, 64)
+    state = torch.zeros(favor.decode_state_bytes(1, 1, 64, 64), dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        favor.favor_decode_init(state, 1, 1, 64, 64)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        favor.favor_decode_step(t, t, t, om, state)
