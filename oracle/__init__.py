@@ -14,6 +14,10 @@ Contents
   *Normalization* equations, for tiny brute-force checks of the linear forms.
 * ``softmax_attention``: exact softmax(Q K^T / sqrt(d)) V, the operator FAVOR+ approximates
   (same page, *Standard Attention Cost*); used only for the convergence check.
+* ``omega_orf``: the random projection Omega (orthogonal random features: Gaussian blocks
+  orthonormalised in order, rows scaled to chi_d lengths), the reference for the device builder.
+* ``elu1_features`` / ``attn_linear_elu``: linear attention with the deterministic elu + 1 feature
+  map (no projection), non-causal and causal.
 
 Every function takes raw (unscaled) Q, K, X; the d^(-1/4) scaling is applied inside.
 """
@@ -189,3 +193,37 @@ def omega_orf(seed: int, m: int, d: int, *, orthogonal: bool = True) -> np.ndarr
     x = si.normal(seed, 5, m * d).reshape(m, d)
     chi = np.sqrt(np.einsum("rc,rc->r", x, x))
     return np.ascontiguousarray(E.reshape(nblk * d, d)[:m] * chi[:, None])
+
+
+def elu1_features(X) -> np.ndarray:
+    """phi(x) = elu(x) + 1 elementwise (x for x > 0 plus 1, exp(x) for x <= 0), feature dimension d.
+
+    The Linear Transformer's feature map, as the comparison table of the question page "How do linear
+    attention variants (Performer, Linformer) achieve O(n) complexity, and what's the quality cost?"
+    and "Performer for vision", *Kernel Choices*, name it: deterministic, positive, no projection.
+    Applied to the raw q and k (no d^(-1/4) scaling: the map defines its own kernel phi(q)^T phi(k)
+    and approximates nothing).
+    """
+    X = _f64(X)
+    return np.where(X > 0.0, X + 1.0, np.exp(np.minimum(X, 0.0)))
+
+
+def attn_linear_elu(Q, K, V, *, causal: bool) -> np.ndarray:
+    """Linear attention with phi = elu + 1: Y = phi(Q) (phi(K)^T V) / phi(Q) (phi(K)^T 1).
+
+    The associativity form ("Linear Attention and the Performer", *The kernelization trick*;
+    "Performer for vision", *How It Works*, Step 1): the d x d state phi(K)^T V and the d-vector
+    phi(K)^T 1 first, then one product per query. Causal: the same with the keys j <= i, by
+    cumulative sums over the tokens (Step 2, prefix sums). [..., n, d] inputs.
+    """
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    PQ, PK = elu1_features(Q), elu1_features(K)
+    if not causal:
+        S = np.swapaxes(PK, -1, -2) @ V          # [..., d, d_v]
+        z = PK.sum(axis=-2)                       # [..., d]
+        return (PQ @ S) / (PQ @ z[..., None])
+    S = np.cumsum(PK[..., :, :, None] * V[..., :, None, :], axis=-3)   # [..., n, d, d_v]
+    z = np.cumsum(PK, axis=-2)                                        # [..., n, d]
+    num = np.einsum("...ir,...irc->...ic", PQ, S)
+    den = np.einsum("...ir,...ir->...i", PQ, z)
+    return num / den[..., None]
