@@ -204,3 +204,38 @@ def test_python_binding_rejects_host_tensors_before_any_launch():
         favor.favor_decode_init(state, 1, 1, 64, 64)
     with pytest.raises(ValueError, match="CUDA tensor"):
         favor.favor_decode_step(t, t, t, om, state)
+
+
+def test_plain_c_program_links_and_calls_the_library(tmp_path):
+    # the boundary is a C ABI: a C99 program (no Python, no torch) includes the header, links the
+    # library and calls its host-side entry points; its answers match the binding's
+    import shutil
+
+    import kernelized_linear_attention_04_b300 as favor
+
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_favor.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include "favor.h"
+int main(void) {
+    size_t ws = favor_workspace_bytes(FAVOR_OP_NONCAUSAL, 1, 8, 4096, 64, 256, FAVOR_BF16, FAVOR_EXP,
+                                      FAVOR_STAB_ROW, 0);
+    size_t st = favor_decode_state_bytes(2, 3, 64, 256);
+    /* argument errors come back as status codes, nothing is launched */
+    favor_status_t bad = favor_attn_causal(0, 0, 0, 0, 0, 1, 1, 16, 96, 64, 64, FAVOR_BF16, FAVOR_EXP, 0.f, 0, 0, 0);
+    printf("%d %zu %zu %d %s\n", favor_abi_version(), ws, st, (int)bad, favor_status_string(bad));
+    return 0;
+}
+''')
+    exe = tmp_path / "use_favor"
+    libdir = os.path.dirname(favor.LIB_PATH)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-o", str(exe), "-L", libdir, "-lfavor", f"-Wl,-rpath,{libdir}"], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
+    bf = torch.bfloat16
+    assert int(out[0]) == favor.abi_version()
+    assert int(out[1]) == favor.workspace_bytes("noncausal", 1, 8, 4096, 64, 256, bf)
+    assert int(out[2]) == favor.decode_state_bytes(2, 3, 64, 256)
+    assert int(out[3]) == 2 and out[4].startswith("FAVOR_ERR_UNSUPPORTED")
