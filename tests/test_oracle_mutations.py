@@ -117,3 +117,119 @@ def test_planted_mistake_is_caught(tmp_path, name):
     with oracle_library(build_variant(tmp_path, name, MUTATIONS[name])):
         failed = pin_failures()
     assert failed, f"planted mistake {name} passed every pin check"
+
+
+# ---------------------------------------------------------------------------------------------
+# The Python parts of the oracle (Omega builder, elu + 1 attention): their source with one planted
+# mistake, executed in a scratch namespace, fails the facts their pins check.
+# ---------------------------------------------------------------------------------------------
+
+def mutated(fn_name, old, new):
+    import inspect
+
+    src = inspect.getsource(getattr(oracle, fn_name))
+    if old is not None:
+        assert src.count(old) == 1, f"mutation site in {fn_name} not found exactly once"
+        src = src.replace(old, new)
+    ns = dict(vars(oracle))
+    exec(compile(src, f"<mutated {fn_name}>", "exec"), ns)
+    return ns[fn_name], ns
+
+
+def omega_failures(omega_fn) -> list[str]:
+    with np.errstate(all="ignore"):  # a mutated builder may overflow; the checks still decide
+        return _omega_failures(omega_fn)
+
+
+def _omega_failures(omega_fn) -> list[str]:
+    failures = []
+    seed, m, d = 11, 130, 64
+    om = omega_fn(seed, m, d)
+    nblk = -(-m // d)
+    G = si.normal(seed, 4, nblk * d * d).reshape(nblk, d, d)
+    E = om / np.linalg.norm(om, axis=1, keepdims=True)
+    for b in range(nblk):
+        Qr, Rr = np.linalg.qr(G[b].T)
+        rows = min(d, m - b * d)
+        if np.abs(E[b * d:b * d + rows] - ((Qr * np.sign(np.diag(Rr))[None, :]).T)[:rows]).max() > 1e-10:
+            failures.append("qr")
+            break
+    chi = np.linalg.norm(si.normal(seed, 5, m * d).reshape(m, d), axis=1)
+    if not np.allclose(np.linalg.norm(om, axis=1), chi, rtol=1e-12):
+        failures.append("chi")
+    return failures
+
+
+OMEGA_MUTATIONS = {
+    "classical_step_uses_raw_row": ("v = v - np.dot(v, E[b, j]) * E[b, j]", "v = v - np.dot(G[b, r], E[b, j]) * E[b, j] * 0.999"),
+    "no_normalisation": ("E[b, r] = v / np.sqrt(np.dot(v, v))", "E[b, r] = v"),
+    "chi_from_wrong_stream": ("x = si.normal(seed, 5, m * d)", "x = si.normal(seed, 4, m * d)"),
+    "columns_instead_of_rows": ("v = G[b, r].copy()", "v = G[b, :, r].copy()"),
+}
+
+
+def test_unmodified_omega_source_passes():
+    fn, _ = mutated("omega_orf", None, None)
+    assert omega_failures(fn) == []
+
+
+@pytest.mark.parametrize("name", sorted(OMEGA_MUTATIONS))
+def test_planted_omega_mistake_is_caught(name):
+    fn, _ = mutated("omega_orf", *OMEGA_MUTATIONS[name])
+    with np.errstate(all="ignore"):
+        assert omega_failures(fn), f"planted mistake {name} passed the Omega pins"
+
+
+def elu_failures(features_fn, attn_fn) -> list[str]:
+    try:
+        with np.errstate(all="ignore"):
+            return _elu_failures(features_fn, attn_fn)
+    except (ValueError, FloatingPointError) as e:  # a mistake that breaks the shapes fails the pins too
+        return [f"error: {e}"]
+
+
+def _elu_failures(features_fn, attn_fn) -> list[str]:
+    import torch
+
+    failures = []
+    x = np.linspace(-6, 6, 241)
+    ref = torch.nn.functional.elu(torch.from_numpy(x)).numpy() + 1.0
+    if not np.allclose(features_fn(x), ref, rtol=1e-15, atol=2.0**-53):
+        failures.append("library_elu")
+    e = math.exp(-1.0)
+    y = attn_fn(np.array([[0.5]]), np.array([[1.0], [-1.0]]), np.array([[2.0], [4.0]]), causal=False)
+    if abs(y[0, 0] - (4.0 + 4.0 * e) / (2.0 + e)) > 1e-15:
+        failures.append("hand_example")
+    yc = attn_fn(np.array([[0.5], [-2.0]]), np.array([[1.0], [-1.0]]), np.array([[2.0], [4.0]]), causal=True)
+    if not (abs(yc[0, 0] - 2.0) < 1e-15):
+        failures.append("first_token")
+    return failures
+
+
+ELU_MUTATIONS = {
+    "without_plus_one": ("elu1_features", "X + 1.0, np.exp(np.minimum(X, 0.0))", "X, np.exp(np.minimum(X, 0.0)) - 1.0"),
+    "relu_plus_one": ("elu1_features", "np.exp(np.minimum(X, 0.0))", "np.ones_like(X)"),
+    "exclusive_prefix": ("attn_linear_elu", "S = np.cumsum(PK[..., :, :, None] * V[..., :, None, :], axis=-3)",
+                         "S = np.cumsum(PK[..., :, :, None] * V[..., :, None, :], axis=-3) - PK[..., :, :, None] * V[..., :, None, :]"),
+    "keys_as_queries": ("attn_linear_elu", "S = np.swapaxes(PK, -1, -2) @ V", "S = np.swapaxes(PQ, -1, -2) @ V"),
+}
+
+
+def test_unmodified_elu_source_passes():
+    feat, _ = mutated("elu1_features", None, None)
+    attn, _ = mutated("attn_linear_elu", None, None)
+    assert elu_failures(feat, attn) == []
+
+
+@pytest.mark.parametrize("name", sorted(ELU_MUTATIONS))
+def test_planted_elu_mistake_is_caught(name):
+    target, old, new = ELU_MUTATIONS[name]
+    if target == "elu1_features":
+        feat, _ = mutated("elu1_features", old, new)
+        _, ns2 = mutated("attn_linear_elu", None, None)
+        ns2["elu1_features"] = feat          # the attention uses the mutated feature map
+        attn = ns2["attn_linear_elu"]
+    else:
+        feat = oracle.elu1_features
+        attn, _ = mutated("attn_linear_elu", old, new)
+    assert elu_failures(feat, attn), f"planted mistake {name} passed the elu pins"
