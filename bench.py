@@ -5,8 +5,9 @@
 
 A step is one full FAVOR+ attention call (every kernel of the path: features, state, readout for
 the non-causal form; the chunked scan for the causal form) over one batch of seeded synthetic input
-already resident in HBM. The default workload is the (B, H, n, d) = (1, 8, 1024, 64) shape of the
-linear-attention lesson's exercise with m = 256 random features, bf16 in / fp32 accumulate.
+already resident in HBM. The default workload is the largest one that fits a single GPU: causal
+generalized-ReLU features, (B, H, n, d) = (8, 32, 32768, 64) with m = 512, bf16 in / fp32
+accumulate. The other workloads are selected with --workload.
 
 Timing: W untimed warm-up steps; K timed steps bracketed by a barrier and device synchronisation;
 each step timed by CUDA events on the launching stream; L2 flushed (a 512 MB write) before every
@@ -36,7 +37,7 @@ sys.path.insert(0, ROOT)
 import seeded_inputs as si  # noqa: E402
 
 METRIC = "FAVOR+ attention tokens/s (B*H*n per s) and % of HBM/tensor roofline"
-DEFAULT_WORKLOAD = "noncausal_bf16_B1H8n1024d64m256"
+DEFAULT_WORKLOAD = "causal_relu_bf16_B8H32n32768d64m512"
 L2_BYTES = 126 * 1024 * 1024
 FLUSH_BYTES = 512 * 1024 * 1024
 # A device-side wait (about 2.5 ms at 2 GHz) enqueued before a timed loop, so that the host queues
@@ -72,7 +73,8 @@ KERNEL_SOURCES = {
     "fused": ["tc.cuh", "tc_noncausal.cuh", "tc_fused.cuh"],
     "state": ["tc.cuh", "tc_noncausal.cuh"], "combine": ["tc.cuh", "tc_noncausal.cuh"],
     "readout": ["tc.cuh", "tc_noncausal.cuh"],
-    "causal": ["tc.cuh", "tc_noncausal.cuh", "tc_causal.cuh", "tc_causal_wide.cuh"],
+    "causal": ["tc.cuh", "tc_noncausal.cuh", "tc_scan.cuh"],
+    "exact": ["tc.cuh", "tc_noncausal.cuh", "tc_exact.cuh"],
 }
 
 
@@ -224,26 +226,32 @@ def max_over_ranks(x: float, device) -> float:
 # CPU oracle timing (the cpu_baseline object, and the whole --impl reference arm)
 # ------------------------------------------------------------------------------------------------
 
-def oracle_sample_heads(w, budget_s: float) -> list[tuple[int, int]]:
-    """Heads for one oracle timing sample: as many as fit `budget_s` at a rough 1 GFLOP/s/core."""
+def oracle_sample(w, budget_s: float) -> tuple[list[tuple[int, int]], int]:
+    """A bounded sample of workload w for one oracle timing step: up to one head per host thread
+    (the oracle runs its heads in parallel) and the first n' tokens of each, n' sized from a short
+    calibration run so that one step takes about `budget_s`. A causal prefix is exactly the first
+    n' rows of the full result; a non-causal prefix is the same computation over n' tokens."""
     import oracle
 
     cores = oracle.get_threads()
-    per_head_flops = 10.0 * w.m * w.d * w.n  # includes the key pre-pass for the head stabiliser
-    k = int(max(1, min(w.heads, budget_s * cores * 1e9 / per_head_flops)))
-    k = max(1, (k // cores) * cores) if k >= cores else k
-    return [(i // w.H, i % w.H) for i in range(min(k, w.heads))]
+    heads = [(i // w.H, i % w.H) for i in range(min(w.heads, cores))]
+    n_cal = min(w.n, 128)
+    inputs = oracle_inputs(w, heads, n_cal)
+    oracle_step(w, inputs)  # first touch
+    t0 = time.perf_counter()
+    oracle_step(w, inputs)
+    per_token = max(time.perf_counter() - t0, 1e-6) / n_cal
+    n_pre = int(max(1, min(w.n, budget_s / per_token)))
+    return heads, n_pre
 
 
-def oracle_inputs(w, heads):
-    import oracle  # noqa: F401
-
+def oracle_inputs(w, heads, n_pre: int):
     Q, K, V = [], [], []
     for b, h in heads:
         hi = si.head_inputs(w, b, h)
-        Q.append(si.to_f64(hi["Q"]))
-        K.append(si.to_f64(hi["K"]))
-        V.append(si.to_f64(hi["V"]))
+        Q.append(si.to_f64(hi["Q"][:n_pre]))
+        K.append(si.to_f64(hi["K"][:n_pre]))
+        V.append(si.to_f64(hi["V"][:n_pre]))
     return np.stack(Q), np.stack(K), np.stack(V), si.omega_for(w)[1]
 
 
@@ -255,11 +263,16 @@ def oracle_step(w, inputs):
     return fn(Q, K, V, om, kind=w.kind, relu_eps=w.relu_eps)
 
 
+def sample_note(w, heads, n_pre: int) -> str:
+    return (f"{len(heads)} of {w.heads} heads x the first {n_pre} of {w.n} tokens each, fp64 C loops, "
+            f"OpenMP over heads")
+
+
 def cpu_baseline(w, target_s: float = 12.0) -> dict:
     import oracle
 
-    heads = oracle_sample_heads(w, budget_s=min(4.0, target_s / 3))
-    inputs = oracle_inputs(w, heads)
+    heads, n_pre = oracle_sample(w, budget_s=min(4.0, target_s / 3))
+    inputs = oracle_inputs(w, heads, n_pre)
     oracle_step(w, inputs)  # load / first-touch
     t0 = time.perf_counter()
     reps = 0
@@ -269,10 +282,9 @@ def cpu_baseline(w, target_s: float = 12.0) -> dict:
         el = time.perf_counter() - t0
         if el >= target_s or reps >= 1000:
             break
-    tokens = reps * len(heads) * w.n
+    tokens = reps * len(heads) * n_pre
     return {"value": tokens / el, "unit": "tokens/s", "cores": oracle.get_threads(), "kind": "oracle",
-            "sample": f"{len(heads)} of {w.heads} heads (all {w.n} tokens each) x {reps} repetitions, "
-                      f"{el:.1f} s wall, fp64 C loops, OpenMP over heads"}
+            "sample": f"{sample_note(w, heads, n_pre)}; {reps} repetitions, {el:.1f} s wall"}
 
 
 def run_reference(args, w):
@@ -281,8 +293,9 @@ def run_reference(args, w):
         return 0
     import oracle
 
-    heads = oracle_sample_heads(w, budget_s=0.5)
-    inputs = oracle_inputs(w, heads)
+    # the whole run (warm-up and timed steps) within about two minutes of host time
+    heads, n_pre = oracle_sample(w, budget_s=min(0.5, 120.0 / (args.steps + args.warmup)))
+    inputs = oracle_inputs(w, heads, n_pre)
     for _ in range(args.warmup):
         oracle_step(w, inputs)
     times = []
@@ -290,28 +303,35 @@ def run_reference(args, w):
         t0 = time.perf_counter()
         oracle_step(w, inputs)
         times.append(time.perf_counter() - t0)
-    tok = len(heads) * w.n
+    tok = len(heads) * n_pre
     value = tok * len(times) / sum(times)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(w),
+        "timing": "host wall clock (time.perf_counter) around each step, fp64 C loops on the host cores",
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.get_threads(), "kind": "oracle",
-                         "sample": f"{len(heads)} of {w.heads} heads (all {w.n} tokens each) per step"},
+                         "sample": f"{sample_note(w, heads, n_pre)}, per step"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
     return 0
 
 
-def workload_config(w, l2_note: str | None = None) -> dict:
+def l2_policy(w) -> tuple[bool, str]:
+    """Whether the timed steps flush L2 first (inputs smaller than twice L2), and how to say so."""
+    flush = path_work(w)[1] < 2 * L2_BYTES
+    return flush, ("flushed before every timed step (512 MB write)" if flush else "inputs larger than L2")
+
+
+def workload_config(w) -> dict:
+    """The `config` object of a bench line; both arms print exactly this for the same workload."""
     c = {"workload": w.name, "form": "causal" if w.causal else "non-causal", "features": w.kind,
          "B": w.B, "H": w.H, "n": w.n, "d": w.d, "m": w.m, "inputs": f"iid N(0, {w.sigma}^2)"}
     if w.causal:
         c["chunk"] = w.chunk
-    if l2_note:
-        c["l2"] = l2_note
+    c["l2"] = l2_policy(w)[1]
     return c
 
 
@@ -356,10 +376,8 @@ def run_ours(args, w):
             favor.favor_attn_noncausal(Q, K, V, Om, kind=w.kind, relu_eps=w.relu_eps, out=Y, workspace=wsp,
                                        stream=st)
 
-    step_bytes = path_work(w)[1]
-    flush = step_bytes < 2 * L2_BYTES
+    flush, _ = l2_policy(w)
     fbuf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
-    l2_note = "flushed before every timed step (512 MB write)" if flush else "inputs larger than L2"
 
     def timed_loop(n_steps, body):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_steps)]
@@ -476,7 +494,7 @@ def run_ours(args, w):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
-            "config": {**workload_config(w, l2_note), "timing": timing},
+            "config": workload_config(w), "timing": timing,
             "path_roofline_frac": (t_roof * 1e3) / ms_per_step,
             "roofline": roofline,
             "e2e": {"value": world * w.tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,

@@ -59,7 +59,16 @@ typedef enum {
 } favor_status_t;
 
 typedef enum { FAVOR_F32 = 0, FAVOR_BF16 = 1 } favor_dtype_t;
-typedef enum { FAVOR_EXP = 0, FAVOR_RELU = 1 } favor_kind_t;
+/* Feature family:
+ *   FAVOR_EXP   positive random features exp(w_r^T x^ - |x^|^2/2 - stab) ("Performer" paper note, *FAVOR+*);
+ *   FAVOR_RELU  generalized ReLU max(0, w_r^T x^) + relu_eps ("Performer for vision", Key Feature 4);
+ *   FAVOR_ELU   elu(x) + 1 on the raw q and k: x_r + 1 for x_r > 0, exp(x_r) otherwise, feature
+ *               dimension d, no projection, no d^(-1/4) scaling (the Linear Transformer's map in the
+ *               comparison table of the question page "How do linear attention variants (Performer,
+ *               Linformer) achieve O(n) complexity, and what's the quality cost?"; "Performer for
+ *               vision", *Kernel Choices*). Calls with this family take m == d and ignore Omega, which
+ *               may be NULL; relu_eps is not used. */
+typedef enum { FAVOR_EXP = 0, FAVOR_RELU = 1, FAVOR_ELU = 2 } favor_kind_t;
 
 /* Stabiliser of favor_features (exp family only; ignored for ReLU):
  *   NONE: stab = 0;  ROW: per token, stab = max_r u_r(x);  HEAD: per (b, h), stab = max over the
@@ -187,6 +196,18 @@ favor_status_t favor_decode_step(const void* q, const void* k, const void* v, co
  */
 favor_status_t favor_omega(uint64_t seed, int m, int d, int orthogonal, favor_dtype_t dt, void* Omega, void* stream);
 
+/*
+ * Exact softmax attention, the operator FAVOR+ approximates ("Performer" paper note, *Standard
+ * Attention Cost*: softmax(Q K^T / sqrt(d)) V, quadratic in n), for the speed and divergence
+ * comparison the pages ask for ("Linear Attention and the Performer", *Exercise*). Not part of the
+ * FAVOR+ path: no n x n matrix is stored (an online softmax over 128-key tiles), but the work is
+ * O(n^2 d).
+ *   Q, K, V, Y [B, H, n, d]; causal != 0 restricts row i to keys j <= i. bf16 with d = 64 only
+ *   (other inputs: FAVOR_ERR_UNSUPPORTED); B*H <= 65535. No workspace. Asynchronous on `stream`.
+ */
+favor_status_t favor_softmax_attn(const void* Q, const void* K, const void* V, void* Y, int B, int H, int n, int d,
+                                  int causal, favor_dtype_t dt, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* favor_status_string(favor_status_t status);
 
@@ -196,6 +217,15 @@ favor_status_t favor_last_device_error(void* stream);
 
 /* FAVOR_ABI_VERSION of the loaded library. */
 int favor_abi_version(void);
+
+/* Test hook for the failure path (no counterpart on the pages). With ns > 0, every bounded device
+ * wait of the calls that follow on the current device gives up after ns nanoseconds instead of its
+ * normal limit, and the causal tensor-core scan withholds the first arrival its MMA issuer waits
+ * for: that wait runs out, the kernel records FAVOR_ERR_TIMEOUT in the device error word, the
+ * CTA's other roles stop, its copies in flight are drained and its tensor memory is released; the
+ * output of that call is undefined. ns = 0 (the initial state) turns the hook off. Synchronises
+ * `stream` after setting the word. Never needed in normal use. */
+favor_status_t favor_test_set_wait_limit(unsigned long long ns, void* stream);
 
 /* ---- tracing: per-kernel device time, recorded with CUDA events around every launch ---------- */
 
@@ -210,7 +240,8 @@ typedef enum {
     FAVOR_KERNEL_DECODE = 7,        /* streaming decode step (favor_decode_step)              */
     FAVOR_KERNEL_DECODE_INIT = 8,   /* decode state reset (favor_decode_init)                 */
     FAVOR_KERNEL_OMEGA = 9,         /* random projection builder (favor_omega)                */
-    FAVOR_KERNEL_COUNT = 10
+    FAVOR_KERNEL_EXACT = 10,        /* exact softmax attention (favor_softmax_attn)           */
+    FAVOR_KERNEL_COUNT = 11
 } favor_kernel_id_t;
 
 /* Starts (on != 0) or stops recording. Starting clears previous records. While recording, every

@@ -22,6 +22,7 @@ from . import build as _build
 
 __all__ = [
     "FavorError", "favor_features", "favor_attn_noncausal", "favor_attn_causal", "favor_attn_noncausal_noalloc",
+    "favor_softmax_attn",
     "workspace_bytes", "NOALLOC_SCRATCH_BYTES",
     "decode_state_bytes", "decode_state", "favor_decode_init", "favor_decode_step", "favor_omega",
     "last_device_error", "trace_enable", "trace_read", "abi_version", "lib", "LIB_PATH",
@@ -31,12 +32,12 @@ __all__ = [
 LIB_PATH = _build.LIB
 
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
-_KINDS = {"exp": 0, "relu": 1}
+_KINDS = {"exp": 0, "relu": 1, "elu": 2}
 _STABS = {"none": 0, "row": 1, "head": 2}
 _OPS = {"features": 0, "noncausal": 1, "causal": 2}
 _STATUS = {0: "FAVOR_OK", 1: "FAVOR_ERR_INVALID_ARG", 2: "FAVOR_ERR_UNSUPPORTED", 3: "FAVOR_ERR_MISALIGNED",
            4: "FAVOR_ERR_WORKSPACE", 5: "FAVOR_ERR_CUDA", 6: "FAVOR_ERR_TIMEOUT"}
-KERNEL_COUNT = 10
+KERNEL_COUNT = 11
 # Size of the library's fixed scratch array used by favor_attn_noncausal_noalloc.
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -46,6 +47,7 @@ EXPORTED_SYMBOLS = (
     "favor_status_string", "favor_last_device_error", "favor_abi_version", "favor_trace_enable",
     "favor_trace_read", "favor_kernel_name", "favor_attn_noncausal_noalloc",
     "favor_decode_state_bytes", "favor_decode_init", "favor_decode_step", "favor_omega",
+    "favor_test_set_wait_limit", "favor_softmax_attn",
 )
 
 
@@ -89,6 +91,10 @@ def _load() -> ctypes.CDLL:
     L.favor_decode_step.restype = i32
     L.favor_omega.argtypes = [ctypes.c_uint64, i32, i32, i32, i32, vp, vp]
     L.favor_omega.restype = i32
+    L.favor_softmax_attn.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
+    L.favor_softmax_attn.restype = i32
+    L.favor_test_set_wait_limit.argtypes = [ctypes.c_ulonglong, vp]
+    L.favor_test_set_wait_limit.restype = i32
     return L
 
 
@@ -159,12 +165,15 @@ def _workspace(nbytes: int, like: torch.Tensor, workspace):
     return workspace, workspace.numel() * workspace.element_size()
 
 
-def favor_features(X: torch.Tensor, Omega: torch.Tensor, *, kind: str = "exp", relu_eps: float = 1e-3,
+def favor_features(X: torch.Tensor, Omega: torch.Tensor | None, *, kind: str = "exp", relu_eps: float = 1e-3,
                    stab: str = "row", out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
                    stream=None) -> torch.Tensor:
-    """phi(X) as fp32 [B, H, n, m] for raw X [B, H, n, d] and Omega [m, d] (same dtype)."""
+    """phi(X) as fp32 [B, H, n, m] for raw X [B, H, n, d] and Omega [m, d] (same dtype). kind="elu":
+    phi = elu(X) + 1 with m = d; Omega is not used (pass None)."""
     B, H, n, d = _dims(X, "X")
-    m = int(Omega.shape[0])
+    m = d if kind == "elu" else int(Omega.shape[0])
+    if kind == "elu":
+        Omega = None
     if out is None:
         out = torch.empty((B, H, n, m), dtype=torch.float32, device=X.device)
     ws, wsb = _workspace(workspace_bytes("features", B, H, n, d, m, X.dtype, kind=kind, stab=stab), X, workspace)
@@ -174,24 +183,29 @@ def favor_features(X: torch.Tensor, Omega: torch.Tensor, *, kind: str = "exp", r
     return out
 
 
-def _attn_prep(Q, K, V, Omega, out):
+def _attn_prep(Q, K, V, Omega, out, kind="exp"):
     B, H, n, d = _dims(Q, "Q")
     if K.shape != Q.shape or V.shape != Q.shape:
         raise ValueError("Q, K, V must have the same shape")
+    if out is None:
+        out = torch.empty_like(Q)
+    if kind == "elu":  # elu + 1 features: feature dimension d, no projection (Omega is not used)
+        if not (Q.dtype == K.dtype == V.dtype):
+            raise TypeError("Q, K and V must share one dtype")
+        return B, H, n, d, d, out
     if not (Q.dtype == K.dtype == V.dtype == Omega.dtype):
         raise TypeError("Q, K, V and Omega must share one dtype")
     if Omega.dim() != 2 or Omega.shape[1] != d or not Omega.is_contiguous():
         raise ValueError("Omega must be a contiguous [m, d] tensor")
-    if out is None:
-        out = torch.empty_like(Q)
     return B, H, n, d, int(Omega.shape[0]), out
 
 
-def favor_attn_noncausal(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, Omega: torch.Tensor, *,
+def favor_attn_noncausal(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, Omega: torch.Tensor | None, *,
                          kind: str = "exp", relu_eps: float = 1e-3, out: torch.Tensor | None = None,
                          workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Y = Phi(Q)(Phi(K)^T V) / Phi(Q)(Phi(K)^T 1), all keys."""
-    B, H, n, d, m, out = _attn_prep(Q, K, V, Omega, out)
+    B, H, n, d, m, out = _attn_prep(Q, K, V, Omega, out, kind)
+    Omega = None if kind == "elu" else Omega
     ws, wsb = _workspace(workspace_bytes("noncausal", B, H, n, d, m, Q.dtype, kind=kind), Q, workspace)
     _require_cuda(Q=Q, K=K, V=V, Omega=Omega, out=out, workspace=ws)
     _check(lib.favor_attn_noncausal(_ptr(Q), _ptr(K), _ptr(V), _ptr(Omega), _ptr(out), B, H, n, d, m,
@@ -200,11 +214,12 @@ def favor_attn_noncausal(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, Omeg
     return out
 
 
-def favor_attn_causal(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, Omega: torch.Tensor, *, chunk: int = 64,
+def favor_attn_causal(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, Omega: torch.Tensor | None, *, chunk: int = 64,
                       kind: str = "exp", relu_eps: float = 1e-3, out: torch.Tensor | None = None,
                       workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Causal FAVOR+ attention (keys j <= i) as a chunked prefix-sum scan."""
-    B, H, n, d, m, out = _attn_prep(Q, K, V, Omega, out)
+    B, H, n, d, m, out = _attn_prep(Q, K, V, Omega, out, kind)
+    Omega = None if kind == "elu" else Omega
     ws, wsb = _workspace(workspace_bytes("causal", B, H, n, d, m, Q.dtype, kind=kind, chunk=chunk), Q, workspace)
     _require_cuda(Q=Q, K=K, V=V, Omega=Omega, out=out, workspace=ws)
     _check(lib.favor_attn_causal(_ptr(Q), _ptr(K), _ptr(V), _ptr(Omega), _ptr(out), B, H, n, d, m, chunk,
@@ -213,7 +228,22 @@ def favor_attn_causal(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, Omega: 
     return out
 
 
-def favor_attn_noncausal_noalloc(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, Omega: torch.Tensor, *,
+def favor_softmax_attn(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, causal: bool = False,
+                       out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Exact softmax(Q K^T / sqrt(d)) V (the operator FAVOR+ approximates), O(n^2 d) work; bf16,
+    d = 64. For speed and divergence comparisons."""
+    B, H, n, d = _dims(Q, "Q")
+    if K.shape != Q.shape or V.shape != Q.shape or not (Q.dtype == K.dtype == V.dtype):
+        raise ValueError("Q, K, V must have the same shape and dtype")
+    if out is None:
+        out = torch.empty_like(Q)
+    _require_cuda(Q=Q, K=K, V=V, out=out)
+    _check(lib.favor_softmax_attn(_ptr(Q), _ptr(K), _ptr(V), _ptr(out), B, H, n, d, 1 if causal else 0,
+                                  _DTYPES[Q.dtype], _stream_handle(stream)), "favor_softmax_attn")
+    return out
+
+
+def favor_attn_noncausal_noalloc(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, Omega: torch.Tensor | None, *,
                                  kind: str = "exp", relu_eps: float = 1e-3, out: torch.Tensor | None = None,
                                  stream=None) -> torch.Tensor:
     """Same result as favor_attn_noncausal, for callers that cannot allocate device scratch.
@@ -223,7 +253,8 @@ def favor_attn_noncausal_noalloc(Q: torch.Tensor, K: torch.Tensor, V: torch.Tens
     share that array: do not let two of them overlap on the GPU. Make the first call on a device
     outside stream capture (it looks up the array's address).
     """
-    B, H, n, d, m, out = _attn_prep(Q, K, V, Omega, out)
+    B, H, n, d, m, out = _attn_prep(Q, K, V, Omega, out, kind)
+    Omega = None if kind == "elu" else Omega
     _require_cuda(Q=Q, K=K, V=V, Omega=Omega, out=out)
     _check(lib.favor_attn_noncausal_noalloc(_ptr(Q), _ptr(K), _ptr(V), _ptr(Omega), _ptr(out), B, H, n, d, m,
                                             _DTYPES[Q.dtype], _KINDS[kind], relu_eps, _stream_handle(stream)),
@@ -273,19 +304,23 @@ def decode_state(B: int, H: int, d: int, m: int, device="cuda", stream=None) -> 
     return favor_decode_init(state, B, H, d, m, stream)
 
 
-def favor_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, Omega: torch.Tensor, state: torch.Tensor,
-                      *, kind: str = "exp", relu_eps: float = 1e-3, out: torch.Tensor | None = None,
-                      stream=None) -> torch.Tensor:
-    """Appends one token per head (q, k, v: [B, H, d]) to `state` and returns its output y [B, H, d]."""
+def favor_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, Omega: torch.Tensor | None,
+                      state: torch.Tensor, *, kind: str = "exp", relu_eps: float = 1e-3,
+                      out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Appends one token per head (q, k, v: [B, H, d]) to `state` and returns its output y [B, H, d].
+    kind="elu": m = d and Omega is not used (pass None)."""
     for t, name in ((q, "q"), (k, "k"), (v, "v")):
         if t.dim() != 3 or not t.is_contiguous() or t.dtype not in _DTYPES:
             raise ValueError(f"{name} must be a contiguous [B, H, d] float32/bfloat16 tensor")
         if t.shape != q.shape or t.dtype != q.dtype:
             raise ValueError("q, k and v must have the same shape and dtype")
     B, H, d = (int(x) for x in q.shape)
-    if Omega.dim() != 2 or Omega.shape[1] != d or Omega.dtype != q.dtype or not Omega.is_contiguous():
-        raise ValueError("Omega must be a contiguous [m, d] tensor of the same dtype as q")
-    m = int(Omega.shape[0])
+    if kind == "elu":
+        Omega, m = None, d
+    else:
+        if Omega.dim() != 2 or Omega.shape[1] != d or Omega.dtype != q.dtype or not Omega.is_contiguous():
+            raise ValueError("Omega must be a contiguous [m, d] tensor of the same dtype as q")
+        m = int(Omega.shape[0])
     if out is None:
         out = torch.empty_like(q)
     _require_cuda(q=q, k=k, v=v, Omega=Omega, state=state, out=out)

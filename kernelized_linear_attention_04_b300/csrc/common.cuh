@@ -9,6 +9,7 @@ namespace favor {
 
 constexpr int kKindExp = 0;
 constexpr int kKindRelu = 1;
+constexpr int kKindElu = 2;
 constexpr int kStabNone = 0;
 constexpr int kStabRow = 1;
 constexpr int kStabHead = 2;
@@ -18,6 +19,13 @@ constexpr float kLog2e = 1.4426950408889634f;
 // Device error word: set (never trapped on) by a kernel whose bounded wait gave up.
 constexpr unsigned kDevErrTimeout = 1u;
 __device__ unsigned int g_favor_error;
+
+// Test hook, 0 (off) unless a caller arms it through favor_test_set_wait_limit: while it holds a
+// nonzero value, every bounded wait gives up after that many nanoseconds instead of its normal limit,
+// and the causal tensor-core scan withholds the first arrival its MMA issuer waits for, so that the
+// timeout path (error word, abort of the other roles, TMA drain, TMEM release) runs on demand
+// without any fault or hang.
+__device__ unsigned long long g_favor_test_wait_ns;
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -43,6 +51,16 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
+}
+
+// Feature of a family without a stabiliser, from the projection a: generalized ReLU
+// max(0, a) * g + eps (a = w_r . x^); elu + 1 (whose projection is the identity and whose input is
+// the raw x, so a = x_r): a + 1 for a > 0, exp(a) otherwise (g and eps unused).
+__device__ __forceinline__ float phi_plain(float a, int kind, float g, float eps) {
+    if (kind != kKindElu) return fmaxf(a, 0.f) * g + eps;
+    float e;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(fminf(a, 0.f) * kLog2e));
+    return a > 0.f ? a + 1.f : e;
 }
 
 // exp(u - stab) for the exp family, evaluated as 2^((u - stab) * log2 e).

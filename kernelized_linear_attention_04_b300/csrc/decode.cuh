@@ -184,8 +184,8 @@ __global__ void __launch_bounds__(kThreads)
             pq[r] = exp_shift(pq[r], qmax);
             pk[r] = exp_shift(pk[r] - hk, new_stab);
         } else {
-            pq[r] = fmaxf(pq[r], 0.f) + relu_eps_s;
-            pk[r] = fmaxf(pk[r], 0.f) + relu_eps_s;
+            pq[r] = phi_plain(pq[r], kind, 1.f, relu_eps_s);
+            pk[r] = phi_plain(pk[r], kind, 1.f, relu_eps_s);
         }
     }
     __syncthreads();

@@ -13,8 +13,8 @@
 #include "common.cuh"
 #include "simt_kernels.cuh"
 #include "tc_noncausal.cuh"
-#include "tc_causal.cuh"
-#include "tc_causal_wide.cuh"
+#include "tc_scan.cuh"
+#include "tc_exact.cuh"
 #include "tc_features.cuh"
 #include "tc_fused.cuh"
 #include "decode.cuh"
@@ -94,9 +94,10 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 favor_status_t check_shape(int B, int H, int n, int d, int m, favor_dtype_t dt, favor_kind_t kind) {
     if (B < 0 || H < 0 || n < 0) return FAVOR_ERR_INVALID_ARG;
     if (dt != FAVOR_F32 && dt != FAVOR_BF16) return FAVOR_ERR_INVALID_ARG;
-    if (kind != FAVOR_EXP && kind != FAVOR_RELU) return FAVOR_ERR_INVALID_ARG;
+    if (kind != FAVOR_EXP && kind != FAVOR_RELU && kind != FAVOR_ELU) return FAVOR_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return FAVOR_ERR_UNSUPPORTED;
     if (m < 64 || m > 512 || m % 64 != 0) return FAVOR_ERR_UNSUPPORTED;
+    if (kind == FAVOR_ELU && m != d) return FAVOR_ERR_UNSUPPORTED;  // elu + 1: feature dimension d
     return FAVOR_OK;
 }
 
@@ -191,19 +192,9 @@ size_t noncausal_ws_bytes(int B, int H, int n, int d, int m, favor_dtype_t dt) {
     return tc_noncausal_ok(d, m, dt) ? tc_noncausal_ws(B, H, n, d, m).total : noncausal_ws(B, H, n, d, m).total;
 }
 
-// The tensor-core causal scan takes bf16 with d = 64. Heads of up to 256 features run the pipelined
-// scan (one 128-feature group per CTA, a cluster of 1 or 2 CTAs per head); wider heads (up to 512)
-// run the one-tile-at-a-time scan with up to two groups per CTA.
+// The tensor-core causal scan takes bf16 with d = 64 and m <= 512: one 128-feature group per CTA, a
+// cluster of ceil(m / 128) CTAs per head.
 bool tc_causal_ok(int d, int m, favor_dtype_t dt) { return dt == FAVOR_BF16 && d == 64 && m_padded(m) <= 512; }
-
-// Cluster size of the wide-head scan: with fewer heads than SMs, one group per CTA (three groups take
-// a cluster of four, the last CTA holding only padding features); otherwise two groups per CTA.
-int causal_wide_cluster(int BH, int m) {
-    const int groups = m_padded(m) / 128;
-    int cs = groups == 3 ? 4 : groups;
-    if (BH >= kNumSMs) cs = groups <= 2 ? 1 : 2;
-    return cs;
-}
 
 size_t causal_ws_bytes(int B, int H, int d, int m) {
     const size_t BH = (size_t)B * H;
@@ -216,6 +207,9 @@ size_t features_ws_bytes(int B, int H, favor_kind_t kind, favor_stab_t stab) {
 }
 
 float qk_scale(int d) { return (float)std::pow((double)d, -0.25); }
+// Scale applied to the projections: d^-1/4 for the random-feature families; the elu + 1 family
+// works on the raw q and k.
+float feat_scale(int d, int kind) { return kind == kKindElu ? 1.f : qk_scale(d); }
 
 template <class Kern>
 favor_status_t set_smem(Kern k, size_t bytes) {
@@ -242,7 +236,7 @@ favor_status_t simt_features(const void* X, const void* Om, float* Phi, int B, i
     dim3 grid((n + kTok - 1) / kTok, BH);
     FAVOR_TRY(traced(FAVOR_KERNEL_FEATURES, s, [&] {
         kern<<<grid, kThreads, smem, s>>>(static_cast<const T*>(X), static_cast<const T*>(Om), Phi, n, m, kind, eps,
-                                          stab, qk_scale(D), head_max);
+                                          stab, feat_scale(D, kind), head_max);
     }));
     if (kind == kKindExp && stab == kStabHead) {
         int64_t per_head = (int64_t)n * m;
@@ -269,7 +263,7 @@ favor_status_t simt_noncausal(const void* Q, const void* K, const void* V, const
     int64_t tps = ((int64_t)n + w.splits - 1) / w.splits;
     tps = (tps + kTok - 1) / kTok * kTok;
     int splits = (int)((n + tps - 1) / tps);  // every split owns at least one token
-    const float sc = qk_scale(D);
+    const float sc = feat_scale(D, kind);
 
     size_t smem_state = sizeof(float) * (2 * kTok * D + kOmChunk * (D + 1) + kTok * kSlice + kTok + 8);
     auto kstate = state_kernel<T, D>;
@@ -305,7 +299,7 @@ favor_status_t simt_causal(const void* Q, const void* K, const void* V, const vo
     FAVOR_TRY(set_smem(kern, smem));
     FAVOR_TRY(traced(FAVOR_KERNEL_CAUSAL, s, [&] {
         kern<<<BH, kThreads, smem, s>>>(static_cast<const T*>(Q), static_cast<const T*>(K), static_cast<const T*>(V),
-                                        static_cast<const T*>(Om), static_cast<T*>(Y), n, m, kind, eps, qk_scale(D), Sg,
+                                        static_cast<const T*>(Om), static_cast<T*>(Y), n, m, kind, eps, feat_scale(D, kind), Sg,
                                         zg);
     }));
     return FAVOR_OK;
@@ -326,7 +320,7 @@ favor_status_t tc_fused(const void* Q, const void* K, const void* V, const void*
     float* Zp = reinterpret_cast<float*>(base);
     base += tcfu::fused_ws_part((size_t)BH * T * 2 * m_pad * 4);
     float* Stab = reinterpret_cast<float*>(base);
-    tcfu::FusedParams fp{n,  m,  m_pad, kind, eps * std::sqrt((float)m), qk_scale(64), static_cast<__nv_bfloat16*>(Y),
+    tcfu::FusedParams fp{n,  m,  m_pad, kind, eps * std::sqrt((float)m), feat_scale(64, kind), static_cast<__nv_bfloat16*>(Y),
                          Pp, Zp, Stab};
     const size_t smem = tcfu::FusedSmem::bytes(m_pad);
     FAVOR_TRY(set_smem(tcfu::nc_fused_small, smem));
@@ -362,7 +356,7 @@ favor_status_t tc_noncausal(const void* Q, const void* K, const void* V, const v
     if (!tma::encode_bf16_3d(&mK, K, D, n, BH, 64, tcnc::kTile) || !tma::encode_bf16_3d(&mV, V, D, n, BH, 64, tcnc::kTile) ||
         !tma::encode_bf16_3d(&mQ, Q, D, n, BH, 64, tcnc::kTile) || !tma::encode_bf16_2d(&mOm, Om, D, m, 64, 128))
         return FAVOR_ERR_CUDA;
-    const float sc = qk_scale(D);
+    const float sc = feat_scale(D, kind);
     const float eps_s = eps * std::sqrt((float)m);
     const int groups = w.m_pad / 128;
 
@@ -410,46 +404,29 @@ favor_status_t tc_noncausal(const void* Q, const void* K, const void* V, const v
 favor_status_t tc_causal(const void* Q, const void* K, const void* V, const void* Om, void* Y, int B, int H, int n,
                          int m, int kind, float eps, cudaStream_t s) {
     const int BH = B * H;
-    const int groups = m_padded(m) / 128;
-    const bool wide = groups > 2;
+    const int cs = m_padded(m) / 128;
     CUtensorMap mQ, mK, mV, mOm;
-    const int tile = wide ? tccw::kTile : tcc::kTile;
-    if (!tma::encode_bf16_3d(&mQ, Q, 64, n, BH, 64, tile) || !tma::encode_bf16_3d(&mK, K, 64, n, BH, 64, tile) ||
-        !tma::encode_bf16_3d(&mV, V, 64, n, BH, 64, tile) || !tma::encode_bf16_2d(&mOm, Om, 64, m, 64, 128))
+    if (!tma::encode_bf16_3d(&mQ, Q, 64, n, BH, 64, tcs::kTile) || !tma::encode_bf16_3d(&mK, K, 64, n, BH, 64, tcs::kTile) ||
+        !tma::encode_bf16_3d(&mV, V, 64, n, BH, 64, tcs::kTile) || !tma::encode_bf16_2d(&mOm, Om, 64, m, 64, 128))
         return FAVOR_ERR_CUDA;
+    tcs::ScanParams sp{n, m, kind, eps * std::sqrt((float)m), feat_scale(64, kind), static_cast<__nv_bfloat16*>(Y)};
+    const size_t smem = tcs::ScanSmem::bytes(cs);
+    auto kern = kind == kKindExp ? tcs::causal_scan<kKindExp> : kind == kKindRelu ? tcs::causal_scan<kKindRelu> : tcs::causal_scan<kKindElu>;
+    FAVOR_TRY(set_smem(kern, smem));
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cfg.stream = s;
+    cfg.gridDim = dim3(BH * cs, 1, 1);
+    cfg.blockDim = dim3(tcs::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
     cudaError_t lerr = cudaSuccess;
-    if (!wide) {
-        const int cs = groups;  // one 128-feature group per CTA
-        tcc::CausalParams cp{n,   m, kind, eps * std::sqrt((float)m), qk_scale(64), static_cast<const __nv_bfloat16*>(K),
-                             static_cast<__nv_bfloat16*>(Y)};
-        const size_t smem = tcc::CausalSmem::bytes(cs);
-        FAVOR_TRY(set_smem(tcc::causal_tc, smem));
-        cfg.gridDim = dim3(BH * cs, 1, 1);
-        cfg.blockDim = dim3(tcc::kThreads, 1, 1);
-        cfg.dynamicSmemBytes = smem;
-        attr[0].val.clusterDim.x = cs;
-        FAVOR_TRY(traced(FAVOR_KERNEL_CAUSAL, s, [&] { lerr = cudaLaunchKernelEx(&cfg, tcc::causal_tc, mQ, mK, mV, mOm, cp); }));
-    } else {
-        const int cs = causal_wide_cluster(BH, m);
-        const int m_cta = ((groups + cs - 1) / cs) * 128;  // features per CTA
-        tccw::CausalParams cp{n, m, m_cta, kind, eps * std::sqrt((float)m), qk_scale(64), static_cast<__nv_bfloat16*>(Y)};
-        const size_t smem = tccw::CausalSmem::bytes(m_cta);
-        FAVOR_TRY(set_smem(tccw::causal_tc_wide, smem));
-        cfg.gridDim = dim3(BH * cs, 1, 1);
-        cfg.blockDim = dim3(tccw::kThreads, 1, 1);
-        cfg.dynamicSmemBytes = smem;
-        attr[0].val.clusterDim.x = cs;
-        FAVOR_TRY(traced(FAVOR_KERNEL_CAUSAL, s,
-                         [&] { lerr = cudaLaunchKernelEx(&cfg, tccw::causal_tc_wide, mQ, mK, mV, mOm, cp); }));
-    }
+    FAVOR_TRY(traced(FAVOR_KERNEL_CAUSAL, s, [&] { lerr = cudaLaunchKernelEx(&cfg, kern, mQ, mK, mV, mOm, sp); }));
     return lerr == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;
 }
 
@@ -466,7 +443,7 @@ favor_status_t tc_features(const void* X, const void* Om, float* Phi, int B, int
     const int tpc = (tiles + chunks - 1) / chunks;
     const int grid_x = (tiles + tpc - 1) / tpc;
     unsigned* head_max = static_cast<unsigned*>(ws);
-    tcf::FeatParams fp{n, m, m_pad, tpc, kind, stab, 0, eps, qk_scale(D), Phi, head_max};
+    tcf::FeatParams fp{n, m, m_pad, tpc, kind, stab, 0, eps, feat_scale(D, kind), Phi, head_max};
     const size_t smem = tcf::FeatSmem<D>::bytes(m_pad);
     auto kern = tcf::features_tc<D>;
     FAVOR_TRY(set_smem(kern, smem));
@@ -494,10 +471,50 @@ favor_status_t check_attn_args(const void* Q, const void* K, const void* V, cons
     FAVOR_TRY(check_shape(B, H, n, d, m, dt, kind));
     if (!(eps >= 0.f) || !std::isfinite(eps)) return FAVOR_ERR_INVALID_ARG;
     if ((int64_t)B * H * n == 0) return FAVOR_OK;
-    if (!Q || !K || !V || !Om || !Y) return FAVOR_ERR_INVALID_ARG;
+    if (!Q || !K || !V || !Y || (!Om && kind != FAVOR_ELU)) return FAVOR_ERR_INVALID_ARG;
     if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(Om, 16) || !aligned(Y, 16))
         return FAVOR_ERR_MISALIGNED;
     return FAVOR_OK;
+}
+
+// The projection of the elu + 1 family is the identity (m = d): the tensor-core kernels run their
+// projection MMA on it (exact: one nonzero product per output) and the CUDA-core kernels their
+// dot products. One copy per dtype and head size, built at compile time.
+template <typename E, int D>
+struct Eye {
+    E v[D * D];
+};
+template <typename E, int D>
+constexpr Eye<E, D> make_eye(E one) {
+    Eye<E, D> e{};
+    for (int i = 0; i < D; ++i) e.v[i * D + i] = one;
+    return e;
+}
+__device__ const Eye<uint16_t, 64> g_eye_bf16_64 = make_eye<uint16_t, 64>(0x3F80u);  // bf16 1.0
+__device__ const Eye<uint16_t, 128> g_eye_bf16_128 = make_eye<uint16_t, 128>(0x3F80u);
+__device__ const Eye<float, 64> g_eye_f32_64 = make_eye<float, 64>(1.f);
+__device__ const Eye<float, 128> g_eye_f32_128 = make_eye<float, 128>(1.f);
+
+std::mutex g_eye_mu;
+void* g_eye_addr[64][4] = {};
+
+// Device address of the identity of head size d in dtype dt on the current device (looked up once
+// per device); nullptr on failure.
+const void* eye_ptr(int d, favor_dtype_t dt) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    const int k = (dt == FAVOR_BF16 ? 0 : 2) + (d == 128 ? 1 : 0);
+    std::lock_guard<std::mutex> g(g_eye_mu);
+    if (!g_eye_addr[dev][k]) {
+        void* p = nullptr;
+        cudaError_t e = k == 0 ? cudaGetSymbolAddress(&p, g_eye_bf16_64)
+                        : k == 1 ? cudaGetSymbolAddress(&p, g_eye_bf16_128)
+                        : k == 2 ? cudaGetSymbolAddress(&p, g_eye_f32_64)
+                                 : cudaGetSymbolAddress(&p, g_eye_f32_128);
+        if (e != cudaSuccess) return nullptr;
+        g_eye_addr[dev][k] = p;
+    }
+    return g_eye_addr[dev][k];
 }
 
 favor_status_t check_ws(void* ws, size_t ws_bytes, size_t need) {
@@ -542,6 +559,7 @@ const char* favor_kernel_name(int kid) {
         case FAVOR_KERNEL_DECODE_INIT: return "decode_init";
         case FAVOR_KERNEL_OMEGA: return "omega";
         case FAVOR_KERNEL_FUSED: return "fused";
+        case FAVOR_KERNEL_EXACT: return "exact";
     }
     return "unknown";
 }
@@ -569,9 +587,10 @@ favor_status_t favor_features(const void* X, const void* Omega, float* Phi, int 
     if (!(relu_eps >= 0.f) || !std::isfinite(relu_eps)) return FAVOR_ERR_INVALID_ARG;
     if ((int64_t)B * H * n == 0) return FAVOR_OK;
     if (!heads_ok(B, H, kMaxHeadsGridY)) return FAVOR_ERR_UNSUPPORTED;
-    if (!X || !Omega || !Phi) return FAVOR_ERR_INVALID_ARG;
+    if (!X || !Phi || (!Omega && kind != FAVOR_ELU)) return FAVOR_ERR_INVALID_ARG;
     if (!aligned(X, 16) || !aligned(Omega, 16) || !aligned(Phi, 16)) return FAVOR_ERR_MISALIGNED;
     FAVOR_TRY(check_ws(workspace, ws_bytes, features_ws_bytes(B, H, kind, stab)));
+    if (kind == FAVOR_ELU && !(Omega = eye_ptr(d, dt))) return FAVOR_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dt == FAVOR_BF16)
         return d == 64 ? tc_features<64>(X, Omega, Phi, B, H, n, m, (int)kind, relu_eps, (int)stab, workspace, s)
@@ -587,6 +606,7 @@ favor_status_t favor_attn_noncausal(const void* Q, const void* K, const void* V,
     if ((int64_t)B * H * n == 0) return FAVOR_OK;
     if (!heads_ok(B, H, kMaxHeadsGridY)) return FAVOR_ERR_UNSUPPORTED;
     FAVOR_TRY(check_ws(workspace, ws_bytes, noncausal_ws_bytes(B, H, n, d, m, dt)));
+    if (kind == FAVOR_ELU && !(Omega = eye_ptr(d, dt))) return FAVOR_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (tc_fused_ok(n, d, m, dt)) return tc_fused(Q, K, V, Omega, Y, B, H, n, m, (int)kind, relu_eps, workspace, s);
     if (tc_noncausal_ok(d, m, dt))
@@ -602,6 +622,7 @@ favor_status_t favor_attn_causal(const void* Q, const void* K, const void* V, co
     if (chunk != 0 && chunk != 64 && chunk != 128) return FAVOR_ERR_UNSUPPORTED;
     if ((int64_t)B * H * n == 0) return FAVOR_OK;
     if (!heads_ok(B, H, kMaxHeads)) return FAVOR_ERR_UNSUPPORTED;
+    if (kind == FAVOR_ELU && !(Omega = eye_ptr(d, dt))) return FAVOR_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (tc_causal_ok(d, m, dt)) return tc_causal(Q, K, V, Omega, Y, B, H, n, m, (int)kind, relu_eps, s);
     FAVOR_TRY(check_ws(workspace, ws_bytes, causal_ws_bytes(B, H, d, m)));
@@ -650,7 +671,7 @@ favor_status_t decode_launch(const void* q, const void* k, const void* v, const 
             static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), static_cast<const T*>(Om),
             static_cast<T*>(y), reinterpret_cast<float*>(base), reinterpret_cast<float*>(base + L.off_z),
             reinterpret_cast<float*>(base + L.off_stab), reinterpret_cast<float*>(base + L.off_part),
-            reinterpret_cast<unsigned*>(base + L.off_cnt), m, kind, eps * std::sqrt((float)m), qk_scale(D));
+            reinterpret_cast<unsigned*>(base + L.off_cnt), m, kind, eps * std::sqrt((float)m), feat_scale(D, kind));
     }));
     return cudaGetLastError() == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;
 }
@@ -706,6 +727,7 @@ favor_status_t favor_decode_step(const void* q, const void* k, const void* v, co
     if ((int64_t)B * H == 0) return FAVOR_OK;
     if (!heads_ok(B, H, kMaxHeads)) return FAVOR_ERR_UNSUPPORTED;
     FAVOR_TRY(check_decode_state(state, state_bytes, B, H, d, m));
+    if (kind == FAVOR_ELU && !(Omega = eye_ptr(d, dt))) return FAVOR_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return FAVOR_DISPATCH(dt, d, decode_launch, q, k, v, Omega, y, state, B * H, m, (int)kind, relu_eps, s);
 }
@@ -774,6 +796,35 @@ favor_status_t favor_last_device_error(void* stream) {
     unsigned zero = 0;
     if (cudaMemcpyToSymbol(g_favor_error, &zero, sizeof(zero)) != cudaSuccess) return FAVOR_ERR_CUDA;
     return FAVOR_ERR_TIMEOUT;
+}
+
+favor_status_t favor_softmax_attn(const void* Q, const void* K, const void* V, void* Y, int B, int H, int n, int d,
+                                  int causal, favor_dtype_t dt, void* stream) {
+    if (B < 0 || H < 0 || n < 0 || (dt != FAVOR_F32 && dt != FAVOR_BF16)) return FAVOR_ERR_INVALID_ARG;
+    if (dt != FAVOR_BF16 || d != 64) return FAVOR_ERR_UNSUPPORTED;
+    if ((int64_t)B * H * n == 0) return FAVOR_OK;
+    if (!heads_ok(B, H, kMaxHeadsGridY)) return FAVOR_ERR_UNSUPPORTED;
+    if (!Q || !K || !V || !Y) return FAVOR_ERR_INVALID_ARG;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(Y, 16)) return FAVOR_ERR_MISALIGNED;
+    const int BH = B * H;
+    CUtensorMap mQ, mK, mV;
+    if (!tma::encode_bf16_3d(&mQ, Q, 64, n, BH, 64, tce::kTile) || !tma::encode_bf16_3d(&mK, K, 64, n, BH, 64, tce::kTile) ||
+        !tma::encode_bf16_3d(&mV, V, 64, n, BH, 64, tce::kTile))
+        return FAVOR_ERR_CUDA;
+    tce::ExactParams ep{n, causal ? 1 : 0, kLog2e / std::sqrt((float)d), static_cast<__nv_bfloat16*>(Y)};
+    const size_t smem = tce::ExactSmem::bytes();
+    FAVOR_TRY(set_smem(tce::exact_attn, smem));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const dim3 grid((n + tce::kTile - 1) / tce::kTile, BH);
+    FAVOR_TRY(traced(FAVOR_KERNEL_EXACT, s, [&] { tce::exact_attn<<<grid, tce::kThreads, smem, s>>>(mQ, mK, mV, ep); }));
+    return FAVOR_OK;
+}
+
+favor_status_t favor_test_set_wait_limit(unsigned long long ns, void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyToSymbolAsync(g_favor_test_wait_ns, &ns, sizeof(ns), 0, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return FAVOR_ERR_CUDA;
+    return cudaStreamSynchronize(s) == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;
 }
 
 favor_status_t favor_trace_enable(int on) {

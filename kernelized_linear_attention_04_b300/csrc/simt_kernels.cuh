@@ -111,8 +111,8 @@ __global__ void __launch_bounds__(kThreads) features_kernel(const T* __restrict_
         if (row >= n) continue;
         float* pr = ps + t * m;
         float* out = Phi + row * m;
-        if (kind == kKindRelu) {
-            for (int r = lane; r < m; r += 32) out[r] = fmaxf(pr[r], 0.f) * inv_sqrt_m + relu_eps;
+        if (kind != kKindExp) {
+            for (int r = lane; r < m; r += 32) out[r] = phi_plain(pr[r], kind, inv_sqrt_m, relu_eps);
             continue;
         }
         float rmax = -INFINITY;
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kThreads) state_kernel(const T* __restrict__ K
         } else {
             for (int e = threadIdx.x; e < kTok * kSlice; e += kThreads) {
                 int t = e / kSlice;
-                ps[e] = t < nvalid ? fmaxf(ps[e], 0.f) * inv_sqrt_m + relu_eps : 0.f;
+                ps[e] = t < nvalid ? phi_plain(ps[e], kind, inv_sqrt_m, relu_eps) : 0.f;
             }
         }
         __syncthreads();
@@ -291,9 +291,9 @@ __global__ void __launch_bounds__(kThreads) readout_kernel(const T* __restrict__
     for (int t = warp; t < kTok; t += kThreads / 32) {
         float* pr = ps + t * m;
         float dsum = 0.f;
-        if (kind == kKindRelu) {
+        if (kind != kKindExp) {
             for (int r = lane; r < m; r += 32) {
-                pr[r] = fmaxf(pr[r], 0.f) * inv_sqrt_m + relu_eps;
+                pr[r] = phi_plain(pr[r], kind, inv_sqrt_m, relu_eps);
                 dsum = fmaf(pr[r], z[r], dsum);
             }
         } else {
@@ -408,8 +408,8 @@ __global__ void __launch_bounds__(kThreads) causal_kernel(const T* __restrict__ 
         } else {
             for (int e = threadIdx.x; e < kTok * m; e += kThreads) {
                 int t = e / m;
-                pk[e] = t < nvalid ? fmaxf(pk[e], 0.f) * inv_sqrt_m + relu_eps : 0.f;
-                pq[e] = fmaxf(pq[e], 0.f) * inv_sqrt_m + relu_eps;
+                pk[e] = t < nvalid ? phi_plain(pk[e], kind, inv_sqrt_m, relu_eps) : 0.f;
+                pq[e] = phi_plain(pq[e], kind, inv_sqrt_m, relu_eps);
             }
         }
         __syncthreads();

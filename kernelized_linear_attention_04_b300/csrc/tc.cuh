@@ -39,6 +39,15 @@ __device__ __forceinline__ uint64_t globaltimer() {
 
 __device__ __forceinline__ uint32_t elect_lane0() { return (threadIdx.x & 31) == 0; }
 
+// One lane of the (converged) warp is elected; true in that lane only.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred P1;\n\telect.sync _|P1, 0xffffffff;\n\tselp.b32 %0, 1, 0, P1;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // ---------------------------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------------------------
@@ -67,21 +76,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-
 // Waits for phase `parity` of `bar` to complete. Returns false (after flagging the error and the
 // CTA abort word) if it does not within kWaitLimitNs, or if another role of the CTA already gave up.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
+    const uint64_t tlim = g_favor_test_wait_ns;
+    const uint64_t limit = tlim ? tlim : kWaitLimitNs;
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) {
-                atomicOr(&g_favor_error, kDevErrTimeout);
-                *abort_flag = 1;
-                return false;
-            }
+        if ((it & 255u) != 0) continue;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > limit) {
+            atomicOr(&g_favor_error, kDevErrTimeout);
+            *abort_flag = 1;
+            return false;
         }
     }
 }
@@ -102,15 +111,16 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
+    const uint64_t tlim = g_favor_test_wait_ns;
+    const uint64_t limit = tlim ? tlim : kWaitLimitNs;
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait_cluster(bar, parity)) return true;
-        if ((it & 255u) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) {
-                atomicOr(&g_favor_error, kDevErrTimeout);
-                *abort_flag = 1;
-                return false;
-            }
+        if ((it & 255u) != 0) continue;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > limit) {
+            atomicOr(&g_favor_error, kDevErrTimeout);
+            *abort_flag = 1;
+            return false;
         }
     }
 }
@@ -286,6 +296,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
            | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
 
+// A descriptor moved on by `bytes` (a multiple of 16) within its shared-memory buffer: the start
+// address field holds address / 16 in 14 bits, which no shared-memory address overflows.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) { return desc + (uint64_t)(bytes >> 4); }
+
 // Shared-memory matrix descriptor with the 128-byte swizzle. Byte offsets must be multiples of 16.
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
     return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16) |
@@ -321,6 +335,32 @@ __device__ __forceinline__ void fma2(float& x0, float& x1, float s, float c) {
         : "+f"(x0), "+f"(x1)
         : "f"(s), "f"(c));
 }
+// Two features as one bf16x2 word from two raw projections a0, a1:
+//   generalized ReLU: max(a s, 0) + eps = max(a s + eps, eps), the sum rounded once to bf16 (the
+//   max of two bf16 values is exact), with eps2 = bf16x2 {eps, eps};
+//   exp family: 2^(a A2 - c) with c the row (or key) constant in binary orders of magnitude.
+__device__ __forceinline__ uint32_t relu_pair(uint32_t a0, uint32_t a1, float s, float eps, uint32_t eps2) {
+    float x0 = __uint_as_float(a0), x1 = __uint_as_float(a1);
+    fma2(x0, x1, s, eps);
+    uint32_t h;
+    asm("{\n\t.reg .b32 t;\n\tcvt.rn.bf16x2.f32 t, %2, %1;\n\tmax.bf16x2 %0, t, %3;\n\t}"
+        : "=r"(h)
+        : "f"(x0), "f"(x1), "r"(eps2));
+    return h;
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ uint32_t exp_pair(uint32_t a0, uint32_t a1, float A2, float c) {
+    float x0 = __uint_as_float(a0), x1 = __uint_as_float(a1);
+    fma2(x0, x1, A2, -c);
+    uint32_t h;
+    asm("cvt.rn.bf16x2.f32 %0, %2, %1;" : "=r"(h) : "f"(ex2_approx(x0)), "f"(ex2_approx(x1)));
+    return h;
+}
+
 __device__ __forceinline__ void tmem_ld2(uint32_t taddr, uint32_t& r0, uint32_t& r1) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(taddr));
 }
@@ -345,6 +385,24 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t& r0) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r0) : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t r0) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(r0) : "memory");
+}
+
+// Named barrier among `nthreads` threads that also returns whether `pred` held in any of them.
+__device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
 
 // Two fp32 -> one bf16x2 word (lo in bits 0..15), round to nearest even.
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {

@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const float a = __uint_as_float(v[i]);
-                    o[i] = exp_kind ? ex2(fmaf(a, A2, -stab_r - lsm)) : fmaxf(a * p.scale, 0.f) * inv_sqrt_m + p.relu_eps;
+                    o[i] = exp_kind ? ex2(fmaf(a, A2, -stab_r - lsm)) : phi_plain(a * p.scale, p.kind, inv_sqrt_m, p.relu_eps);
                 }
                 const int f0 = cg * Wf + c0;
                 if (valid) {

@@ -242,8 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         f0 = ex2(fmaf(a0, A2, -cj[i]));
                         f1 = ex2(fmaf(a1, A2, -cj[i + 1]));
                     } else {
-                        f0 = cj[i] == 0.f ? fmaxf(a0 * p.scale, 0.f) + p.relu_eps_s : 0.f;
-                        f1 = cj[i + 1] == 0.f ? fmaxf(a1 * p.scale, 0.f) + p.relu_eps_s : 0.f;
+                        f0 = cj[i] == 0.f ? phi_plain(a0 * p.scale, p.kind, 1.f, p.relu_eps_s) : 0.f;
+                        f1 = cj[i + 1] == 0.f ? phi_plain(a1 * p.scale, p.kind, 1.f, p.relu_eps_s) : 0.f;
                     }
                     zpart += f0 + f1;
                     pk[i / 2] = pack_bf16(f0, f1);
@@ -307,8 +307,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     f0 = ex2(fmaf(__uint_as_float(v[i]), A2, -cst));
                     f1 = ex2(fmaf(__uint_as_float(v[i + 1]), A2, -cst));
                 } else {
-                    f0 = fmaxf(__uint_as_float(v[i]) * p.scale, 0.f) + p.relu_eps_s;
-                    f1 = fmaxf(__uint_as_float(v[i + 1]) * p.scale, 0.f) + p.relu_eps_s;
+                    f0 = phi_plain(__uint_as_float(v[i]) * p.scale, p.kind, 1.f, p.relu_eps_s);
+                    f1 = phi_plain(__uint_as_float(v[i + 1]) * p.scale, p.kind, 1.f, p.relu_eps_s);
                 }
                 pk[i / 2] = pack_bf16(f0, f1);
             }

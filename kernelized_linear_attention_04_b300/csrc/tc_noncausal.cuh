@@ -437,10 +437,10 @@ __global__ void __launch_bounds__(kStateThreads, 1)
                             f[2] = ex2(fmaf(__uint_as_float(vv[i + 2]), A2, -c4.z));
                             f[3] = ex2(fmaf(__uint_as_float(vv[i + 3]), A2, -c4.w));
                         } else {
-                            f[0] = c4.x == 0.f ? fmaxf(__uint_as_float(vv[i + 0]) * p.scale, 0.f) + p.relu_eps_s : 0.f;
-                            f[1] = c4.y == 0.f ? fmaxf(__uint_as_float(vv[i + 1]) * p.scale, 0.f) + p.relu_eps_s : 0.f;
-                            f[2] = c4.z == 0.f ? fmaxf(__uint_as_float(vv[i + 2]) * p.scale, 0.f) + p.relu_eps_s : 0.f;
-                            f[3] = c4.w == 0.f ? fmaxf(__uint_as_float(vv[i + 3]) * p.scale, 0.f) + p.relu_eps_s : 0.f;
+                            f[0] = c4.x == 0.f ? phi_plain(__uint_as_float(vv[i + 0]) * p.scale, p.kind, 1.f, p.relu_eps_s) : 0.f;
+                            f[1] = c4.y == 0.f ? phi_plain(__uint_as_float(vv[i + 1]) * p.scale, p.kind, 1.f, p.relu_eps_s) : 0.f;
+                            f[2] = c4.z == 0.f ? phi_plain(__uint_as_float(vv[i + 2]) * p.scale, p.kind, 1.f, p.relu_eps_s) : 0.f;
+                            f[3] = c4.w == 0.f ? phi_plain(__uint_as_float(vv[i + 3]) * p.scale, p.kind, 1.f, p.relu_eps_s) : 0.f;
                         }
                         pk[i / 2] = pack_bf16(f[0], f[1]);
                         pk[i / 2 + 1] = pack_bf16(f[2], f[3]);
@@ -790,7 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     f[k] = exp_kind ? ex2(fmaf(__uint_as_float(v[i + k]), A2, -cst))
-                                    : fmaxf(__uint_as_float(v[i + k]) * p.scale, 0.f) + p.relu_eps_s;
+                                    : phi_plain(__uint_as_float(v[i + k]) * p.scale, p.kind, 1.f, p.relu_eps_s);
                 const uint32_t w0 = pack_bf16(f[0], f[1]), w1 = pack_bf16(f[2], f[3]);
                 pk[i / 2] = w0;
                 pk[i / 2 + 1] = w1;

@@ -1,0 +1,850 @@
+// Tensor-core (tcgen05 + TMA + TMEM) causal FAVOR+ scan, bf16 in / fp32 accumulate, d = 64,
+// m <= 512.
+//
+// One thread-block cluster of CS = ceil(m / 128) CTAs walks the 128-token tiles of one head in
+// order; CTA `rank` owns the features [128 rank, 128 rank + 128). Per tile t (query rows i, keys j
+// of the tile) each CTA forms, over its own features,
+//   num_i = phi(q_i) S_<t + sum_{j <= i} (phi(q_i) . phi(k_j)) v_j
+//   den_i = phi(q_i) z_<t + sum_{j <= i}  phi(q_i) . phi(k_j)
+// and then S_<t+1 = S_<t + Phi(K_t)^T V_t, z_<t+1 = z_<t + Phi(K_t)^T 1 ("Performer for vision",
+// *How It Works*, Step 2: prefix sums; the state is carried every 128 tokens and keys are masked
+// by j <= i inside the tile, which for two 64-token chunks is exactly their chunked prefix sum).
+// The CTAs of a cluster then add their partial results row by row through distributed shared
+// memory.
+//
+// Every contraction runs on the tensor cores, with the A operand in TMEM wherever it is produced
+// there:
+//   P_K   = K_t Omega_g^T        (A, B from shared memory)           -> TMEM, tokens on lanes
+//   P_Q   = Q_t Omega_g^T        (same)                              -> TMEM, tokens on lanes
+//   SC    = phi(Q) phi(K)^T      (A: phi(Q) packed bf16 in TMEM, B: phi(K) in shared memory)
+//   NUM   = phi(Q) [S | z]_<t    (A: phi(Q) in TMEM, B: bf16 image of the state; for the exp family
+//                                 a second MMA adds phi(Q) S_lo, the rounding remainder of S)
+//   [S|z] += phi(K)^T [V | 1]    (A: phi(K) in shared memory, read transposed)
+//   NUM  += A~ [V | 1]           (A: masked scores A~ packed bf16 in TMEM, in place of SC)
+// Columns 64 and 65 of NUM add up to the denominator (the ones column of [V | 1]; z and its
+// rounding remainder in the state image), so no row sum is formed on the CUDA cores. MMA issue
+// order per tile: scores(t), inter(t), proj Q(t+1), state(t), intra(t), proj K(t+2); each warp
+// team below works on one stage while the tensor cores run the others.
+//
+// Warp roles:
+//   warp 0       TMA producer (lane 0): Omega_g once; K and Q single-buffered, V double-buffered.
+//   warp 1       MMA issuer (the warp waits, one elected lane issues).
+//   warps 2-9    Q team: phi(Q_t) from P_Q (two warps per TMEM lane quarter, 64 features each) into
+//                the packed phi(Q) columns; for exp features the exact row maximum over the CTA's
+//                features is exchanged between the two halves of the row.
+//   warps 10-13  K team: phi(K_t) from P_K into shared memory (K-major rows, the scores' B operand
+//                and, read transposed, the state's A operand); the running key stabiliser.
+//   warps 14-17  A team: SC -> A~ (masked by j <= i, bf16) in place; then the bf16 image of
+//                [S | z] after the state update (rescaled first if the key stabiliser rose).
+//   warps 18-21  O team: NUM -> y, with the cluster exchange.
+//
+// Stabilisers (exp family; Y does not depend on them, both cancel between num and den):
+//   queries: c_i = the exact largest w_r . q^_i over the CTA's features (the row's largest feature
+//   is 1); the common -|q^_i|^2/2 is dropped;
+//   keys: a running constant per CTA, the exact largest exponent w_r . k^_j - |k^_j|^2/2 seen so
+//   far over the CTA's features and the head's keys, raised (and the state rescaled) only when a
+//   tile exceeds it by more than kSlackHi binary orders of magnitude;
+//   across the cluster, each CTA's partial row carries its exponent offset e = c_i + beta; the
+//   owner of the row weights the partials by 2^(e - max e).
+// The common factor 1/sqrt(m) is dropped. The generalized-ReLU and elu + 1 families have no
+// stabiliser.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "tc.cuh"
+#include "tc_noncausal.cuh"  // shared helpers: ex2, tile_row_sqnorm
+
+namespace favor {
+namespace tcs {
+
+using namespace favor::tc;
+using tcnc::ex2;
+using tcnc::tile_row_sqnorm;
+
+constexpr int kTile = 128;
+constexpr int kD = 64;
+constexpr int kMaxCluster = 4;                    // m <= 512
+constexpr int kQWarp0 = 2, kQWarps = 8;
+constexpr int kKWarp0 = kQWarp0 + kQWarps, kKWarps = 4;
+constexpr int kAWarp0 = kKWarp0 + kKWarps, kAWarps = 4;
+constexpr int kOWarp0 = kAWarp0 + kAWarps, kOWarps = 4;
+constexpr int kThreads = 32 * (kOWarp0 + kOWarps);  // 704
+constexpr int kTileBytes = kTile * kD * 2;          // 16 KB: [128 x 64] bf16
+constexpr int kPhiBytes = kTile * 128 * 2;          // 32 KB: [128 tokens x 128 features] bf16
+constexpr int kXRow = 144;                          // bytes per row of the cluster exchange: 64 fp16 y, den, e
+constexpr float kSlackHi = 16.f;                    // key stabiliser rises once exceeded by 2^16
+
+// Timeline of one CTA for profiling builds (compiled with -DFAVOR_SCAN_TRACE): the SM clock at
+// named points of each role, for the first kTraceTiles tiles of CTA 0. Off in the library.
+#ifdef FAVOR_SCAN_TRACE
+constexpr int kTraceTiles = 16, kTraceEvents = 32;
+__device__ unsigned long long g_scan_trace[kTraceTiles][kTraceEvents];
+#define SCAN_TRACE(t, ev)                                                              \
+    do {                                                                               \
+        if (blockIdx.x == 0 && (t) < kTraceTiles) g_scan_trace[(t)][(ev)] = clock64(); \
+    } while (0)
+#else
+#define SCAN_TRACE(t, ev) ((void)0)
+#endif
+
+// TMEM columns (512 allocated)
+constexpr uint32_t kColS = 0;      // [S | z]: 64 columns of S, z in column 64, 65..79 zero
+constexpr uint32_t kColPQ = 80;    // phi(Q) packed bf16: 128 features in 64 columns
+constexpr uint32_t kColNum = 144;  // NUM: 64 numerator columns, denominator parts in columns 64, 65
+constexpr uint32_t kColR0 = 224;   // two 128-column regions: P_K(t), then P_Q(t), then SC(t) / A~(t)
+constexpr uint32_t kColSpare = 480;  // 32 columns: second half of an owner's NUM rows during the exchange
+
+// Shared memory offsets from the 1024-aligned base.
+constexpr uint32_t kOffOm = 0;
+constexpr uint32_t kOffQ = kOffOm + kTileBytes;
+constexpr uint32_t kOffK = kOffQ + kTileBytes;
+constexpr uint32_t kOffV = kOffK + kTileBytes;          // two buffers
+constexpr uint32_t kOffPK = kOffV + 2 * kTileBytes;     // two phi(K) buffers
+constexpr uint32_t kOffSnap = kOffPK + 2 * kPhiBytes;   // S image (bf16 hi), MN-major [128 features x 64]
+constexpr uint32_t kOffZb = kOffSnap + kTileBytes;      // z image: elements 0 (hi) and 1 (lo) of each feature row
+constexpr uint32_t kOffSlo = kOffZb + kTileBytes;       // S rounding remainder (bf16 lo), exp family
+constexpr uint32_t kOffOnes = kOffSlo + kTileBytes;     // element 0 of each token row = 1
+constexpr uint32_t kOffCq = kOffOnes + kTileBytes;      // [2][128] f32 query row constants
+constexpr uint32_t kOffMx = kOffCq + 2 * 128 * 4;       // [2][2][128] f32 row-max halves
+constexpr uint32_t kOffX = kOffMx + 2 * 2 * 128 * 4;    // cluster exchange receive buffer
+
+struct ScanParams {
+    int n;
+    int m;
+    int kind;
+    float relu_eps_s;  // relu_eps * sqrt(m): the features are scaled by sqrt(m) (a common factor)
+    float scale;       // d^-1/4 (1 for elu + 1)
+    __nv_bfloat16* Y;
+};
+
+struct ScanSmem {
+    static int rows_per_owner(int cs) { return (kTile + cs - 1) / cs; }
+    static size_t x_bytes(int cs) { return cs > 1 ? (size_t)(cs - 1) * rows_per_owner(cs) * kXRow : 0; }
+    static size_t bytes(int cs) { return 1024 + kOffX + x_bytes(cs); }
+};
+
+// Number of O-team warps (32 rows each) holding at least one row of owner `o`.
+__device__ __forceinline__ int owner_warps(int o, int rp) {
+    int c = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) c += ((32 * q) / rp <= o && o <= (32 * q + 31) / rp) ? 1 : 0;
+    return c;
+}
+
+// bf16 image of 8 fp32 values as one 16-byte chunk, and (lo) the bf16 rounding of what the first
+// image leaves out.
+__device__ __forceinline__ uint4 pack8_hi(const uint32_t* v) {
+    return make_uint4(pack_bf16(__uint_as_float(v[0]), __uint_as_float(v[1])),
+                      pack_bf16(__uint_as_float(v[2]), __uint_as_float(v[3])),
+                      pack_bf16(__uint_as_float(v[4]), __uint_as_float(v[5])),
+                      pack_bf16(__uint_as_float(v[6]), __uint_as_float(v[7])));
+}
+__device__ __forceinline__ uint32_t lo_pair(uint32_t x0, uint32_t x1, uint32_t hw) {
+    return pack_bf16(__uint_as_float(x0) - __uint_as_float(hw << 16), __uint_as_float(x1) - __uint_as_float(hw & 0xFFFF0000u));
+}
+
+// KIND: the feature family (kKindExp, kKindRelu, kKindElu), fixed per instance so that each
+// instance carries only its own feature map and stabiliser code.
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    causal_scan(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+                const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mOm, ScanParams p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];  // aligned to 1024 by hand below
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int CS = (int)cluster_size();
+    const int rank = (int)cluster_rank();
+    const int RP = (kTile + CS - 1) / CS;  // rows finalised by each CTA of the cluster
+    const int feat0 = rank * 128;
+    uint8_t* sOm = smem + kOffOm;
+    uint8_t* sQ = smem + kOffQ;
+    uint8_t* sK = smem + kOffK;
+    uint8_t* sV = smem + kOffV;
+    uint8_t* sPK = smem + kOffPK;
+    uint8_t* sSnap = smem + kOffSnap;
+    uint8_t* sZb = smem + kOffZb;
+    uint8_t* sSlo = smem + kOffSlo;
+    uint8_t* sOnes = smem + kOffOnes;
+    float* sCq = reinterpret_cast<float*>(smem + kOffCq);
+    float* sMx = reinterpret_cast<float*>(smem + kOffMx);
+    uint8_t* sX = smem + kOffX;
+    __shared__ uint64_t bar_om, bar_kfull, bar_kfree, bar_qfull, bar_qfree, bar_vfull[2], bar_vfree[2];
+    __shared__ uint64_t bar_pk[2], bar_pkfree[2], bar_pq[2], bar_phq, bar_phk[2], bar_phkfree[2];
+    __shared__ uint64_t bar_sc, bar_atil, bar_st, bar_snap, bar_num, bar_numfree, bar_beta[4], bar_cq[2];
+    __shared__ uint64_t bar_xfull, bar_xfree, bar_drain;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+    __shared__ float sBeta[4], sF[4], sKmx[4];
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int bh = blockIdx.x / CS;
+    const int T = (p.n + kTile - 1) / kTile;
+    constexpr bool exp_kind = KIND == kKindExp;
+    constexpr bool hilo = exp_kind;     // state image with its rounding remainder
+    const float A2 = p.scale * kLog2e;  // projections -> exponents in binary orders of magnitude
+    uint32_t eps2;                      // bf16x2 {eps, eps} of the ReLU family's floor
+    {
+        const __nv_bfloat162 e2 = __floats2bfloat162_rn(p.relu_eps_s, p.relu_eps_s);
+        eps2 = *reinterpret_cast<const uint32_t*>(&e2);
+    }
+    // 32 raw projections -> 16 bf16x2 words of features (zero when `real` is false: padding
+    // features of the last 128-feature group); c is the row or key constant of the exp family.
+    auto features16 = [&](const uint32_t (&v)[32], uint32_t (&w)[16], bool real, float c) {
+        if (!real) {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) w[k] = 0u;
+        } else if constexpr (KIND == kKindExp) {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) w[k] = exp_pair(v[2 * k], v[2 * k + 1], A2, c);
+        } else if constexpr (KIND == kKindRelu) {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) w[k] = relu_pair(v[2 * k], v[2 * k + 1], p.scale, p.relu_eps_s, eps2);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                w[k] = pack_bf16(phi_plain(__uint_as_float(v[2 * k]), KIND, 1.f, 0.f),
+                                 phi_plain(__uint_as_float(v[2 * k + 1]), KIND, 1.f, 0.f));
+        }
+    };
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(&bar_om, 1);
+        mbar_init(&bar_kfull, 1);
+        mbar_init(&bar_kfree, kKWarps);
+        mbar_init(&bar_qfull, 1);
+        mbar_init(&bar_qfree, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bar_vfull[b], 1);
+            mbar_init(&bar_vfree[b], 1);
+            mbar_init(&bar_pk[b], 1);
+            mbar_init(&bar_pkfree[b], kKWarps);
+            mbar_init(&bar_pq[b], 1);
+            mbar_init(&bar_phk[b], kKWarps);
+            mbar_init(&bar_phkfree[b], 1);
+            mbar_init(&bar_cq[b], kQWarps / 2);
+        }
+        for (int b = 0; b < 4; ++b) mbar_init(&bar_beta[b], 1);
+        mbar_init(&bar_phq, kQWarps);
+        mbar_init(&bar_sc, 1);
+        mbar_init(&bar_atil, kAWarps);
+        mbar_init(&bar_st, 1);
+        mbar_init(&bar_snap, kAWarps);
+        mbar_init(&bar_num, 1);
+        mbar_init(&bar_numfree, kOWarps);
+        mbar_init(&bar_xfull, CS > 1 ? (CS - 1) * owner_warps(rank, RP) : 1);
+        mbar_init(&bar_xfree, CS > 1 ? CS - 1 : 1);
+        mbar_init(&bar_drain, 1);
+        fence_mbar_init();
+    }
+    // Constant operands: the ones column of [V | 1] (element 0 of every token row), and the initial
+    // state image S_<0 = 0, z_<0 = 0. In the 128-byte swizzle, element 0 of row k sits in 16-byte
+    // chunk (k mod 8) of the row.
+    for (int i = threadIdx.x; i < kTileBytes / 16; i += blockDim.x) {
+        const int row = i >> 3, chunk = i & 7;
+        reinterpret_cast<uint4*>(sOnes)[i] = make_uint4(chunk == (row & 7) ? 0x00003F80u : 0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4*>(sSnap)[i] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4*>(sSlo)[i] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4*>(sZb)[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_async_smem();
+    if (warp == 1) tmem_alloc(&tmem_base, 512);
+    __syncthreads();
+    cluster_sync();  // every CTA's barriers are initialised before any remote arrive
+    tc_fence_after();
+    const uint32_t tbase = tmem_base;
+
+    if (warp == 0) {
+        // ---------------- TMA producer (lane 0) ----------------
+        if (lane == 0) {
+            tma_prefetch_desc(&mOm);
+            tma_prefetch_desc(&mQ);
+            tma_prefetch_desc(&mK);
+            tma_prefetch_desc(&mV);
+            mbar_arrive_expect_tx(&bar_om, (uint32_t)kTileBytes);
+            tma_load_2d(sOm, &mOm, &bar_om, 0, feat0);
+            int kl = 0, ql = 0, vl = 0;  // tiles loaded
+            for (int t = 0; t < T; ++t) {
+                const int b = t & 1, u = t >> 1;
+                // K(t) once the K team has taken the norms of K(t-1) and P_K(t-1) has read it
+                if (t > 0 && !mbar_wait(&bar_kfree, (t - 1) & 1, &abort_flag)) break;
+                mbar_arrive_expect_tx(&bar_kfull, kTileBytes);
+                tma_load_3d(sK, &mK, &bar_kfull, 0, t * kTile, bh);
+                kl = t + 1;
+                // Q(t) once P_Q(t-1) has read Q(t-1)
+                if (t > 0 && !mbar_wait(&bar_qfree, (t - 1) & 1, &abort_flag)) break;
+                mbar_arrive_expect_tx(&bar_qfull, kTileBytes);
+                tma_load_3d(sQ, &mQ, &bar_qfull, 0, t * kTile, bh);
+                ql = t + 1;
+                // V(t) once the intra MMA of tile t-2 (the last reader of buffer b) is done
+                if (t > 1 && !mbar_wait(&bar_vfree[b], (u & 1) ^ 1, &abort_flag)) break;
+                mbar_arrive_expect_tx(&bar_vfull[b], kTileBytes);
+                tma_load_3d(sV + b * kTileBytes, &mV, &bar_vfull[b], 0, t * kTile, bh);
+                vl = t + 1;
+            }
+            // Drain the loads in flight before the CTA may exit.
+            volatile int never = 0;
+            mbar_wait(&bar_om, 0, &never);
+            if (kl > 0) mbar_wait(&bar_kfull, (kl - 1) & 1, &never);
+            if (ql > 0) mbar_wait(&bar_qfull, (ql - 1) & 1, &never);
+            for (int t = vl - 2 < 0 ? 0 : vl - 2; t < vl; ++t) mbar_wait(&bar_vfull[t & 1], (t >> 1) & 1, &never);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer: the whole warp waits, one elected lane issues ----------------
+        constexpr uint32_t id_p = idesc_bf16(128, 128, false, false);      // P = X Omega_g^T
+        constexpr uint32_t id_sc = idesc_bf16(128, 128, false, false);     // SC = phi(Q) phi(K)^T
+        constexpr uint32_t id_o = idesc_bf16(128, kD + 16, false, true);   // NUM += {phi(Q), A~} [.. | ..]
+        constexpr uint32_t id_lo = idesc_bf16(128, kD, false, true);       // NUM += phi(Q) S_lo
+        constexpr uint32_t id_st = idesc_bf16(128, kD + 16, true, true);   // [S|z] += phi(K)^T [V | 1]
+        // Base descriptors; each MMA moves one on by a constant offset.
+        const uint64_t d_om = sdesc_sw128(smem_u32(sOm), 16, 1024);
+        const uint64_t d_q = sdesc_sw128(smem_u32(sQ), 16, 1024);
+        const uint64_t d_k = sdesc_sw128(smem_u32(sK), 16, 1024);
+        const uint64_t d_snap = sdesc_sw128(smem_u32(sSnap), kOffZb - kOffSnap, 1024);
+        const uint64_t d_slo = sdesc_sw128(smem_u32(sSlo), 16, 1024);
+        uint64_t d_pk_sc[2], d_pk_st[2], d_v[2];
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            d_pk_sc[b] = sdesc_sw128(smem_u32(sPK + b * kPhiBytes), 16, 1024);
+            d_pk_st[b] = sdesc_sw128(smem_u32(sPK + b * kPhiBytes), 16384, 1024);
+            d_v[b] = sdesc_sw128(smem_u32(sV + b * kTileBytes), (uint32_t)(sOnes - (sV + b * kTileBytes)), 1024);
+        }
+        const bool leader = elect_one();
+        bool ok = mbar_wait(&bar_om, 0, &abort_flag);
+        tc_fence_after();
+        // P_K(t) into region t & 1 (once K(t) is loaded)
+        auto issue_pk = [&](int t) -> bool {
+            if (!mbar_wait(&bar_kfull, t & 1, &abort_flag)) return false;
+            tc_fence_after();
+            if (leader) {
+                const uint32_t dcol = tbase + kColR0 + 128u * (uint32_t)(t & 1);
+#pragma unroll
+                for (int ks = 0; ks < kD / 16; ++ks)
+                    mma_ss(dcol, sdesc_add(d_k, 32u * ks), sdesc_add(d_om, 32u * ks), id_p, ks > 0);
+                mma_commit(&bar_pk[t & 1]);
+            }
+            __syncwarp();
+            return true;
+        };
+        // P_Q(t) into region t & 1, once Q(t) is loaded and the K team has read P_K(t)
+        auto issue_pq = [&](int t) -> bool {
+            const int b = t & 1;
+            if (!mbar_wait(&bar_qfull, t & 1, &abort_flag)) return false;
+            if (!mbar_wait(&bar_pkfree[b], (t >> 1) & 1, &abort_flag)) return false;
+            tc_fence_after();
+            if (leader) {
+                const uint32_t dcol = tbase + kColR0 + 128u * (uint32_t)b;
+#pragma unroll
+                for (int ks = 0; ks < kD / 16; ++ks)
+                    mma_ss(dcol, sdesc_add(d_q, 32u * ks), sdesc_add(d_om, 32u * ks), id_p, ks > 0);
+                mma_commit(&bar_pq[b]);
+                mma_commit(&bar_qfree);
+            }
+            __syncwarp();
+            return true;
+        };
+        if (ok && T > 0) ok = issue_pk(0) && issue_pq(0) && (T < 2 || issue_pk(1));
+        for (int t = 0; t < T && ok; ++t) {
+            const int b = t & 1, u = t >> 1;
+            const uint32_t R = tbase + kColR0 + 128u * (uint32_t)b;
+            const uint32_t pq = tbase + kColPQ;
+            const uint32_t num = tbase + kColNum;
+            // scores: SC = phi(Q_t) phi(K_t)^T (K = 128 features, two K atoms of phi(K))
+            SCAN_TRACE(t, 20);
+            ok = mbar_wait(&bar_phq, t & 1, &abort_flag) && mbar_wait(&bar_phk[b], u & 1, &abort_flag);
+            if (!ok) break;
+            SCAN_TRACE(t, 0);
+            tc_fence_after();
+            if (leader) {
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_ts(R, pq + 8u * ks, sdesc_add(d_pk_sc[b], (ks >> 2) * 16384u + (ks & 3) * 32u), id_sc, ks > 0);
+                mma_commit(&bar_sc);
+            }
+            __syncwarp();
+            // inter: NUM = phi(Q_t) [S_<t | z_<t] (K = 128 features), plus phi(Q_t) S_lo
+            SCAN_TRACE(t, 21);
+            ok = mbar_wait(&bar_snap, t & 1, &abort_flag) && mbar_wait(&bar_numfree, (t & 1) ^ 1, &abort_flag);
+            if (!ok) break;
+            SCAN_TRACE(t, 1);
+            tc_fence_after();
+            if (leader) {
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) mma_ts(num, pq + 8u * ks, sdesc_add(d_snap, 2048u * ks), id_o, ks > 0);
+                if (hilo) {
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) mma_ts(num, pq + 8u * ks, sdesc_add(d_slo, 2048u * ks), id_lo, 1u);
+                }
+            }
+            __syncwarp();
+            // the next tile's query projection (phi(Q_t) has been read by now, in MMA order), so
+            // that phi(Q_{t+1}) is formed while this tile's state and intra MMAs run
+            if (t + 1 < T && !(ok = issue_pq(t + 1))) break;
+            SCAN_TRACE(t, 2);
+            // state: [S | z] += phi(K_t)^T [V_t | 1] (K = 128 tokens; phi(K) read MN-major, its
+            // second 64-feature region LBO bytes on; the ones are the second N region of B)
+            if (!(ok = mbar_wait(&bar_vfull[b], u & 1, &abort_flag))) break;
+            tc_fence_after();
+            if (leader) {
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_ss(tbase + kColS, sdesc_add(d_pk_st[b], 2048u * ks), sdesc_add(d_v[b], 2048u * ks), id_st,
+                           (t > 0 || ks > 0) ? 1u : 0u);
+                mma_commit(&bar_st);
+                mma_commit(&bar_phkfree[b]);
+            }
+            __syncwarp();
+            SCAN_TRACE(t, 3);
+            // intra: NUM += A~ [V_t | 1] (K = 128 keys, A~ packed in place of the scores)
+            SCAN_TRACE(t, 22);
+            if (!(ok = mbar_wait(&bar_atil, t & 1, &abort_flag))) break;
+            SCAN_TRACE(t, 4);
+            tc_fence_after();
+            if (leader) {
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) mma_ts(num, R + 8u * ks, sdesc_add(d_v[b], 2048u * ks), id_o, 1u);
+                mma_commit(&bar_num);
+                mma_commit(&bar_vfree[b]);
+            }
+            __syncwarp();
+            if (t + 2 < T && !(ok = issue_pk(t + 2))) break;
+            SCAN_TRACE(t, 5);
+        }
+        // Every MMA issued (all of them, or those before a wait gave up) completes before TMEM is
+        // released.
+        if (leader) mma_commit(&bar_drain);
+        __syncwarp();
+        volatile int never = 0;
+        mbar_wait(&bar_drain, 0, &never);
+    } else if (warp < kKWarp0) {
+        // ---------------- Q team: 8 warps ----------------
+        const int qw = warp - kQWarp0;
+        const int q = warp & 3, h = qw >> 2;  // TMEM lane quarter, feature half
+        const int r = q * 32 + lane;          // token row of the tile
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        const int fv = min(64, max(0, p.m - feat0 - 64 * h));  // real features among this warp's 64
+        bool failed = false;
+        for (int t = 0; t < T; ++t) {
+            const int b = t & 1, u = t >> 1;
+            failed |= !mbar_wait(&bar_pq[b], u & 1, &abort_flag);
+            if (warp == kQWarp0 && lane == 0) SCAN_TRACE(t, 6);
+            __syncwarp();
+            tc_fence_after();
+            const uint32_t pa = tbase + lane_off + kColR0 + 128u * (uint32_t)b + 64u * (uint32_t)h;
+            float c = 0.f;
+            if (exp_kind) {
+                float mx = -INFINITY;
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    if (32 * cc < fv) {
+                        uint32_t v[32];
+                        tmem_ld32(pa + 32u * cc, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(v[i]));
+                    }
+                }
+                float* mxb = sMx + (t & 1) * 256;
+                mxb[h * 128 + r] = mx;
+                named_bar(1, 32 * kQWarps);
+                c = A2 * fmaxf(mxb[r], mxb[128 + r]);
+                if (h == 0) {
+                    sCq[(t & 1) * 128 + r] = c;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar_cq[t & 1]);
+                }
+            }
+#pragma unroll 1
+            for (int cc = 0; cc < 2; ++cc) {
+                uint32_t v[32], w[16];
+                tmem_ld32(pa + 32u * cc, v);
+                tmem_ld_wait();
+                features16(v, w, 32 * cc < fv, c);
+                tmem_st16(tbase + lane_off + kColPQ + 32u * h + 16u * cc, w);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_phq);
+            if (warp == kQWarp0 && lane == 0) SCAN_TRACE(t, 7);
+        }
+        (void)failed;
+    } else if (warp < kAWarp0) {
+        // ---------------- K team: 4 warps ----------------
+        const int q = warp & 3;
+        const int r = q * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        const int fv = min(128, p.m - feat0);  // real features of this CTA (64 or 128)
+        const float s2 = p.scale * p.scale;
+        float beta = -INFINITY;  // running key stabiliser, binary orders of magnitude
+        bool failed = false;
+        for (int t = 0; t < T; ++t) {
+            const int b = t & 1, u = t >> 1;
+            const bool valid = t * kTile + r < p.n;
+            float kn = 0.f;  // |k^_r|^2 / 2 in binary orders of magnitude
+            if (exp_kind) {
+                failed |= !mbar_wait(&bar_kfull, t & 1, &abort_flag);
+                __syncwarp();
+                kn = 0.5f * s2 * tile_row_sqnorm<64>(sK, r) * kLog2e;
+            }
+            failed |= !mbar_wait(&bar_pk[b], u & 1, &abort_flag);
+            if (warp == kKWarp0 && lane == 0) SCAN_TRACE(t, 8);
+            __syncwarp();
+            tc_fence_after();
+            if (lane == 0) mbar_arrive(&bar_kfree);  // K(t) has been read by P_K(t) and for the norms
+            const uint32_t pa = tbase + lane_off + kColR0 + 128u * (uint32_t)b;
+            float f = 1.f;
+            if (exp_kind) {
+                float mx = -INFINITY;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    if (32 * cc < fv) {
+                        uint32_t v[32];
+                        tmem_ld32(pa + 32u * cc, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(v[i]));
+                    }
+                }
+                const float mj = valid ? fmaf(A2, mx, -kn) : -INFINITY;
+                if (named_bar_or(2, 32 * kKWarps, mj > beta + kSlackHi)) {
+                    const float wm = warp_max(mj);
+                    if (lane == 0) sKmx[q] = wm;
+                    named_bar(2, 32 * kKWarps);
+                    const float M = fmaxf(fmaxf(sKmx[0], sKmx[1]), fmaxf(sKmx[2], sKmx[3]));
+                    f = ex2(beta - M);  // 0 on the first tile (beta = -inf), when the state is still empty
+                    beta = M;
+                }
+            } else {
+                beta = 0.f;
+            }
+            if (r == 0) {
+                sBeta[t & 3] = beta;
+                sF[t & 3] = f;
+                mbar_arrive(&bar_beta[t & 3]);
+                SCAN_TRACE(t, 9);
+            }
+            // phi(K_t) into buffer b once the MMAs of tile t-2 have read it
+            if (t >= 2) {
+                failed |= !mbar_wait(&bar_phkfree[b], (u & 1) ^ 1, &abort_flag);
+                __syncwarp();
+            }
+            uint8_t* dst = sPK + b * kPhiBytes;
+            const float ck = kn + beta;
+            const uint32_t keep = valid ? 0xFFFFFFFFu : 0u;  // keys past n contribute nothing
+#pragma unroll 1
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t v[32], w[16];
+                tmem_ld32(pa + 32u * cc, v);
+                tmem_ld_wait();
+                if (cc == 3) {  // P_K(t) fully read: the region may take P_Q(t)
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar_pkfree[b]);
+                }
+                features16(v, w, 32 * cc < fv, ck);
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4)
+                    *reinterpret_cast<uint4*>(dst + (cc >> 1) * 16384 + sw128_offset(r, (cc & 1) * 4 + k4)) =
+                        make_uint4(w[4 * k4] & keep, w[4 * k4 + 1] & keep, w[4 * k4 + 2] & keep, w[4 * k4 + 3] & keep);
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_phk[b]);
+            if (warp == kKWarp0 && lane == 0) SCAN_TRACE(t, 10);
+        }
+        (void)failed;
+    } else if (warp < kOWarp0) {
+        // ---------------- A team: 4 warps ----------------
+        const int q = warp & 3;
+        const int r = q * 32 + lane;  // query row of SC; feature row of the state
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        bool failed = false;
+        const bool withhold = g_favor_test_wait_ns != 0;  // test hook: never publish the first state image
+        // the state image before tile 0 (zero) is in place
+        __syncwarp();
+        if (lane == 0 && !withhold) mbar_arrive(&bar_snap);
+        for (int t = 0; t < T; ++t) {
+            failed |= !mbar_wait(&bar_sc, t & 1, &abort_flag);
+            if (warp == kAWarp0 && lane == 0) SCAN_TRACE(t, 11);
+            __syncwarp();
+            tc_fence_after();
+            const uint32_t ra = tbase + lane_off + kColR0 + 128u * (uint32_t)(t & 1);
+            // keys [32 cc, 32 cc + 32) of row 32 q + lane: all after the warp's rows (cc > q), all at
+            // or before them (cc < q), or across the diagonal (cc == q). Packed key j -> column j / 2;
+            // chunk cc writes columns the chunks up to cc have already been read from.
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t w[16];
+                if (cc > q) {
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) w[k] = 0u;
+                } else {
+                    uint32_t v[32];
+                    tmem_ld32(ra + 32u * cc, v);
+                    tmem_ld_wait();
+                    if (cc < q) {
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) w[k] = pack_bf16(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            const float a0 = 2 * k <= lane ? __uint_as_float(v[2 * k]) : 0.f;
+                            const float a1 = 2 * k + 1 <= lane ? __uint_as_float(v[2 * k + 1]) : 0.f;
+                            w[k] = pack_bf16(a0, a1);
+                        }
+                    }
+                }
+                tmem_st16(ra + 16u * cc, w);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_atil);
+            if (warp == kAWarp0 && lane == 0) SCAN_TRACE(t, 12);
+            // ---- the state image S_<t+1 once state(t) is done (rescaled if the key stabiliser rose)
+            if (t + 1 < T) {
+                const int t1 = t + 1;
+                failed |= !mbar_wait(&bar_st, t & 1, &abort_flag);
+                failed |= !mbar_wait(&bar_beta[t1 & 3], (t1 >> 2) & 1, &abort_flag);
+                if (warp == kAWarp0 && lane == 0) SCAN_TRACE(t, 13);
+                __syncwarp();
+                tc_fence_after();
+                const float f = sF[t1 & 3];
+                const uint32_t sa = tbase + lane_off + kColS;
+                uint32_t zr;
+                tmem_ld1(sa + 64, zr);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t v[32];
+                    tmem_ld32(sa + 32u * hh, v);
+                    tmem_ld_wait();
+                    if (f != 1.f) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
+                        tmem_st32(sa + 32u * hh, v);
+                    }
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 o = pack8_hi(v + 8 * c);
+                        *reinterpret_cast<uint4*>(sSnap + sw128_offset(r, 4 * hh + c)) = o;
+                        if (hilo) {
+                            const uint4 ol = make_uint4(lo_pair(v[8 * c + 0], v[8 * c + 1], o.x), lo_pair(v[8 * c + 2], v[8 * c + 3], o.y),
+                                                        lo_pair(v[8 * c + 4], v[8 * c + 5], o.z), lo_pair(v[8 * c + 6], v[8 * c + 7], o.w));
+                            *reinterpret_cast<uint4*>(sSlo + sw128_offset(r, 4 * hh + c)) = ol;
+                        }
+                    }
+                }
+                if (f != 1.f) {
+                    zr = __float_as_uint(__uint_as_float(zr) * f);
+                    tmem_st1(sa + 64, zr);
+                    tmem_st_wait();
+                }
+                // z as bf16 hi (element 0) and lo (element 1): the two denominator columns of NUM
+                const float zf = __uint_as_float(zr);
+                const uint32_t zh = pack_bf16(zf, 0.f);
+                *reinterpret_cast<uint32_t*>(sZb + sw128_offset(r, 0)) =
+                    (zh & 0xFFFFu) | (pack_bf16(zf - __uint_as_float(zh << 16), 0.f) << 16);
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_snap);
+                if (warp == kAWarp0 && lane == 0) SCAN_TRACE(t, 14);
+            }
+        }
+        (void)failed;
+    } else {
+        // ---------------- O team: 4 warps ----------------
+        const int ow = warp - kOWarp0;
+        const int q = warp & 3;
+        const int r = q * 32 + lane;  // query row of NUM
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        const int owner = r / RP;
+        const bool mine = owner == rank;
+        bool failed = false;
+        for (int tt = 0; tt < T; ++tt) {
+            failed |= !mbar_wait(&bar_num, tt & 1, &abort_flag);
+            if (warp == kOWarp0 && lane == 0) SCAN_TRACE(tt, 15);
+            __syncwarp();
+            tc_fence_after();
+            // NUM in two loads: the second half with the denominator first (converted to its output
+            // form, and for the rows this CTA finalises also parked in the spare TMEM columns), then the
+            // first half, after which NUM is released; at most one half is held as fp32.
+            const uint32_t na = tbase + lane_off + kColNum;
+            const bool any_mine = CS > 1 && __any_sync(0xffffffffu, mine);
+            uint32_t v[32], d0, d1, w1[16];
+            tmem_ld32(na + 32, v);
+            tmem_ld1(na + 64, d0);
+            tmem_ld1(na + 65, d1);
+            tmem_ld_wait();
+            const float den_own = __uint_as_float(d0) + __uint_as_float(d1);
+            const float inv_own = den_own > 0.f ? 1.f / den_own : 0.f;
+            auto pack_y = [&](float a0, float a1) -> uint32_t {
+                if (CS == 1) return pack_bf16(a0, a1);  // the output itself
+                __half2 h2 = __floats2half2_rn(a0, a1);  // a partial y for the row's owner
+                return *reinterpret_cast<uint32_t*>(&h2);
+            };
+#pragma unroll
+            for (int k = 0; k < 16; ++k) w1[k] = pack_y(__uint_as_float(v[2 * k]) * inv_own, __uint_as_float(v[2 * k + 1]) * inv_own);
+            if (any_mine) tmem_st32(tbase + lane_off + kColSpare, v);
+            tmem_ld32(na, v);
+            tmem_ld_wait();
+            const int i_tok = tt * kTile + r;
+            const bool valid = i_tok < p.n;
+            float e_own = 0.f;
+            if (exp_kind && CS > 1) {
+                failed |= !mbar_wait(&bar_cq[tt & 1], (tt >> 1) & 1, &abort_flag);
+                failed |= !mbar_wait(&bar_beta[tt & 3], (tt >> 2) & 1, &abort_flag);
+                e_own = sCq[(tt & 1) * 128 + r] + sBeta[tt & 3];
+            }
+            __syncwarp();
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_numfree);  // NUM may take the next tile's inter MMA
+            if (warp == kOWarp0 && lane == 0) SCAN_TRACE(tt, 16);
+            if (CS == 1) {
+                if (valid) {
+                    uint4* dst = reinterpret_cast<uint4*>(p.Y + ((size_t)bh * p.n + i_tok) * kD);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        dst[c] = make_uint4(pack_y(__uint_as_float(v[8 * c + 0]) * inv_own, __uint_as_float(v[8 * c + 1]) * inv_own),
+                                            pack_y(__uint_as_float(v[8 * c + 2]) * inv_own, __uint_as_float(v[8 * c + 3]) * inv_own),
+                                            pack_y(__uint_as_float(v[8 * c + 4]) * inv_own, __uint_as_float(v[8 * c + 5]) * inv_own),
+                                            pack_y(__uint_as_float(v[8 * c + 6]) * inv_own, __uint_as_float(v[8 * c + 7]) * inv_own));
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) dst[4 + c] = make_uint4(w1[4 * c], w1[4 * c + 1], w1[4 * c + 2], w1[4 * c + 3]);
+                }
+            } else {
+                if (!mine) {
+                    // y = num / den of this CTA's features (fp16: a convex combination of the values, so
+                    // bounded by them), den and e, to the CTA that finalises the row
+                    failed |= !mbar_wait_cluster(&bar_xfree, (tt & 1) ^ 1, &abort_flag);
+                    const int slot = rank < owner ? rank : rank - 1;
+                    const uint32_t ca = mapa(smem_u32(sX + ((size_t)slot * RP + (r - owner * RP)) * kXRow), owner);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        st_cluster_v4(ca + 16 * c,
+                                      make_uint4(pack_y(__uint_as_float(v[8 * c + 0]) * inv_own, __uint_as_float(v[8 * c + 1]) * inv_own),
+                                                 pack_y(__uint_as_float(v[8 * c + 2]) * inv_own, __uint_as_float(v[8 * c + 3]) * inv_own),
+                                                 pack_y(__uint_as_float(v[8 * c + 4]) * inv_own, __uint_as_float(v[8 * c + 5]) * inv_own),
+                                                 pack_y(__uint_as_float(v[8 * c + 6]) * inv_own, __uint_as_float(v[8 * c + 7]) * inv_own)));
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) st_cluster_v4(ca + 64 + 16 * c, make_uint4(w1[4 * c], w1[4 * c + 1], w1[4 * c + 2], w1[4 * c + 3]));
+                    st_cluster_v2(ca + 128, __float_as_uint(den_own), __float_as_uint(e_own));
+                }
+                __syncwarp();
+                for (int o = 0; o < CS; ++o) {
+                    if (o == rank) continue;
+                    if (__any_sync(0xffffffffu, owner == o) && lane == 0) mbar_arrive_cluster(mapa(smem_u32(&bar_xfull), o));
+                }
+                if (mine) {
+                    // weights 2^(e - max e) over the cluster's partials, peers in rank order; a row's
+                    // result is sum_g w_g num_g / sum_g w_g den_g
+                    failed |= !mbar_wait_cluster(&bar_xfull, tt & 1, &abort_flag);
+                    if (warp == kOWarp0 && lane == 0) SCAN_TRACE(tt, 17);
+                    const uint8_t* rowx = sX + (size_t)(r - rank * RP) * kXRow;
+                    float E = e_own;
+                    for (int sl = 0; sl < CS - 1; ++sl)
+                        E = fmaxf(E, *reinterpret_cast<const float*>(rowx + (size_t)sl * RP * kXRow + 132));
+                    const float wo = exp_kind ? ex2(e_own - E) : 1.f;
+                    float wsum = wo * den_own, wd[kMaxCluster - 1];
+#pragma unroll
+                    for (int sl = 0; sl < kMaxCluster - 1; ++sl) {
+                        wd[sl] = 0.f;
+                        if (sl < CS - 1) {
+                            const uint8_t* src = rowx + (size_t)sl * RP * kXRow;
+                            wd[sl] = (exp_kind ? ex2(*reinterpret_cast<const float*>(src + 132) - E) : 1.f) *
+                                     *reinterpret_cast<const float*>(src + 128);
+                            wsum += wd[sl];
+                        }
+                    }
+                    const float inv = 1.f / wsum;
+                    if (valid) {
+                        uint4* dst = reinterpret_cast<uint4*>(p.Y + ((size_t)bh * p.n + i_tok) * kD);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            float acc[8];
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) acc[k] = __uint_as_float(v[8 * c + k]) * wo;
+                            for (int sl = 0; sl < CS - 1; ++sl) {
+                                const uint4 hv = *reinterpret_cast<const uint4*>(rowx + (size_t)sl * RP * kXRow + 16 * c);
+                                const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+#pragma unroll
+                                for (int k = 0; k < 4; ++k) {
+                                    const float2 y2 = __half22float2(*reinterpret_cast<const __half2*>(&hw[k]));
+                                    acc[2 * k] = fmaf(wd[sl], y2.x, acc[2 * k]);
+                                    acc[2 * k + 1] = fmaf(wd[sl], y2.y, acc[2 * k + 1]);
+                                }
+                            }
+                            dst[c] = make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
+                                                pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
+                        }
+                    }
+                }
+                // the second half of the own rows, from the spare columns
+                __syncwarp();
+                if (__any_sync(0xffffffffu, mine)) {
+                    uint32_t u1[32];
+                    tmem_ld32(tbase + lane_off + kColSpare, u1);
+                    tmem_ld_wait();
+                    if (mine && valid) {
+                        const uint8_t* rowx = sX + (size_t)(r - rank * RP) * kXRow;
+                        float E = e_own;
+                        for (int sl = 0; sl < CS - 1; ++sl)
+                            E = fmaxf(E, *reinterpret_cast<const float*>(rowx + (size_t)sl * RP * kXRow + 132));
+                        const float wo = exp_kind ? ex2(e_own - E) : 1.f;
+                        float wsum = wo * den_own, wd[kMaxCluster - 1];
+#pragma unroll
+                        for (int sl = 0; sl < kMaxCluster - 1; ++sl) {
+                            wd[sl] = 0.f;
+                            if (sl < CS - 1) {
+                                const uint8_t* src = rowx + (size_t)sl * RP * kXRow;
+                                wd[sl] = (exp_kind ? ex2(*reinterpret_cast<const float*>(src + 132) - E) : 1.f) *
+                                         *reinterpret_cast<const float*>(src + 128);
+                                wsum += wd[sl];
+                            }
+                        }
+                        const float inv = 1.f / wsum;
+                        uint4* dst = reinterpret_cast<uint4*>(p.Y + ((size_t)bh * p.n + i_tok) * kD + 32);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            float acc[8];
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) acc[k] = __uint_as_float(u1[8 * c + k]) * wo;
+                            for (int sl = 0; sl < CS - 1; ++sl) {
+                                const uint4 hv = *reinterpret_cast<const uint4*>(rowx + (size_t)sl * RP * kXRow + 64 + 16 * c);
+                                const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+#pragma unroll
+                                for (int k = 0; k < 4; ++k) {
+                                    const float2 y2 = __half22float2(*reinterpret_cast<const __half2*>(&hw[k]));
+                                    acc[2 * k] = fmaf(wd[sl], y2.x, acc[2 * k]);
+                                    acc[2 * k + 1] = fmaf(wd[sl], y2.y, acc[2 * k + 1]);
+                                }
+                            }
+                            dst[c] = make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
+                                                pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
+                        }
+                    }
+                }
+                // every row of the receive buffer has been read: the peers may send the next tile
+                named_bar(3, 32 * kOWarps);
+                if (ow == 0 && lane == 0)
+                    for (int o = 0; o < CS; ++o)
+                        if (o != rank) mbar_arrive_cluster(mapa(smem_u32(&bar_xfree), o));
+            }
+            if (warp == kOWarp0 && lane == 0) SCAN_TRACE(tt, 18);
+        }
+        (void)failed;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 512);
+    }
+    cluster_sync();  // no CTA leaves while a peer may still write into its shared memory
+}
+
+}  // namespace tcs
+}  // namespace favor

@@ -37,7 +37,7 @@ def test_status_strings_and_kernel_names():
     for code in range(7):
         assert favor.lib.favor_status_string(code).decode().startswith("FAVOR_")
     assert favor.KERNEL_NAMES[0] == "features"
-    assert favor.KERNEL_NAMES[-1] == "omega"
+    assert favor.KERNEL_NAMES[-1] == "exact"
 
 
 def test_workspace_sizes():

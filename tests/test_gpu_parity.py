@@ -69,6 +69,85 @@ def test_attention_small_cases(favor, dtype, causal, kind, n, d, m):
     assert_close_attn(f64(Y), ref, dtype, f"{dtype} causal={causal} {kind} n={n} d={d} m={m}")
 
 
+# Every feature-group count of the causal tensor-core scan (clusters of 1 to 4 CTAs, the last one
+# partly padding when m is not a multiple of 128) and every non-causal tensor-core path: the fused
+# single launch (n <= 1024, d = 64), the state / combine / readout kernels beyond it (ReLU and exp,
+# d = 64 and 128), and the CUDA-core kernels bf16 falls back to at d = 128 with m > 256.
+SCAN_CASES = [(kind, n, m) for kind in ("exp", "relu") for m in (64, 128, 192, 256, 320, 384, 448, 512)
+              for n in (130, 515)]
+
+
+@pytest.mark.parametrize("kind,n,m", SCAN_CASES)
+def test_causal_scan_feature_groups(favor, kind, n, m):
+    w = si.Workload("case", 1, 3, n, 64, m, "bf16", True, kind=kind, seed=31 + n + m, omega_seed=7 + m)
+    Q, K, V, Om, om64 = device_inputs(w)
+    Y = run_attn(favor, w, Q, K, V, Om)
+    assert favor.last_device_error() == 0
+    ref = oracle_attn(w, f64(Q), f64(K), f64(V), om64)
+    assert_close_attn(f64(Y), ref, "bf16", f"causal {kind} n={n} m={m}")
+
+
+NONCAUSAL_PATH_CASES = (
+    [("relu", n, d, m) for n in (1025, 1500, 4099) for d in (64, 128) for m in (128, 256)]
+    + [("exp", n, 64, 256) for n in (1025, 4096)]
+    + [("exp", 700, 128, m) for m in (320, 384, 448, 512)]
+    + [("relu", 700, 128, 512)]
+)
+
+
+@pytest.mark.parametrize("kind,n,d,m", NONCAUSAL_PATH_CASES)
+def test_noncausal_paths(favor, kind, n, d, m):
+    w = si.Workload("case", 1, 2, n, d, m, "bf16", False, kind=kind, seed=41 + n + d, omega_seed=9 + m)
+    Q, K, V, Om, om64 = device_inputs(w)
+    Y = run_attn(favor, w, Q, K, V, Om)
+    assert favor.last_device_error() == 0
+    ref = oracle_attn(w, f64(Q), f64(K), f64(V), om64)
+    assert_close_attn(f64(Y), ref, "bf16", f"non-causal {kind} n={n} d={d} m={m}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("n", [200, 1500])
+def test_large_norm_inputs_stay_finite(favor, causal, n):
+    """Queries and keys five times the workloads' scale (|q| about 40 at d = 64): every exponent
+    stabiliser must follow the real largest exponent, not a norm bound far above it, or all of a
+    row's features underflow and num / den becomes 0 / 0."""
+    w = si.Workload("case", 1, 2, n, 64, 256, "bf16", causal, seed=57 + n, omega_seed=58)
+    Q, K, V, Om, om64 = device_inputs(w)
+    Q5 = (Q.float() * 5).to(Q.dtype).contiguous()
+    K5 = (K.float() * 5).to(K.dtype).contiguous()
+    Y = run_attn(favor, w, Q5, K5, V, Om)
+    assert favor.last_device_error() == 0
+    assert torch.isfinite(Y.float()).all()
+    ref = oracle_attn(w, f64(Q5), f64(K5), f64(V), om64)
+    assert_close_attn(f64(Y), ref, "bf16", f"x5 inputs causal={causal} n={n}")
+
+
+@pytest.mark.parametrize("n,d,m,dtype", [(1000, 64, 256, "bf16"), (3000, 64, 256, "bf16"), (3000, 128, 256, "bf16"),
+                                         (700, 128, 512, "bf16"), (700, 64, 256, "f32")])
+def test_noncausal_on_poisoned_workspace(favor, n, d, m, dtype):
+    """The caller's workspace holds NaN before the call (fused, three-kernel and CUDA-core paths):
+    nothing in it may be read before the call itself has written it."""
+    w = si.Workload("case", 1, 3, n, d, m, dtype, False, seed=71 + n, omega_seed=72)
+    Q, K, V, Om, om64 = device_inputs(w)
+    nb = favor.workspace_bytes("noncausal", w.B, w.H, n, d, m, torch_dtype(w))
+    ws = torch.full((max(nb, 4) // 4,), float("nan"), dtype=torch.float32, device=Q.device)
+    Y = favor.favor_attn_noncausal(Q, K, V, Om, workspace=ws.view(torch.uint8))
+    assert favor.last_device_error() == 0
+    ref = oracle_attn(w, f64(Q), f64(K), f64(V), om64)
+    assert_close_attn(f64(Y), ref, dtype, f"poisoned workspace n={n} d={d} m={m} {dtype}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_grid_limit_heads(favor, causal):
+    """B*H = 65535 heads (the largest count the non-causal calls take) of one token each."""
+    w = si.Workload("case", 1, 65535, 1, 64, 64, "bf16", causal, seed=61, omega_seed=62)
+    Q, K, V, Om, om64 = device_inputs(w)
+    Y = run_attn(favor, w, Q, K, V, Om)
+    assert favor.last_device_error() == 0
+    ref = oracle_attn(w, f64(Q), f64(K), f64(V), om64)
+    assert_close_attn(f64(Y), ref, "bf16", f"65535 heads causal={causal}")
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("kind,stab", [("exp", "row"), ("exp", "head"), ("exp", "none"), ("relu", "row")])
 @pytest.mark.parametrize("n,d,m", [(1, 64, 64), (77, 64, 256), (300, 128, 256), (129, 64, 512)])

@@ -13,6 +13,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import seeded_inputs as si
 from tests.helpers import assert_close_attn, device_inputs
 
@@ -37,13 +38,15 @@ def _noalloc_c_call(favor, Q, K, V, Om, Y, w):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_noalloc_matches_workspace_entry_point_twice(favor, dtype):
-    cases = [si.Workload("noalloc_a", 1, 8, 1024, 64, 256, dtype, False, seed=501, omega_seed=502),
-             si.Workload("noalloc_b", 2, 3, 777, 128, 192, dtype, False, seed=503, omega_seed=504)]
+    # The d = 128 case runs first and fills the scratch; the fused (n <= 1024, d = 64) case then runs
+    # on what it left behind. Each call is checked against the workspace entry point and the oracle.
+    cases = [si.Workload("noalloc_b", 2, 3, 777, 128, 192, dtype, False, seed=503, omega_seed=504),
+             si.Workload("noalloc_a", 1, 8, 1024, 64, 256, dtype, False, seed=501, omega_seed=502)]
     for w in cases:  # two calls in a row; the second reuses scratch the first one filled
         assert favor.workspace_bytes("noncausal", w.B, w.H, w.n, w.d, w.m,
                                      torch.bfloat16 if dtype == "bf16" else torch.float32) \
             <= favor.NOALLOC_SCRATCH_BYTES
-        Q, K, V, Om, _ = device_inputs(w)
+        Q, K, V, Om, om64 = device_inputs(w)
         ref = favor.favor_attn_noncausal(Q, K, V, Om)
         Y = torch.full_like(Q, float("nan"))
         assert _noalloc_c_call(favor, Q, K, V, Om, Y, w) == 0
@@ -51,6 +54,9 @@ def test_noalloc_matches_workspace_entry_point_twice(favor, dtype):
         assert favor.last_device_error() == 0
         got = Y.float().cpu().numpy().astype(np.float64)
         assert_close_attn(got, ref.float().cpu().numpy().astype(np.float64), dtype, f"noalloc {w.name}")
+        f64 = lambda t: t.float().cpu().numpy().astype(np.float64)  # noqa: E731
+        oref = oracle.attn_noncausal(f64(Q), f64(K), f64(V), om64, kind=w.kind, relu_eps=w.relu_eps)
+        assert_close_attn(got, oref, dtype, f"noalloc {w.name} vs oracle")
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(favor):
