@@ -360,7 +360,7 @@ favor_status_t tc_noncausal(const void* Q, const void* K, const void* V, const v
     const float eps_s = eps * std::sqrt((float)m);
     const int groups = w.m_pad / 128;
 
-    tcnc::StateParams sp{n, w.m_pad, groups, w.tokens_per_split, kind, eps_s, sc, pS, pz, pst};
+    tcnc::StateParams sp{n, m, w.m_pad, groups, w.tokens_per_split, kind, eps_s, sc, pS, pz, pst};
     const size_t smem_state = tcnc::StateSmem<D>::bytes(groups);
     auto kstate = tcnc::nc_state_tc<D>;
     FAVOR_TRY(set_smem(kstate, smem_state));

@@ -3,7 +3,7 @@
 // One thread-block cluster per head, one CTA per 128-token tile. Each CTA
 //   1. projects its key tile with the features on the TMEM lanes, turns U^T into phi(K)^T in place
 //      and accumulates its partial S = phi(K)^T V (tcgen05, A from TMEM) and z (per-lane sums), with
-//      a key stabiliser of its own (12 nats below the tile's largest bound W |k^| - |k^|^2 / 2);
+//      a key stabiliser of its own (the tile's exact largest exponent w_r . k^_j - |k^_j|^2 / 2);
 //   2. writes the partial (fp32, straight from TMEM), its z and its stabiliser to the workspace in
 //      global memory (L2) and arrives on a cluster barrier; while the barrier completes it projects
 //      its query tile (tokens on the lanes) and forms phi(Q) in place with the exact row stabiliser;
@@ -11,22 +11,22 @@
 //      rank order, each rescaled to the cluster's largest stabiliser, writes the bf16 rows into its
 //      own copy of the readout MMA's operand (swizzled, MN-major) and bulk-copies that contiguous
 //      block into every peer (completing on the peer's mbarrier); z it sums for all rows itself and
-//      stores as a bf16 hi + lo pair in two extra operand columns;
+//      stores as a bf16 hi + lo pair in two extra operand columns; for the exp family the rounding
+//      remainder of S (S - bf16(S), itself in bf16) goes the same way in a second operand;
 //   4. once the peers' blocks have landed, takes [num | den] = phi(Q) [S | z_hi + z_lo] in one MMA
-//      (N = 64 + 16) and stores Y = num / den.
+//      chain (N = 64 + 16), adds phi(Q) S_lo (exp family) and stores Y = num / den.
 // Distributed shared memory carries only the bf16 rows (per SM its bandwidth is far below L2's), in
 // bulk copies of whole row blocks.
 #pragma once
 
 #include "tc.cuh"
-#include "tc_noncausal.cuh"  // ex2, kStabSlackLo, tile_row_sqnorm, phi_col
+#include "tc_noncausal.cuh"  // ex2, tile_row_sqnorm, phi_col
 
 namespace favor {
 namespace tcfu {
 
 using namespace favor::tc;
 using tcnc::ex2;
-using tcnc::kStabSlackLo;
 using tcnc::tile_row_sqnorm;
 
 constexpr int kTile = 128;
@@ -59,7 +59,7 @@ struct FusedSmem {
     // Omega (m_pad x 128 B), K, V, Q tiles, the readout's B operand (two 64-column MN regions of
     // m_pad x 128 B: S, then z_hi, z_lo and zeros), per-key constants, row-max exchange.
     static size_t bytes(int m_pad) {
-        return 1024 + (size_t)m_pad * 128 + 3 * kTileBytes + 2 * (size_t)m_pad * 128 + 128 * 4 + 4 * 128 * 4;
+        return 1024 + (size_t)m_pad * 128 + 3 * kTileBytes + 3 * (size_t)m_pad * 128 + 128 * 4 + 4 * 128 * 4;
     }
 };
 
@@ -75,7 +75,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sV = sK + kTileBytes;
     uint8_t* sQ = sV + kTileBytes;
     uint8_t* sS = sQ + kTileBytes;                         // bf16 [S | z] operand, 2 x MP x 128 B
-    float* sC = reinterpret_cast<float*>(sS + 2 * (size_t)MP * 128);  // [128] per-key constants
+    uint8_t* sSlo = sS + 2 * (size_t)MP * 128;             // bf16 S - bf16(S) operand, MP x 128 B
+    float* sC = reinterpret_cast<float*>(sSlo + (size_t)MP * 128);  // [128] per-key constants
     float* sMax = sC + 128;                                // [4][128] row-max shares
     __shared__ uint64_t bar_load, bar_q, bar_u, bar_phi, bar_s, bar_pq, bar_phiq, bar_num, bar_own, bar_img;
     __shared__ uint32_t tmem_base;
@@ -105,8 +106,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bar_own, kEpiWarps);
         mbar_init(&bar_img, 1);
         fence_mbar_init();
-        // the peers' rows of the operand arrive by bulk copies (after the first cluster barrier)
-        mbar_arrive_expect_tx(&bar_img, (uint32_t)(MP - own_rows) * 128);
+        // the peers' rows of the operand (and of the remainder, exp family) arrive by bulk copies
+        // (after the first cluster barrier)
+        mbar_arrive_expect_tx(&bar_img, (uint32_t)(MP - own_rows) * 128 * (p.kind == kKindExp ? 2u : 1u));
         // the loads start before the TMEM allocation and the CTA barrier
         tma_prefetch_desc(&mQ);
         tma_prefetch_desc(&mK);
@@ -189,34 +191,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- key side ----------------
         failed |= !mbar_wait(&bar_load, 0, &abort_flag);
         __syncwarp();
-        // warps 1..4 own the tile's 128 keys (|k^|^2); warps 5..16 take the row norms of Omega for
-        // W = the largest of them (identical in every CTA of the cluster)
-        float kn2 = 0.f;
+        // warps 1..4 own the tile's 128 keys: the per-key part of the exponent, |k^|^2 / 2 (binary
+        // orders of magnitude), +inf for keys past n
         if (ew < 4) {
-            if (exp_kind) kn2 = p.scale * p.scale * tile_row_sqnorm<64>(sK, r);
-        } else if (exp_kind) {
-            float w2 = 0.f;
-            for (int row = (ew - 4) * 32 + lane; row < MP; row += 32 * (kEpiWarps - 4))
-                w2 = fmaxf(w2, tile_row_sqnorm<64>(sOm + (size_t)(row >> 7) * 16384, row & 127));
-            w2 = warp_max(w2);
-            if (lane == 0) red[ew] = w2;
+            const float kn2 = exp_kind ? p.scale * p.scale * tile_row_sqnorm<64>(sK, r) : 0.f;
+            sC[r] = r < nvalid ? 0.5f * kn2 * kLog2e : INFINITY;
         }
-        named_bar(1, 32 * kEpiWarps);
-        if (ew < 4) {  // the tile's stabiliser: largest bound W |k^| - |k^|^2 / 2 over its valid keys
-            float W = 0.f;
-            if (exp_kind) {
-                float m2 = 0.f;
-#pragma unroll
-                for (int i = 4; i < kEpiWarps; ++i) m2 = fmaxf(m2, red[i]);
-                W = sqrtf(m2);
-            }
-            const float b = r < nvalid ? W * sqrtf(kn2) - 0.5f * kn2 : -INFINITY;
-            const float bm = warp_max(b);
-            if (lane == 0) red[ew] = bm;
-        }
-        named_bar(1, 32 * kEpiWarps);
-        const float stab = exp_kind ? fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])) - kStabSlackLo : 0.f;
-        if (ew < 4) sC[r] = r < nvalid ? (exp_kind ? (0.5f * kn2 + stab) * kLog2e : 0.f) : INFINITY;
         named_bar(1, 32 * kEpiWarps);
         // phi^T for group tm (team of 8 warps), tokens [64 cg, 64 cg + 64) of the tile
         const int tm = ew / 8, cg = (ew % 8) >> 2;
@@ -224,12 +204,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         failed |= !mbar_wait(&bar_u, 0, &abort_flag);
         __syncwarp();
         tc_fence_after();
+        uint32_t v[64];
         if (tm < G) {
             const uint32_t ua = tbase + lane_off + 256 + 128 * tm + 64 * cg;
-            uint32_t v[64];
             tmem_ld32(ua, *reinterpret_cast<uint32_t(*)[32]>(v));
             tmem_ld32(ua + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
             tmem_ld_wait();
+        }
+        // The tile's key stabiliser: the exact largest exponent w_r . k^_j - |k^_j|^2 / 2 over its
+        // valid keys and real features (the tile's largest key feature is then 1).
+        float stab = 0.f;  // binary orders of magnitude
+        if (exp_kind) {
+            float mx = -INFINITY;
+            if (tm < G && tm * 128 + r < p.m) {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) mx = fmaxf(mx, fmaf(__uint_as_float(v[i]), A2, -sC[64 * cg + i]));
+            }
+            mx = warp_max(mx);
+            if (lane == 0) red[ew] = mx;
+            named_bar(1, 32 * kEpiWarps);
+            stab = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < kEpiWarps; ++i) stab = fmaxf(stab, red[i]);
+        }
+        const bool real_feat = tm * 128 + r < p.m;  // padding features get phi = 0
+        if (tm < G) {
+            const uint32_t ua = tbase + lane_off + 256 + 128 * tm + 64 * cg;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const float* cj = sC + 64 * cg + 32 * hh;
@@ -239,12 +239,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float a0 = __uint_as_float(v[32 * hh + i]), a1 = __uint_as_float(v[32 * hh + i + 1]);
                     float f0, f1;
                     if (exp_kind) {
-                        f0 = ex2(fmaf(a0, A2, -cj[i]));
-                        f1 = ex2(fmaf(a1, A2, -cj[i + 1]));
+                        f0 = ex2(fmaf(a0, A2, -(cj[i] + stab)));
+                        f1 = ex2(fmaf(a1, A2, -(cj[i + 1] + stab)));
                     } else {
                         f0 = cj[i] == 0.f ? phi_plain(a0 * p.scale, p.kind, 1.f, p.relu_eps_s) : 0.f;
                         f1 = cj[i + 1] == 0.f ? phi_plain(a1 * p.scale, p.kind, 1.f, p.relu_eps_s) : 0.f;
                     }
+                    if (!real_feat) f0 = f1 = 0.f;
                     zpart += f0 + f1;
                     pk[i / 2] = pack_bf16(f0, f1);
                 }
@@ -272,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                          __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3])));
             __stcg(p.Zp + ((size_t)(bh * T + rank) * 2 + cg) * MP + feat, zpart);
         }
-        if (ew == 0 && lane == 0) __stcg(p.Stab + bh * kMaxCluster + rank, stab);
+        if (ew == 0 && lane == 0) __stcg(p.Stab + bh * kMaxCluster + rank, stab / kLog2e);
         tc_fence_before();
         __syncwarp();
     }
@@ -375,8 +376,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) acc[k] = 0.f;
             }
-            *reinterpret_cast<uint2*>(sS + sw128_offset(row, c4 >> 1) + 8 * (c4 & 1)) =
-                make_uint2(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]));
+            const uint32_t off = sw128_offset(row, c4 >> 1) + 8 * (c4 & 1);
+            const uint2 hi = make_uint2(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]));
+            *reinterpret_cast<uint2*>(sS + off) = hi;
+            if (exp_kind)
+                *reinterpret_cast<uint2*>(sSlo + off) =
+                    make_uint2(pack_bf16(acc[0] - __uint_as_float(hi.x << 16), acc[1] - __uint_as_float(hi.x & 0xFFFF0000u)),
+                               pack_bf16(acc[2] - __uint_as_float(hi.y << 16), acc[3] - __uint_as_float(hi.y & 0xFFFF0000u)));
         }
         if (fz < MP) {
             weights();
@@ -397,9 +403,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the owned rows are one contiguous block of the operand: copy it into every peer
             const uint32_t off = (uint32_t)own_lo * 128;
             for (int c = 0; c < T; ++c)
-                if (c != rank)
+                if (c != rank) {
                     bulk_copy_to_peer(mapa(smem_u32(sS + off), c), sS + off, (uint32_t)own_rows * 128,
                                       mapa(smem_u32(&bar_img), c));
+                    if (exp_kind)
+                        bulk_copy_to_peer(mapa(smem_u32(sSlo + off), c), sSlo + off, (uint32_t)own_rows * 128,
+                                          mapa(smem_u32(&bar_img), c));
+                }
         }
         __syncwarp();
     }
@@ -415,6 +425,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int ks = 0; ks < MP / 16; ++ks) {
                     uint64_t bd = sdesc_sw128(smem_u32(sS + ks * 2048), (uint32_t)MP * 128, 1024);
                     mma_ts(tbase, tbase + 256 + ks * 8, bd, id_n, ks > 0);
+                }
+                if (p.kind == kKindExp) {
+                    constexpr uint32_t id_lo = idesc_bf16(128, kD, false, true);
+                    for (int ks = 0; ks < MP / 16; ++ks) {
+                        uint64_t bd = sdesc_sw128(smem_u32(sSlo + ks * 2048), 16, 1024);
+                        mma_ts(tbase, tbase + 256 + ks * 8, bd, id_lo, 1u);
+                    }
                 }
             }
             mma_commit(&bar_num);

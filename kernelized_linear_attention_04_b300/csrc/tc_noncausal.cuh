@@ -14,11 +14,13 @@
 //                 cores, num = phi(Q) S on the tensor cores, Y = num / den stored in whole sectors.
 //
 // Stabilisers. A query row may use any constant of its own and a head's keys any one constant:
-// both cancel between numerator and denominator. Queries use their exact row maximum. Keys use
-// the bound  u_r(k) <= W |k^| - |k^|^2 / 2  (Cauchy-Schwarz, W = largest row norm of Omega), held
-// per CTA as a running value that only moves (with a rescale of the accumulated S and z) when a
-// tile's bound exceeds it by more than kStabSlackHi; the common factor 1/sqrt(m) is dropped on both
-// sides for the same reason.
+// both cancel between numerator and denominator. Queries use their exact row maximum. Keys use a
+// running constant per CTA that follows the exact largest key exponent of the tiles already
+// reduced (known two tiles late), and is never less than the bound
+// u_r(k) <= W |k^| - |k^|^2 / 2 (Cauchy-Schwarz, W = largest row norm of Omega) of the current
+// tile minus kStabGuard, so that no feature can overflow before its tile's maximum is known; each
+// move rescales the accumulated S and z. The common factor 1/sqrt(m) is dropped on both sides for
+// the same reason.
 #pragma once
 
 #include "tc.cuh"
@@ -32,8 +34,10 @@ constexpr int kTile = 128;            // tokens per tile (the MMA M or N extent)
 constexpr int kEpiWarps = 16;         // four column groups x four TMEM lane quarters
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kThreads = 64 + kEpiThreads;  // warp 0: TMA, warp 1: MMA, then the epilogue warps
-constexpr float kStabSlackLo = 12.f;  // after a (re)set, the key stabiliser sits this far below the bound
-constexpr float kStabSlackHi = 24.f;  // ... and is raised once a tile's bound exceeds it by this much
+constexpr float kStabSlackHi = 24.f;  // the key constant is raised once a key exponent exceeds it by this much
+constexpr float kStabGuard = 60.f;    // ... and never lies further than this below the current tile's bound
+constexpr float kStabSlackDown = 40.f;  // ... lowered once the keys seen so far all lie this far below it
+constexpr float kStabStepDown = 20.f;   // ... by at most this much per tile
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -78,6 +82,7 @@ __device__ __forceinline__ float tile_row_sqnorm(const uint8_t* tile, int row) {
 // =============================================================================================
 struct StateParams {
     int n;              // tokens per head
+    int m;              // features
     int m_pad;          // features, padded to a multiple of 128
     int groups;         // 128-feature groups handled by this CTA (1..4, D=128: 1..2)
     int tokens_per_split;
@@ -140,6 +145,8 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     // on a slot barrier could: a team that does not use a slot may be two of its phases behind).
     __shared__ uint64_t bar_rs, bar_sdone;
     __shared__ float sF[2];  // per-tile rescale factor of the accumulated state (1 = none)
+    __shared__ float sStabT[2];                       // the key stabiliser of tile t (slot t & 1), nats
+    __shared__ float sUnitMax[4][kStateEpiWarps];     // per epilogue warp: exact largest key exponent of tile t (slot t & 3)
     __shared__ float sRed[2][kStateNormWarps];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
@@ -312,7 +319,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
             for (int i = 0; i < kStateNormWarps; ++i) m2 = fmaxf(m2, sRed[1][i]);
             W = sqrtf(m2);
         }
-        float stab = 0.f;
+        float stab = 0.f, run = -INFINITY;  // run: exact largest key exponent of the tiles reported so far
         for (int t = 0; t < T; ++t) {
             const int st = t % NK, b2 = t & 1;
             ok &= mbar_wait(&bar_nempty[b2], ((t >> 1) & 1) ^ 1, &abort_flag);
@@ -339,19 +346,36 @@ __global__ void __launch_bounds__(kStateThreads, 1)
                 float Bt = -INFINITY;
 #pragma unroll
                 for (int i = 0; i < kStateNormWarps; ++i) Bt = fmaxf(Bt, sRed[b2][i]);
-                if (t == 0) {
-                    stab = Bt - kStabSlackLo;
-                } else if (Bt > stab + kStabSlackHi) {
-                    const float nst = Bt - kStabSlackLo;
-                    f = ex2((stab - nst) * kLog2e);
-                    stab = nst;
+                // The constant follows the exact largest key exponent of the tiles seen so far (from
+                // the epilogue, two tiles behind): raised to it once it is exceeded by kStabSlackHi,
+                // lowered towards it by at most kStabStepDown per tile once it lies kStabSlackDown
+                // below (the unreported tile t-1 sits below e^kStabGuard before that step, so it
+                // stays finite after it). The bound keeps every feature of tile t below
+                // e^kStabGuard at all times.
+                if (t >= 2) {
+#pragma unroll
+                    for (int i = 0; i < kStateEpiWarps; ++i) run = fmaxf(run, sUnitMax[(t - 2) & 3][i]);
                 }
+                const float guard = Bt - kStabGuard;
+                float nst = stab;
+                if (t == 0) {
+                    nst = guard;
+                } else {
+                    if (run > nst + kStabSlackHi) nst = run;
+                    else if (run > -INFINITY && run < nst - kStabSlackDown) nst = fmaxf(run, nst - kStabStepDown);
+                    if (guard > nst) nst = guard;
+                    if (nst != stab) f = ex2((stab - nst) * kLog2e);
+                }
+                stab = nst;
             }
 #pragma unroll
             for (int i = 0; i < 2; ++i)
                 sC[b2 * 128 + nw * 64 + lane + 32 * i] =
                     v2[i] ? (p.kind == kKindExp ? (h2[i] + stab) * kLog2e : 0.f) : INFINITY;
-            if (nw == 0 && lane == 0) sF[b2] = f;
+            if (nw == 0 && lane == 0) {
+                sF[b2] = f;
+                sStabT[b2] = stab;
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_nfull[b2]);
         }
@@ -408,9 +432,12 @@ __global__ void __launch_bounds__(kStateThreads, 1)
                 named_bar(1, 32 * kStateEpiWarps);  // both teams' parts are rescaled before any phi of tile t
             }
             const float* cj = sC + b2 * 128 + 64 * cg;
+            const float stab_t = sStabT[b2];
+            float umax = -INFINITY;  // exact largest key exponent of the units this warp handles (log2, relative)
             for (int g = 0; g < G; ++g) {
                 const int u = t * UPT + g;
                 if ((u & 1) != tm) continue;
+                const bool real_feat = f0 + g * 128 + r < p.m;
                 const int s = u % kStateSlots;
                 failed |= !mbar_wait(&bar_ufull[s], (u / kStateSlots) & 1, &abort_flag);
                 __syncwarp();
@@ -436,6 +463,11 @@ __global__ void __launch_bounds__(kStateThreads, 1)
                             f[1] = ex2(fmaf(__uint_as_float(vv[i + 1]), A2, -c4.y));
                             f[2] = ex2(fmaf(__uint_as_float(vv[i + 2]), A2, -c4.z));
                             f[3] = ex2(fmaf(__uint_as_float(vv[i + 3]), A2, -c4.w));
+                            if (real_feat)
+                                umax = fmaxf(fmaxf(umax, fmaxf(fmaf(__uint_as_float(vv[i + 0]), A2, -c4.x),
+                                                               fmaf(__uint_as_float(vv[i + 1]), A2, -c4.y))),
+                                             fmaxf(fmaf(__uint_as_float(vv[i + 2]), A2, -c4.z),
+                                                   fmaf(__uint_as_float(vv[i + 3]), A2, -c4.w)));
                         } else {
                             f[0] = c4.x == 0.f ? phi_plain(__uint_as_float(vv[i + 0]) * p.scale, p.kind, 1.f, p.relu_eps_s) : 0.f;
                             f[1] = c4.y == 0.f ? phi_plain(__uint_as_float(vv[i + 1]) * p.scale, p.kind, 1.f, p.relu_eps_s) : 0.f;
@@ -457,6 +489,10 @@ __global__ void __launch_bounds__(kStateThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar_phi[s]);
+            }
+            if (p.kind == kKindExp) {  // for the key constant two tiles on (nats, absolute)
+                umax = warp_max(umax);
+                if (lane == 0) sUnitMax[t & 3][ew] = umax == -INFINITY ? -INFINITY : umax / kLog2e + stab_t;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_nempty[b2]);
