@@ -117,10 +117,13 @@ favor_status_t favor_attn_noncausal(const void* Q, const void* K, const void* V,
  *   y_i = phi(q_i)^T S_i / phi(q_i)^T z_i,  S_i = sum_{j<=i} phi(k_j) v_j^T,  z_i = sum_{j<=i} phi(k_j).
  * Computed as a chunked scan: per chunk, an intra-chunk lower-triangular block plus the carried
  * prefix state. chunk: 0 (implementation default), 64 or 128; the result does not depend on it
- * beyond rounding. bf16 with d = 64 and m <= 512 runs a tensor-core scan (pipelined over tiles
- * for m <= 256), which carries the state every 128 tokens and masks j <= i inside each 128-token
- * tile (two 64-token chunks give exactly that sum); other inputs run on CUDA cores in 16-token
- * steps. Shapes and dtypes as above. Workspace: 0 bytes on the tensor-core scans.
+ * beyond rounding. bf16 with d = 64 and m <= 512 runs a tensor-core scan, one CTA per 128-feature
+ * group and a thread-block cluster of ceil(m / 128) CTAs per head, which carries the state every
+ * 128 tokens and masks j <= i inside each 128-token tile (two 64-token chunks give exactly that
+ * sum); other inputs run on CUDA cores in 16-token steps. Shapes and dtypes as above. Workspace
+ * (favor_workspace_bytes): 0 bytes for m <= 128; for m > 128 the CTAs of a head exchange their
+ * partial output rows through it (B*H * 4 * ceil(m/128) * 18432 bytes; its contents on entry
+ * do not matter).
  */
 favor_status_t favor_attn_causal(const void* Q, const void* K, const void* V, const void* Omega, void* Y,
                                  int B, int H, int n, int d, int m, int chunk, favor_dtype_t dt,

@@ -195,6 +195,8 @@ size_t noncausal_ws_bytes(int B, int H, int n, int d, int m, favor_dtype_t dt) {
 // The tensor-core causal scan takes bf16 with d = 64 and m <= 512: one 128-feature group per CTA, a
 // cluster of ceil(m / 128) CTAs per head.
 bool tc_causal_ok(int d, int m, favor_dtype_t dt) { return dt == FAVOR_BF16 && d == 64 && m_padded(m) <= 512; }
+// With a cluster, the ring of partial rows the CTAs of a head combine through (L2-resident).
+size_t tc_causal_ws_bytes(int B, int H, int m) { return tcs::ScanWs::bytes((size_t)B * H, m_padded(m) / 128); }
 
 size_t causal_ws_bytes(int B, int H, int d, int m) {
     const size_t BH = (size_t)B * H;
@@ -402,15 +404,17 @@ favor_status_t tc_noncausal(const void* Q, const void* K, const void* V, const v
 }
 
 favor_status_t tc_causal(const void* Q, const void* K, const void* V, const void* Om, void* Y, int B, int H, int n,
-                         int m, int kind, float eps, cudaStream_t s) {
+                         int m, int kind, float eps, void* ws, cudaStream_t s) {
     const int BH = B * H;
     const int cs = m_padded(m) / 128;
     CUtensorMap mQ, mK, mV, mOm;
     if (!tma::encode_bf16_3d(&mQ, Q, 64, n, BH, 64, tcs::kTile) || !tma::encode_bf16_3d(&mK, K, 64, n, BH, 64, tcs::kTile) ||
         !tma::encode_bf16_3d(&mV, V, 64, n, BH, 64, tcs::kTile) || !tma::encode_bf16_2d(&mOm, Om, 64, m, 64, 128))
         return FAVOR_ERR_CUDA;
-    tcs::ScanParams sp{n, m, kind, eps * std::sqrt((float)m), feat_scale(64, kind), static_cast<__nv_bfloat16*>(Y)};
-    const size_t smem = tcs::ScanSmem::bytes(cs);
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+    tcs::ScanParams sp{n, m, kind, eps * std::sqrt((float)m), feat_scale(64, kind), static_cast<__nv_bfloat16*>(Y),
+                       cs > 1 ? wsb : nullptr};
+    const size_t smem = tcs::ScanSmem::bytes();
     auto kern = kind == kKindExp ? tcs::causal_scan<kKindExp> : kind == kKindRelu ? tcs::causal_scan<kKindRelu> : tcs::causal_scan<kKindElu>;
     FAVOR_TRY(set_smem(kern, smem));
     cudaLaunchConfig_t cfg = {};
@@ -574,7 +578,7 @@ size_t favor_workspace_bytes(favor_op_t op, int B, int H, int n, int d, int m, f
         case FAVOR_OP_NONCAUSAL: return noncausal_ws_bytes(B, H, n, d, m, dt);
         case FAVOR_OP_CAUSAL:
             if (chunk != 0 && chunk != 64 && chunk != 128) return (size_t)-1;
-            return tc_causal_ok(d, m, dt) ? 0 : causal_ws_bytes(B, H, d, m);
+            return tc_causal_ok(d, m, dt) ? tc_causal_ws_bytes(B, H, m) : causal_ws_bytes(B, H, d, m);
     }
     return (size_t)-1;
 }
@@ -624,7 +628,10 @@ favor_status_t favor_attn_causal(const void* Q, const void* K, const void* V, co
     if (!heads_ok(B, H, kMaxHeads)) return FAVOR_ERR_UNSUPPORTED;
     if (kind == FAVOR_ELU && !(Omega = eye_ptr(d, dt))) return FAVOR_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (tc_causal_ok(d, m, dt)) return tc_causal(Q, K, V, Omega, Y, B, H, n, m, (int)kind, relu_eps, s);
+    if (tc_causal_ok(d, m, dt)) {
+        FAVOR_TRY(check_ws(workspace, ws_bytes, tc_causal_ws_bytes(B, H, m)));
+        return tc_causal(Q, K, V, Omega, Y, B, H, n, m, (int)kind, relu_eps, workspace, s);
+    }
     FAVOR_TRY(check_ws(workspace, ws_bytes, causal_ws_bytes(B, H, d, m)));
     return FAVOR_DISPATCH(dt, d, simt_causal, Q, K, V, Omega, Y, B, H, n, m, (int)kind, relu_eps, workspace, s);
 }

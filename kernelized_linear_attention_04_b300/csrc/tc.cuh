@@ -125,6 +125,38 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
     }
 }
 
+// Orders this thread's earlier memory accesses before its later ones for all threads of the cluster.
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------------------------
+// Counters in global memory shared by the CTAs of a cluster: a release increment after the data it
+// publishes, and a bounded acquire wait for a count (like mbar_wait: false on expiry or abort).
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ bool counter_wait(const unsigned* p, unsigned target, volatile int* abort_flag) {
+    if (ld_acquire(p) >= target) return true;
+    const uint64_t t0 = globaltimer();
+    const uint64_t tlim = g_favor_test_wait_ns;
+    const uint64_t limit = tlim ? tlim : kWaitLimitNs;
+    for (uint32_t it = 1;; ++it) {
+        if (ld_acquire(p) >= target) return true;
+        if ((it & 15u) != 0) continue;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > limit) {
+            atomicOr(&g_favor_error, kDevErrTimeout);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------------------------
 // Thread-block clusters: rank, distributed shared memory, remote arrivals, cluster barrier
 // ---------------------------------------------------------------------------------------------
@@ -352,6 +384,14 @@ __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+// log2(x) for x > 0 (lg2.approx on x scaled into the normal range first, so that subnormal x keep
+// their value); -inf for x = 0.
+__device__ __forceinline__ float log2_pos(float x) {
+    const bool sub = x < 0x1p-100f;
+    float y;
+    asm("lg2.approx.f32 %0, %1;" : "=f"(y) : "f"(sub ? x * 0x1p64f : x));
+    return sub ? y - 64.f : y;
 }
 __device__ __forceinline__ uint32_t exp_pair(uint32_t a0, uint32_t a1, float A2, float c) {
     float x0 = __uint_as_float(a0), x1 = __uint_as_float(a1);

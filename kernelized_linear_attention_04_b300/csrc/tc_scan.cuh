@@ -9,8 +9,10 @@
 // and then S_<t+1 = S_<t + Phi(K_t)^T V_t, z_<t+1 = z_<t + Phi(K_t)^T 1 ("Performer for vision",
 // *How It Works*, Step 2: prefix sums; the state is carried every 128 tokens and keys are masked
 // by j <= i inside the tile, which for two 64-token chunks is exactly their chunked prefix sum).
-// The CTAs of a cluster then add their partial results row by row through distributed shared
-// memory.
+// The CTAs of a cluster then combine their partial results row by row: each writes its partial
+// rows of tile t into a ring of kRing tiles in global memory (L2-resident) and signals the rows'
+// owners through their mbarriers a tile later; a separate warp team of each CTA combines the rows
+// it finalises, so that neither the tensor-core pipeline nor the NUM drain waits on a peer.
 //
 // Every contraction runs on the tensor cores, with the A operand in TMEM wherever it is produced
 // there:
@@ -36,7 +38,8 @@
 //                and, read transposed, the state's A operand); the running key stabiliser.
 //   warps 14-17  A team: SC -> A~ (masked by j <= i, bf16) in place; then the bf16 image of
 //                [S | z] after the state update (rescaled first if the key stabiliser rose).
-//   warps 18-21  O team: NUM -> y, with the cluster exchange.
+//   warps 18-21  O team: NUM -> y (alone: the output; in a cluster: the partial rows, to the ring).
+//   warps 22-25  X team (cluster only): the rows this CTA finalises, from the ring's partials.
 //
 // Stabilisers (exp family; Y does not depend on them, both cancel between num and den):
 //   queries: c_i = the exact largest w_r . q^_i over the CTA's features (the row's largest feature
@@ -44,8 +47,8 @@
 //   keys: a running constant per CTA, the exact largest exponent w_r . k^_j - |k^_j|^2/2 seen so
 //   far over the CTA's features and the head's keys, raised (and the state rescaled) only when a
 //   tile exceeds it by more than kSlackHi binary orders of magnitude;
-//   across the cluster, each CTA's partial row carries its exponent offset e = c_i + beta; the
-//   owner of the row weights the partials by 2^(e - max e).
+//   across the cluster, each CTA's partial row y_g = num_g / den_g carries the log-weight
+//   l_g = log2(den_g) + c_i + beta; the owner of the row weights the partials by 2^(l_g - max l).
 // The common factor 1/sqrt(m) is dropped. The generalized-ReLU and elu + 1 families have no
 // stabiliser.
 #pragma once
@@ -69,10 +72,12 @@ constexpr int kQWarp0 = 2, kQWarps = 8;
 constexpr int kKWarp0 = kQWarp0 + kQWarps, kKWarps = 4;
 constexpr int kAWarp0 = kKWarp0 + kKWarps, kAWarps = 4;
 constexpr int kOWarp0 = kAWarp0 + kAWarps, kOWarps = 4;
-constexpr int kThreads = 32 * (kOWarp0 + kOWarps);  // 704
+constexpr int kXWarp0 = kOWarp0 + kOWarps, kXWarps = 4;
+constexpr int kThreads = 32 * (kXWarp0 + kXWarps);  // 832
 constexpr int kTileBytes = kTile * kD * 2;          // 16 KB: [128 x 64] bf16
 constexpr int kPhiBytes = kTile * 128 * 2;          // 32 KB: [128 tokens x 128 features] bf16
-constexpr int kXRow = 144;                          // bytes per row of the cluster exchange: 64 fp16 y, den, e
+constexpr int kRing = 4;                            // tiles of partial rows in flight per head
+constexpr int kXChunks = 9;                         // 16-byte chunks of a partial row: 8 of y (fp16), log-weight and scales
 constexpr float kSlackHi = 16.f;                    // key stabiliser rises once exceeded by 2^16
 
 // Timeline of one CTA for profiling builds (compiled with -DFAVOR_SCAN_TRACE): the SM clock at
@@ -93,7 +98,6 @@ constexpr uint32_t kColS = 0;      // [S | z]: 64 columns of S, z in column 64, 
 constexpr uint32_t kColPQ = 80;    // phi(Q) packed bf16: 128 features in 64 columns
 constexpr uint32_t kColNum = 144;  // NUM: 64 numerator columns, denominator parts in columns 64, 65
 constexpr uint32_t kColR0 = 224;   // two 128-column regions: P_K(t), then P_Q(t), then SC(t) / A~(t)
-constexpr uint32_t kColSpare = 480;  // 32 columns: second half of an owner's NUM rows during the exchange
 
 // Shared memory offsets from the 1024-aligned base.
 constexpr uint32_t kOffOm = 0;
@@ -107,7 +111,7 @@ constexpr uint32_t kOffSlo = kOffZb + kTileBytes;       // S rounding remainder 
 constexpr uint32_t kOffOnes = kOffSlo + kTileBytes;     // element 0 of each token row = 1
 constexpr uint32_t kOffCq = kOffOnes + kTileBytes;      // [2][128] f32 query row constants
 constexpr uint32_t kOffMx = kOffCq + 2 * 128 * 4;       // [2][2][128] f32 row-max halves
-constexpr uint32_t kOffX = kOffMx + 2 * 2 * 128 * 4;    // cluster exchange receive buffer
+constexpr uint32_t kOffEnd = kOffMx + 2 * 2 * 128 * 4;
 
 struct ScanParams {
     int n;
@@ -116,19 +120,27 @@ struct ScanParams {
     float relu_eps_s;  // relu_eps * sqrt(m): the features are scaled by sqrt(m) (a common factor)
     float scale;       // d^-1/4 (1 for elu + 1)
     __nv_bfloat16* Y;
+    uint8_t* ring;     // cluster > 1: per head kRing x CS x kXChunks x 128 rows x 16 bytes (ScanWs)
 };
 
 struct ScanSmem {
-    static int rows_per_owner(int cs) { return (kTile + cs - 1) / cs; }
-    static size_t x_bytes(int cs) { return cs > 1 ? (size_t)(cs - 1) * rows_per_owner(cs) * kXRow : 0; }
-    static size_t bytes(int cs) { return 1024 + kOffX + x_bytes(cs); }
+    static size_t bytes() { return 1024 + kOffEnd; }
 };
 
-// Number of O-team warps (32 rows each) holding at least one row of owner `o`.
-__device__ __forceinline__ int owner_warps(int o, int rp) {
+// Workspace of the scan: the ring of partial rows (only for a cluster).
+struct ScanWs {
+    static size_t bytes(size_t BH, int cs) { return cs > 1 ? BH * kRing * cs * kXChunks * kTile * 16 : 0; }
+};
+
+// Whether O-team warp q (rows 32 q .. 32 q + 31) holds rows that CTA o finalises (rows o rp ..).
+__host__ __device__ __forceinline__ bool warp_feeds(int q, int o, int rp) {
+    const int lo = o * rp, hi = min(kTile, lo + rp) - 1;
+    return lo <= 32 * q + 31 && 32 * q <= hi;
+}
+__device__ __forceinline__ int feeding_warps(int o, int rp) {
     int c = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) c += ((32 * q) / rp <= o && o <= (32 * q + 31) / rp) ? 1 : 0;
+    for (int q = 0; q < 4; ++q) c += warp_feeds(q, o, rp) ? 1 : 0;
     return c;
 }
 
@@ -167,11 +179,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sOnes = smem + kOffOnes;
     float* sCq = reinterpret_cast<float*>(smem + kOffCq);
     float* sMx = reinterpret_cast<float*>(smem + kOffMx);
-    uint8_t* sX = smem + kOffX;
     __shared__ uint64_t bar_om, bar_kfull, bar_kfree, bar_qfull, bar_qfree, bar_vfull[2], bar_vfree[2];
     __shared__ uint64_t bar_pk[2], bar_pkfree[2], bar_pq[2], bar_phq, bar_phk[2], bar_phkfree[2];
     __shared__ uint64_t bar_sc, bar_atil, bar_st, bar_snap, bar_num, bar_numfree, bar_beta[4], bar_cq[2];
-    __shared__ uint64_t bar_xfull, bar_xfree, bar_drain;
+    __shared__ uint64_t bar_drain, bar_rfull[kRing], bar_rfree[kRing];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     __shared__ float sBeta[4], sF[4], sKmx[4];
@@ -232,9 +243,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bar_snap, kAWarps);
         mbar_init(&bar_num, 1);
         mbar_init(&bar_numfree, kOWarps);
-        mbar_init(&bar_xfull, CS > 1 ? (CS - 1) * owner_warps(rank, RP) : 1);
-        mbar_init(&bar_xfree, CS > 1 ? CS - 1 : 1);
         mbar_init(&bar_drain, 1);
+        for (int i = 0; i < kRing; ++i) {
+            // a slot's partial rows of this CTA's rows: one arrive per feeding warp of every CTA
+            mbar_init(&bar_rfull[i], CS * feeding_warps(rank, RP));
+            // this CTA's slot has been read by every CTA of the cluster
+            mbar_init(&bar_rfree[i], CS);
+        }
         fence_mbar_init();
     }
     // Constant operands: the ones column of [V | 1] (element 0 of every token row), and the initial
@@ -653,189 +668,202 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         (void)failed;
-    } else {
+    } else if (warp < kXWarp0) {
         // ---------------- O team: 4 warps ----------------
-        const int ow = warp - kOWarp0;
         const int q = warp & 3;
         const int r = q * 32 + lane;  // query row of NUM
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        const int owner = r / RP;
-        const bool mine = owner == rank;
         bool failed = false;
+        // This CTA's part of the head's ring: [slot][rank][chunk][row] x 16 bytes.
+        uint8_t* ring = CS > 1 ? p.ring + (size_t)bh * kRing * CS * kXChunks * kTile * 16 : nullptr;
+        // The partial rows of tile tp are complete: each lane's stores are released, then every
+        // CTA that finalises rows of this warp is signalled.
+        auto publish = [&](int tp) {
+            fence_acq_rel_cluster();
+            __syncwarp();
+            if (lane == 0)
+                for (int o = 0; o < CS; ++o)
+                    if (warp_feeds(q, o, RP)) mbar_arrive_cluster(mapa(smem_u32(&bar_rfull[tp % kRing]), o));
+        };
         for (int tt = 0; tt < T; ++tt) {
+            const int slot = tt % kRing, use = tt / kRing;
+            const int i_tok = tt * kTile + r;
+            // where this row's results go: the output row (alone), or its partial record in the ring
+            uint8_t* rec = CS > 1 ? ring + ((size_t)(slot * CS + rank) * kXChunks) * kTile * 16 + r * 16 : nullptr;
+            uint4* yrow = reinterpret_cast<uint4*>(p.Y + ((size_t)bh * p.n + i_tok) * kD);
+            const bool store = CS > 1 || i_tok < p.n;
+            // the slot's previous tile has been read by every CTA of the cluster
+            if (CS > 1 && use > 0) failed |= !mbar_wait_cluster(&bar_rfree[slot], (use - 1) & 1, &abort_flag);
+            if (warp == kOWarp0 && lane == 0) SCAN_TRACE(tt, 23);
             failed |= !mbar_wait(&bar_num, tt & 1, &abort_flag);
             if (warp == kOWarp0 && lane == 0) SCAN_TRACE(tt, 15);
             __syncwarp();
             tc_fence_after();
-            // NUM in two loads: the second half with the denominator first (converted to its output
-            // form, and for the rows this CTA finalises also parked in the spare TMEM columns), then the
-            // first half, after which NUM is released; at most one half is held as fp32.
+            // NUM in two halves (the second with the denominator first); y = num / den of this CTA's
+            // features. Alone, the bf16 output row; in a cluster, fp16 times a power-of-two scale per
+            // half row (so that any bf16 value range survives), the partial row for its owner.
             const uint32_t na = tbase + lane_off + kColNum;
-            const bool any_mine = CS > 1 && __any_sync(0xffffffffu, mine);
-            uint32_t v[32], d0, d1, w1[16];
+            uint32_t v[32], d0, d1;
             tmem_ld32(na + 32, v);
             tmem_ld1(na + 64, d0);
             tmem_ld1(na + 65, d1);
             tmem_ld_wait();
+            // the previous tile's partial rows (stored an iteration ago) go to their owners first,
+            // so that the release does not wait for this tile's stores
+            if (CS > 1 && tt > 0) publish(tt - 1);
             const float den_own = __uint_as_float(d0) + __uint_as_float(d1);
-            const float inv_own = den_own > 0.f ? 1.f / den_own : 0.f;
-            auto pack_y = [&](float a0, float a1) -> uint32_t {
-                if (CS == 1) return pack_bf16(a0, a1);  // the output itself
-                __half2 h2 = __floats2half2_rn(a0, a1);  // a partial y for the row's owner
-                return *reinterpret_cast<uint32_t*>(&h2);
-            };
+            // y = num / den; a den below 2^-64 (keys far below the stabiliser) is scaled by 2^64 first,
+            // so that 1 / den stays finite
+            const bool tiny = den_own < 0x1p-64f;
+            const float inv_own = den_own > 0.f ? 1.f / (tiny ? den_own * 0x1p64f : den_own) : 0.f;
+            // one half row (32 values in v) -> four 16-byte chunks at chunk c0; returns its scale
+            auto put_half = [&](int c0) -> float {
+                uint32_t w[16];
+                float sc = 1.f, pw = 1.f;
+                if (CS > 1) {
+                    float mx = 0.f;
 #pragma unroll
-            for (int k = 0; k < 16; ++k) w1[k] = pack_y(__uint_as_float(v[2 * k]) * inv_own, __uint_as_float(v[2 * k + 1]) * inv_own);
-            if (any_mine) tmem_st32(tbase + lane_off + kColSpare, v);
+                    for (int k = 0; k < 32; ++k) mx = fmaxf(mx, fabsf(__uint_as_float(v[k])));
+                    mx = (tiny ? mx * 0x1p64f : mx) * inv_own;
+                    // 2^ex with mx 2^-ex in [2^14, 2^15) (from the IEEE exponent field; clamped so
+                    // that all factors stay finite): fp16 keeps 11 bits of every value of the half
+                    const int ex = mx > 0.f ? max(-60, min(113, (int)((__float_as_uint(mx) >> 23) & 0xFFu) - 127 - 14)) : 0;
+                    sc = __uint_as_float((uint32_t)(ex + 127) << 23);
+                    pw = __uint_as_float((uint32_t)(127 - ex) << 23);
+                }
+                const float f = inv_own * pw;
+                auto yv = [&](uint32_t x) { return tiny ? (__uint_as_float(x) * 0x1p64f) * inv_own * pw : __uint_as_float(x) * f; };
+                if (CS == 1) {
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) w[k] = pack_bf16(yv(v[2 * k]), yv(v[2 * k + 1]));
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        __half2 h2 = __floats2half2_rn(yv(v[2 * k]), yv(v[2 * k + 1]));
+                        w[k] = *reinterpret_cast<uint32_t*>(&h2);
+                    }
+                }
+                if (store) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 o = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+                        if (CS == 1) yrow[c0 + c] = o;
+                        else __stcg(reinterpret_cast<uint4*>(rec + (c0 + c) * kTile * 16), o);
+                    }
+                }
+                return sc;
+            };
+            const float sc1 = put_half(4);
             tmem_ld32(na, v);
-            tmem_ld_wait();
-            const int i_tok = tt * kTile + r;
-            const bool valid = i_tok < p.n;
+            // the row's exponent offset: read before NUM is released, which lets the Q and K teams
+            // move on to the tiles that reuse these slots
             float e_own = 0.f;
             if (exp_kind && CS > 1) {
                 failed |= !mbar_wait(&bar_cq[tt & 1], (tt >> 1) & 1, &abort_flag);
                 failed |= !mbar_wait(&bar_beta[tt & 3], (tt >> 2) & 1, &abort_flag);
                 e_own = sCq[(tt & 1) * 128 + r] + sBeta[tt & 3];
             }
-            __syncwarp();
-            tmem_st_wait();
+            tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_numfree);  // NUM may take the next tile's inter MMA
             if (warp == kOWarp0 && lane == 0) SCAN_TRACE(tt, 16);
-            if (CS == 1) {
-                if (valid) {
-                    uint4* dst = reinterpret_cast<uint4*>(p.Y + ((size_t)bh * p.n + i_tok) * kD);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        dst[c] = make_uint4(pack_y(__uint_as_float(v[8 * c + 0]) * inv_own, __uint_as_float(v[8 * c + 1]) * inv_own),
-                                            pack_y(__uint_as_float(v[8 * c + 2]) * inv_own, __uint_as_float(v[8 * c + 3]) * inv_own),
-                                            pack_y(__uint_as_float(v[8 * c + 4]) * inv_own, __uint_as_float(v[8 * c + 5]) * inv_own),
-                                            pack_y(__uint_as_float(v[8 * c + 6]) * inv_own, __uint_as_float(v[8 * c + 7]) * inv_own));
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) dst[4 + c] = make_uint4(w1[4 * c], w1[4 * c + 1], w1[4 * c + 2], w1[4 * c + 3]);
-                }
-            } else {
-                if (!mine) {
-                    // y = num / den of this CTA's features (fp16: a convex combination of the values, so
-                    // bounded by them), den and e, to the CTA that finalises the row
-                    failed |= !mbar_wait_cluster(&bar_xfree, (tt & 1) ^ 1, &abort_flag);
-                    const int slot = rank < owner ? rank : rank - 1;
-                    const uint32_t ca = mapa(smem_u32(sX + ((size_t)slot * RP + (r - owner * RP)) * kXRow), owner);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        st_cluster_v4(ca + 16 * c,
-                                      make_uint4(pack_y(__uint_as_float(v[8 * c + 0]) * inv_own, __uint_as_float(v[8 * c + 1]) * inv_own),
-                                                 pack_y(__uint_as_float(v[8 * c + 2]) * inv_own, __uint_as_float(v[8 * c + 3]) * inv_own),
-                                                 pack_y(__uint_as_float(v[8 * c + 4]) * inv_own, __uint_as_float(v[8 * c + 5]) * inv_own),
-                                                 pack_y(__uint_as_float(v[8 * c + 6]) * inv_own, __uint_as_float(v[8 * c + 7]) * inv_own)));
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) st_cluster_v4(ca + 64 + 16 * c, make_uint4(w1[4 * c], w1[4 * c + 1], w1[4 * c + 2], w1[4 * c + 3]));
-                    st_cluster_v2(ca + 128, __float_as_uint(den_own), __float_as_uint(e_own));
-                }
-                __syncwarp();
-                for (int o = 0; o < CS; ++o) {
-                    if (o == rank) continue;
-                    if (__any_sync(0xffffffffu, owner == o) && lane == 0) mbar_arrive_cluster(mapa(smem_u32(&bar_xfull), o));
-                }
-                if (mine) {
-                    // weights 2^(e - max e) over the cluster's partials, peers in rank order; a row's
-                    // result is sum_g w_g num_g / sum_g w_g den_g
-                    failed |= !mbar_wait_cluster(&bar_xfull, tt & 1, &abort_flag);
-                    if (warp == kOWarp0 && lane == 0) SCAN_TRACE(tt, 17);
-                    const uint8_t* rowx = sX + (size_t)(r - rank * RP) * kXRow;
-                    float E = e_own;
-                    for (int sl = 0; sl < CS - 1; ++sl)
-                        E = fmaxf(E, *reinterpret_cast<const float*>(rowx + (size_t)sl * RP * kXRow + 132));
-                    const float wo = exp_kind ? ex2(e_own - E) : 1.f;
-                    float wsum = wo * den_own, wd[kMaxCluster - 1];
-#pragma unroll
-                    for (int sl = 0; sl < kMaxCluster - 1; ++sl) {
-                        wd[sl] = 0.f;
-                        if (sl < CS - 1) {
-                            const uint8_t* src = rowx + (size_t)sl * RP * kXRow;
-                            wd[sl] = (exp_kind ? ex2(*reinterpret_cast<const float*>(src + 132) - E) : 1.f) *
-                                     *reinterpret_cast<const float*>(src + 128);
-                            wsum += wd[sl];
-                        }
-                    }
-                    const float inv = 1.f / wsum;
-                    if (valid) {
-                        uint4* dst = reinterpret_cast<uint4*>(p.Y + ((size_t)bh * p.n + i_tok) * kD);
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            float acc[8];
-#pragma unroll
-                            for (int k = 0; k < 8; ++k) acc[k] = __uint_as_float(v[8 * c + k]) * wo;
-                            for (int sl = 0; sl < CS - 1; ++sl) {
-                                const uint4 hv = *reinterpret_cast<const uint4*>(rowx + (size_t)sl * RP * kXRow + 16 * c);
-                                const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
-#pragma unroll
-                                for (int k = 0; k < 4; ++k) {
-                                    const float2 y2 = __half22float2(*reinterpret_cast<const __half2*>(&hw[k]));
-                                    acc[2 * k] = fmaf(wd[sl], y2.x, acc[2 * k]);
-                                    acc[2 * k + 1] = fmaf(wd[sl], y2.y, acc[2 * k + 1]);
-                                }
-                            }
-                            dst[c] = make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
-                                                pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
-                        }
-                    }
-                }
-                // the second half of the own rows, from the spare columns
-                __syncwarp();
-                if (__any_sync(0xffffffffu, mine)) {
-                    uint32_t u1[32];
-                    tmem_ld32(tbase + lane_off + kColSpare, u1);
-                    tmem_ld_wait();
-                    if (mine && valid) {
-                        const uint8_t* rowx = sX + (size_t)(r - rank * RP) * kXRow;
-                        float E = e_own;
-                        for (int sl = 0; sl < CS - 1; ++sl)
-                            E = fmaxf(E, *reinterpret_cast<const float*>(rowx + (size_t)sl * RP * kXRow + 132));
-                        const float wo = exp_kind ? ex2(e_own - E) : 1.f;
-                        float wsum = wo * den_own, wd[kMaxCluster - 1];
-#pragma unroll
-                        for (int sl = 0; sl < kMaxCluster - 1; ++sl) {
-                            wd[sl] = 0.f;
-                            if (sl < CS - 1) {
-                                const uint8_t* src = rowx + (size_t)sl * RP * kXRow;
-                                wd[sl] = (exp_kind ? ex2(*reinterpret_cast<const float*>(src + 132) - E) : 1.f) *
-                                         *reinterpret_cast<const float*>(src + 128);
-                                wsum += wd[sl];
-                            }
-                        }
-                        const float inv = 1.f / wsum;
-                        uint4* dst = reinterpret_cast<uint4*>(p.Y + ((size_t)bh * p.n + i_tok) * kD + 32);
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            float acc[8];
-#pragma unroll
-                            for (int k = 0; k < 8; ++k) acc[k] = __uint_as_float(u1[8 * c + k]) * wo;
-                            for (int sl = 0; sl < CS - 1; ++sl) {
-                                const uint4 hv = *reinterpret_cast<const uint4*>(rowx + (size_t)sl * RP * kXRow + 64 + 16 * c);
-                                const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
-#pragma unroll
-                                for (int k = 0; k < 4; ++k) {
-                                    const float2 y2 = __half22float2(*reinterpret_cast<const __half2*>(&hw[k]));
-                                    acc[2 * k] = fmaf(wd[sl], y2.x, acc[2 * k]);
-                                    acc[2 * k + 1] = fmaf(wd[sl], y2.y, acc[2 * k + 1]);
-                                }
-                            }
-                            dst[c] = make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
-                                                pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
-                        }
-                    }
-                }
-                // every row of the receive buffer has been read: the peers may send the next tile
-                named_bar(3, 32 * kOWarps);
-                if (ow == 0 && lane == 0)
-                    for (int o = 0; o < CS; ++o)
-                        if (o != rank) mbar_arrive_cluster(mapa(smem_u32(&bar_xfree), o));
+            const float sc0 = put_half(0);
+            if (CS > 1) {
+                // the row's log-weight: log2(den) plus its exponent offset (-inf: no weight)
+                const float l_own = den_own > 0.f ? log2_pos(den_own) + e_own : -INFINITY;
+                __stcg(reinterpret_cast<uint4*>(rec + 8 * kTile * 16),
+                       make_uint4(__float_as_uint(l_own), __float_as_uint(sc0), __float_as_uint(sc1), 0u));
             }
             if (warp == kOWarp0 && lane == 0) SCAN_TRACE(tt, 18);
         }
+        if (CS > 1 && T > 0) publish(T - 1);
         (void)failed;
+    } else {
+        // ---------------- X team: 4 warps (cluster only) ----------------
+        // The rows [rank RP, rank RP + rows) of each tile from the CS partial rows in the ring: a
+        // row's result is sum_g w_g y_g / sum_g w_g with w_g = 2^(l_g - max l), l_g = log2(den_g) + e_g
+        // (y_g = num_g / den_g as stored, times its power-of-two scale). TPR threads per row, each
+        // taking 8 / TPR consecutive 16-byte chunks of it.
+        if (CS > 1) {
+            const int xt = threadIdx.x - 32 * kXWarp0;
+            const uint8_t* ring = p.ring + (size_t)bh * kRing * CS * kXChunks * kTile * 16;
+            const int row0 = rank * RP, rows = min(RP, kTile - row0);
+            bool failed = false;
+            // one pass: 32 rows, four threads per row with two 16-byte chunks each; returns whether
+            // the thread has output (two chunks in out, for the row at dst)
+            auto combine_pass = [&](int tc, int item, uint4 (&out)[2], uint4*& dst) -> bool {
+                constexpr int NC = kMaxCluster;  // partials past CS carry no weight
+                const int slot = tc % kRing;
+                const int row = row0 + item / 4, c0 = (item % 4) * 2;
+                const int tok = tc * kTile + row;
+                if (!(item < rows * 4 && tok < p.n)) return false;
+                uint4 meta[NC], yv[NC][2];
+#pragma unroll
+                for (int g = 0; g < NC; ++g) {
+                    if (g >= CS) {  // log-weight -inf
+                        meta[g] = make_uint4(0xFF800000u, 0u, 0u, 0u);
+                        yv[g][0] = yv[g][1] = make_uint4(0u, 0u, 0u, 0u);
+                        continue;
+                    }
+                    const uint8_t* rec = ring + ((size_t)(slot * CS + g) * kXChunks) * kTile * 16 + row * 16;
+                    meta[g] = __ldcg(reinterpret_cast<const uint4*>(rec + 8 * kTile * 16));
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) yv[g][k] = __ldcg(reinterpret_cast<const uint4*>(rec + (c0 + k) * kTile * 16));
+                }
+                float L = -INFINITY;
+#pragma unroll
+                for (int g = 0; g < NC; ++g) L = fmaxf(L, __uint_as_float(meta[g].x));
+                float ws[NC], wsum = 0.f;
+#pragma unroll
+                for (int g = 0; g < NC; ++g) {
+                    const float w = L > -INFINITY ? ex2(__uint_as_float(meta[g].x) - L) : 0.f;  // the largest is 1
+                    wsum += w;
+                    ws[g] = w * __uint_as_float(c0 < 4 ? meta[g].y : meta[g].z);
+                }
+                const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int g = 0; g < NC; ++g) {
+                        const uint32_t hw[4] = {yv[g][k].x, yv[g][k].y, yv[g][k].z, yv[g][k].w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 y2 = __half22float2(*reinterpret_cast<const __half2*>(&hw[e]));
+                            acc[2 * e] = fmaf(ws[g], y2.x, acc[2 * e]);
+                            acc[2 * e + 1] = fmaf(ws[g], y2.y, acc[2 * e + 1]);
+                        }
+                    }
+                    out[k] = make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
+                                        pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
+                }
+                dst = reinterpret_cast<uint4*>(p.Y + ((size_t)bh * p.n + tok) * kD + 8 * c0);
+                return true;
+            };
+            // rows <= 64: at most two passes
+            auto combine = [&](int tc) {
+                uint4 o0[2], o1[2];
+                uint4 *d0 = nullptr, *d1 = nullptr;
+                const bool h0 = combine_pass(tc, xt, o0, d0);
+                const bool h1 = rows * 4 > 32 * kXWarps && combine_pass(tc, xt + 32 * kXWarps, o1, d1);
+                // every thread of the team has consumed its loads: the slot is free for its writers'
+                // next use. The outputs are stored after the release, which then has no stores of
+                // this tile to wait for.
+                named_bar(4, 32 * kXWarps);
+                if (xt == 0)
+                    for (int o = 0; o < CS; ++o) mbar_arrive_cluster(mapa(smem_u32(&bar_rfree[tc % kRing]), o));
+                if (h0) { d0[0] = o0[0]; d0[1] = o0[1]; }
+                if (h1) { d1[0] = o1[0]; d1[1] = o1[1]; }
+            };
+            for (int tc = 0; tc < T; ++tc) {
+                failed |= !mbar_wait_cluster(&bar_rfull[tc % kRing], (tc / kRing) & 1, &abort_flag);
+                if (warp == kXWarp0 && lane == 0) SCAN_TRACE(tc, 17);
+                combine(tc);
+                if (warp == kXWarp0 && lane == 0) SCAN_TRACE(tc, 25);
+            }
+            (void)failed;
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -843,7 +871,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tbase, 512);
     }
-    cluster_sync();  // no CTA leaves while a peer may still write into its shared memory
+    cluster_sync();  // the cluster's CTAs leave together
 }
 
 }  // namespace tcs

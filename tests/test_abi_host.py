@@ -72,9 +72,12 @@ def test_workspace_sizes_per_path():
     assert favor.workspace_bytes("noncausal", 1, 8, 100, 64, 256, bf) == up(BH * mp * 256) + up(BH * 2 * mp * 4) + up(BH * 32)
     # longer sequences run the three-kernel path, whose workspace does not grow with n beyond the splits
     assert favor.workspace_bytes("noncausal", 1, 8, 4096, 64, 256, bf) > 0
-    # the tensor-core causal scans keep the state in TMEM: no workspace
-    for m in (64, 192, 256, 384, 512):
+    # the tensor-core causal scans keep the state in TMEM; with more than 128 features the CTAs of a
+    # head combine their partial rows through a ring of 4 tiles x CS CTAs x 9 x 128 rows x 16 bytes
+    for m in (64, 128):
         assert favor.workspace_bytes("causal", 4, 16, 8192, 64, m, bf) == 0
+    for m, cs in ((192, 2), (256, 2), (384, 3), (512, 4)):
+        assert favor.workspace_bytes("causal", 4, 16, 8192, 64, m, bf) == 64 * 4 * cs * 9 * 128 * 16
     # streaming decode state: fp32 S [BH][m][d], z [BH][m], stabilisers [BH][m/64], block partials
     # [BH][m/64][d+2], u32 counter [BH]; 256-byte pieces
     up = lambda b: (b + 255) // 256 * 256
