@@ -78,8 +78,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 // Waits for phase `parity` of `bar` to complete. Returns false (after flagging the error and the
 // CTA abort word) if it does not within kWaitLimitNs, or if another role of the CTA already gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
+// The first test is inline; the polling loop is one out-of-line copy for all call sites, which keeps
+// the many-role kernels' instruction footprint small.
+__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
     const uint64_t t0 = globaltimer();
     const uint64_t tlim = g_favor_test_wait_ns;
     const uint64_t limit = tlim ? tlim : kWaitLimitNs;
@@ -93,6 +94,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
             return false;
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, abort_flag);
 }
 
 // Like mbar_wait, with acquire at cluster scope: for barriers that peers of the cluster arrive on
@@ -108,8 +113,7 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
         : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
+__device__ __noinline__ bool mbar_wait_cluster_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
     const uint64_t t0 = globaltimer();
     const uint64_t tlim = g_favor_test_wait_ns;
     const uint64_t limit = tlim ? tlim : kWaitLimitNs;
@@ -124,38 +128,13 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
         }
     }
 }
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    return mbar_wait_cluster_slow(bar, parity, abort_flag);
+}
 
 // Orders this thread's earlier memory accesses before its later ones for all threads of the cluster.
 __device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
-
-// ---------------------------------------------------------------------------------------------
-// Counters in global memory shared by the CTAs of a cluster: a release increment after the data it
-// publishes, and a bounded acquire wait for a count (like mbar_wait: false on expiry or abort).
-// ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ bool counter_wait(const unsigned* p, unsigned target, volatile int* abort_flag) {
-    if (ld_acquire(p) >= target) return true;
-    const uint64_t t0 = globaltimer();
-    const uint64_t tlim = g_favor_test_wait_ns;
-    const uint64_t limit = tlim ? tlim : kWaitLimitNs;
-    for (uint32_t it = 1;; ++it) {
-        if (ld_acquire(p) >= target) return true;
-        if ((it & 15u) != 0) continue;
-        if (*abort_flag) return false;
-        if (globaltimer() - t0 > limit) {
-            atomicOr(&g_favor_error, kDevErrTimeout);
-            *abort_flag = 1;
-            return false;
-        }
-    }
-}
 
 // ---------------------------------------------------------------------------------------------
 // Thread-block clusters: rank, distributed shared memory, remote arrivals, cluster barrier
@@ -204,6 +183,10 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t caddr) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
 }
+// Relaxed arrive on a peer's mbarrier: ordered only by a preceding fence of the caller.
+__device__ __forceinline__ void mbar_arrive_relaxed_cluster(uint32_t caddr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
 // All threads of every CTA of the cluster.
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -236,6 +219,13 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
         "[%5];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
         : "memory");
+}
+// 3-D tiled prefetch into L2 (no shared memory, no completion): the later load of the same box
+// then hits L2 instead of waiting for device memory.
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
 }
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
     asm volatile(

@@ -40,6 +40,8 @@
 //                [S | z] after the state update (rescaled first if the key stabiliser rose).
 //   warps 18-21  O team: NUM -> y (alone: the output; in a cluster: the partial rows, to the ring).
 //   warps 22-25  X team (cluster only): the rows this CTA finalises, from the ring's partials.
+//   warps 26-27  signal warps (cluster only): release a tile's stored partial rows to the cluster,
+//                and report the slots the X team has read.
 //
 // Stabilisers (exp family; Y does not depend on them, both cancel between num and den):
 //   queries: c_i = the exact largest w_r . q^_i over the CTA's features (the row's largest feature
@@ -73,9 +75,11 @@ constexpr int kKWarp0 = kQWarp0 + kQWarps, kKWarps = 4;
 constexpr int kAWarp0 = kKWarp0 + kKWarps, kAWarps = 4;
 constexpr int kOWarp0 = kAWarp0 + kAWarps, kOWarps = 4;
 constexpr int kXWarp0 = kOWarp0 + kOWarps, kXWarps = 4;
-constexpr int kThreads = 32 * (kXWarp0 + kXWarps);  // 832
+constexpr int kSWarp0 = kXWarp0 + kXWarps, kSWarps = 2;  // ring signalling: full, free
+constexpr int kThreads = 32 * (kSWarp0 + kSWarps);  // 896
 constexpr int kTileBytes = kTile * kD * 2;          // 16 KB: [128 x 64] bf16
 constexpr int kPhiBytes = kTile * 128 * 2;          // 32 KB: [128 tokens x 128 features] bf16
+constexpr int kPrefetch = 3;                        // tiles of K, Q, V prefetched into L2 ahead of their loads
 constexpr int kRing = 4;                            // tiles of partial rows in flight per head
 constexpr int kXChunks = 9;                         // 16-byte chunks of a partial row: 8 of y (fp16), log-weight and scales
 constexpr float kSlackHi = 16.f;                    // key stabiliser rises once exceeded by 2^16
@@ -85,12 +89,20 @@ constexpr float kSlackHi = 16.f;                    // key stabiliser rises once
 #ifdef FAVOR_SCAN_TRACE
 constexpr int kTraceTiles = 16, kTraceEvents = 32;
 __device__ unsigned long long g_scan_trace[kTraceTiles][kTraceEvents];
-#define SCAN_TRACE(t, ev)                                                              \
-    do {                                                                               \
-        if (blockIdx.x == 0 && (t) < kTraceTiles) g_scan_trace[(t)][(ev)] = clock64(); \
+__device__ unsigned long long g_scan_cta_time[2048][6];  // per CTA: clock and globaltimer at start and end, SM id
+__device__ unsigned long long g_scan_cta_wait[2048][10];  // per CTA: cycles the MMA warp spent in each kind of wait
+#define TIMED_WAIT(i, call) ([&]() { const unsigned long long s_ = clock64(); const bool r_ = (call); wacc[i] += clock64() - s_; return r_; }())
+#ifndef FAVOR_SCAN_TRACE_FROM
+#define FAVOR_SCAN_TRACE_FROM 0
+#endif
+#define SCAN_TRACE(t, ev)                                                                            \
+    do {                                                                                             \
+        const int tr_t_ = (t) - FAVOR_SCAN_TRACE_FROM;                                               \
+        if (blockIdx.x == 0 && tr_t_ >= 0 && tr_t_ < kTraceTiles) g_scan_trace[tr_t_][(ev)] = clock64(); \
     } while (0)
 #else
 #define SCAN_TRACE(t, ev) ((void)0)
+#define TIMED_WAIT(i, call) (call)
 #endif
 
 // TMEM columns (512 allocated)
@@ -132,18 +144,6 @@ struct ScanWs {
     static size_t bytes(size_t BH, int cs) { return cs > 1 ? BH * kRing * cs * kXChunks * kTile * 16 : 0; }
 };
 
-// Whether O-team warp q (rows 32 q .. 32 q + 31) holds rows that CTA o finalises (rows o rp ..).
-__host__ __device__ __forceinline__ bool warp_feeds(int q, int o, int rp) {
-    const int lo = o * rp, hi = min(kTile, lo + rp) - 1;
-    return lo <= 32 * q + 31 && 32 * q <= hi;
-}
-__device__ __forceinline__ int feeding_warps(int o, int rp) {
-    int c = 0;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) c += warp_feeds(q, o, rp) ? 1 : 0;
-    return c;
-}
-
 // bf16 image of 8 fp32 values as one 16-byte chunk, and (lo) the bf16 rounding of what the first
 // image leaves out.
 __device__ __forceinline__ uint4 pack8_hi(const uint32_t* v) {
@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ uint64_t bar_om, bar_kfull, bar_kfree, bar_qfull, bar_qfree, bar_vfull[2], bar_vfree[2];
     __shared__ uint64_t bar_pk[2], bar_pkfree[2], bar_pq[2], bar_phq, bar_phk[2], bar_phkfree[2];
     __shared__ uint64_t bar_sc, bar_atil, bar_st, bar_snap, bar_num, bar_numfree, bar_beta[4], bar_cq[2];
-    __shared__ uint64_t bar_drain, bar_rfull[kRing], bar_rfree[kRing];
+    __shared__ uint64_t bar_drain, bar_rfull[kRing], bar_rfree[kRing], bar_ostore[kRing], bar_xread[kRing];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     __shared__ float sBeta[4], sF[4], sKmx[4];
@@ -246,9 +246,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bar_drain, 1);
         for (int i = 0; i < kRing; ++i) {
             // a slot's partial rows of this CTA's rows: one arrive per feeding warp of every CTA
-            mbar_init(&bar_rfull[i], CS * feeding_warps(rank, RP));
+            mbar_init(&bar_rfull[i], CS);
             // this CTA's slot has been read by every CTA of the cluster
             mbar_init(&bar_rfree[i], CS);
+            // this CTA's partial rows of a slot are stored / its X team has read a slot
+            mbar_init(&bar_ostore[i], kOWarps);
+            mbar_init(&bar_xread[i], kXWarps);
         }
         fence_mbar_init();
     }
@@ -267,6 +270,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     cluster_sync();  // every CTA's barriers are initialised before any remote arrive
     tc_fence_after();
+#ifdef FAVOR_SCAN_TRACE
+    if (threadIdx.x == 0 && blockIdx.x < 2048) {
+        g_scan_cta_time[blockIdx.x][0] = clock64();
+        g_scan_cta_time[blockIdx.x][1] = globaltimer();
+        uint32_t smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        g_scan_cta_time[blockIdx.x][4] = smid;
+    }
+#endif
     const uint32_t tbase = tmem_base;
 
     if (warp == 0) {
@@ -279,8 +291,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(&bar_om, (uint32_t)kTileBytes);
             tma_load_2d(sOm, &mOm, &bar_om, 0, feat0);
             int kl = 0, ql = 0, vl = 0;  // tiles loaded
+            // K, Q and V of the tiles kPrefetch ahead go to L2 first: the loads below have only
+            // about one tile of lead (single K and Q buffers), less than a device-memory round
+            // trip under load
+            auto prefetch = [&](int t) {
+                tma_prefetch_3d(&mK, 0, t * kTile, bh);
+                tma_prefetch_3d(&mQ, 0, t * kTile, bh);
+                tma_prefetch_3d(&mV, 0, t * kTile, bh);
+            };
+            for (int t = 1; t < kPrefetch && t < T; ++t) prefetch(t);
             for (int t = 0; t < T; ++t) {
                 const int b = t & 1, u = t >> 1;
+                if (t + kPrefetch < T) prefetch(t + kPrefetch);
                 // K(t) once the K team has taken the norms of K(t-1) and P_K(t-1) has read it
                 if (t > 0 && !mbar_wait(&bar_kfree, (t - 1) & 1, &abort_flag)) break;
                 mbar_arrive_expect_tx(&bar_kfull, kTileBytes);
@@ -325,15 +347,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             d_v[b] = sdesc_sw128(smem_u32(sV + b * kTileBytes), (uint32_t)(sOnes - (sV + b * kTileBytes)), 1024);
         }
         const bool leader = elect_one();
+#ifdef FAVOR_SCAN_TRACE
+        unsigned long long wacc[10] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+#endif
         bool ok = mbar_wait(&bar_om, 0, &abort_flag);
         tc_fence_after();
         // P_K(t) into region t & 1 (once K(t) is loaded)
         auto issue_pk = [&](int t) -> bool {
-            if (!mbar_wait(&bar_kfull, t & 1, &abort_flag)) return false;
+            if (!TIMED_WAIT(0, mbar_wait(&bar_kfull, t & 1, &abort_flag))) return false;
             tc_fence_after();
             if (leader) {
                 const uint32_t dcol = tbase + kColR0 + 128u * (uint32_t)(t & 1);
-#pragma unroll
+#pragma unroll 1
                 for (int ks = 0; ks < kD / 16; ++ks)
                     mma_ss(dcol, sdesc_add(d_k, 32u * ks), sdesc_add(d_om, 32u * ks), id_p, ks > 0);
                 mma_commit(&bar_pk[t & 1]);
@@ -344,12 +369,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P_Q(t) into region t & 1, once Q(t) is loaded and the K team has read P_K(t)
         auto issue_pq = [&](int t) -> bool {
             const int b = t & 1;
-            if (!mbar_wait(&bar_qfull, t & 1, &abort_flag)) return false;
-            if (!mbar_wait(&bar_pkfree[b], (t >> 1) & 1, &abort_flag)) return false;
+            if (!TIMED_WAIT(1, mbar_wait(&bar_qfull, t & 1, &abort_flag))) return false;
+            if (!TIMED_WAIT(2, mbar_wait(&bar_pkfree[b], (t >> 1) & 1, &abort_flag))) return false;
             tc_fence_after();
             if (leader) {
                 const uint32_t dcol = tbase + kColR0 + 128u * (uint32_t)b;
-#pragma unroll
+#pragma unroll 1
                 for (int ks = 0; ks < kD / 16; ++ks)
                     mma_ss(dcol, sdesc_add(d_q, 32u * ks), sdesc_add(d_om, 32u * ks), id_p, ks > 0);
                 mma_commit(&bar_pq[b]);
@@ -366,12 +391,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t num = tbase + kColNum;
             // scores: SC = phi(Q_t) phi(K_t)^T (K = 128 features, two K atoms of phi(K))
             SCAN_TRACE(t, 20);
-            ok = mbar_wait(&bar_phq, t & 1, &abort_flag) && mbar_wait(&bar_phk[b], u & 1, &abort_flag);
+            ok = TIMED_WAIT(3, mbar_wait(&bar_phq, t & 1, &abort_flag)) && TIMED_WAIT(4, mbar_wait(&bar_phk[b], u & 1, &abort_flag));
             if (!ok) break;
             SCAN_TRACE(t, 0);
             tc_fence_after();
             if (leader) {
-#pragma unroll
+#pragma unroll 1
                 for (int ks = 0; ks < 8; ++ks)
                     mma_ts(R, pq + 8u * ks, sdesc_add(d_pk_sc[b], (ks >> 2) * 16384u + (ks & 3) * 32u), id_sc, ks > 0);
                 mma_commit(&bar_sc);
@@ -379,15 +404,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             // inter: NUM = phi(Q_t) [S_<t | z_<t] (K = 128 features), plus phi(Q_t) S_lo
             SCAN_TRACE(t, 21);
-            ok = mbar_wait(&bar_snap, t & 1, &abort_flag) && mbar_wait(&bar_numfree, (t & 1) ^ 1, &abort_flag);
+            ok = TIMED_WAIT(5, mbar_wait(&bar_snap, t & 1, &abort_flag)) && TIMED_WAIT(6, mbar_wait(&bar_numfree, (t & 1) ^ 1, &abort_flag));
             if (!ok) break;
             SCAN_TRACE(t, 1);
             tc_fence_after();
             if (leader) {
-#pragma unroll
+#pragma unroll 1
                 for (int ks = 0; ks < 8; ++ks) mma_ts(num, pq + 8u * ks, sdesc_add(d_snap, 2048u * ks), id_o, ks > 0);
                 if (hilo) {
-#pragma unroll
+#pragma unroll 1
                     for (int ks = 0; ks < 8; ++ks) mma_ts(num, pq + 8u * ks, sdesc_add(d_slo, 2048u * ks), id_lo, 1u);
                 }
             }
@@ -398,10 +423,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             SCAN_TRACE(t, 2);
             // state: [S | z] += phi(K_t)^T [V_t | 1] (K = 128 tokens; phi(K) read MN-major, its
             // second 64-feature region LBO bytes on; the ones are the second N region of B)
-            if (!(ok = mbar_wait(&bar_vfull[b], u & 1, &abort_flag))) break;
+            if (!(ok = TIMED_WAIT(7, mbar_wait(&bar_vfull[b], u & 1, &abort_flag)))) break;
             tc_fence_after();
             if (leader) {
-#pragma unroll
+#pragma unroll 1
                 for (int ks = 0; ks < 8; ++ks)
                     mma_ss(tbase + kColS, sdesc_add(d_pk_st[b], 2048u * ks), sdesc_add(d_v[b], 2048u * ks), id_st,
                            (t > 0 || ks > 0) ? 1u : 0u);
@@ -412,11 +437,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             SCAN_TRACE(t, 3);
             // intra: NUM += A~ [V_t | 1] (K = 128 keys, A~ packed in place of the scores)
             SCAN_TRACE(t, 22);
-            if (!(ok = mbar_wait(&bar_atil, t & 1, &abort_flag))) break;
+            if (!(ok = TIMED_WAIT(8, mbar_wait(&bar_atil, t & 1, &abort_flag)))) break;
             SCAN_TRACE(t, 4);
             tc_fence_after();
             if (leader) {
-#pragma unroll
+#pragma unroll 1
                 for (int ks = 0; ks < 8; ++ks) mma_ts(num, R + 8u * ks, sdesc_add(d_v[b], 2048u * ks), id_o, 1u);
                 mma_commit(&bar_num);
                 mma_commit(&bar_vfree[b]);
@@ -425,6 +450,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (t + 2 < T && !(ok = issue_pk(t + 2))) break;
             SCAN_TRACE(t, 5);
         }
+#ifdef FAVOR_SCAN_TRACE
+        if (lane == 0 && blockIdx.x < 2048)
+            for (int i = 0; i < 10; ++i) g_scan_cta_wait[blockIdx.x][i] = wacc[i];
+#endif
         // Every MMA issued (all of them, or those before a wait gave up) completes before TMEM is
         // released.
         if (leader) mma_commit(&bar_drain);
@@ -588,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // keys [32 cc, 32 cc + 32) of row 32 q + lane: all after the warp's rows (cc > q), all at
             // or before them (cc < q), or across the diagonal (cc == q). Packed key j -> column j / 2;
             // chunk cc writes columns the chunks up to cc have already been read from.
-#pragma unroll
+#pragma unroll 1
             for (int cc = 0; cc < 4; ++cc) {
                 uint32_t w[16];
                 if (cc > q) {
@@ -596,21 +625,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int k = 0; k < 16; ++k) w[k] = 0u;
                 } else {
                     uint32_t v[32];
-                    tmem_ld32(ra + 32u * cc, v);
+                    tmem_ld32(ra + 32u * (uint32_t)cc, v);
                     tmem_ld_wait();
-                    if (cc < q) {
+                    const int lim = cc < q ? 31 : lane;  // keys j <= i of the chunk
 #pragma unroll
-                        for (int k = 0; k < 16; ++k) w[k] = pack_bf16(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < 16; ++k) {
-                            const float a0 = 2 * k <= lane ? __uint_as_float(v[2 * k]) : 0.f;
-                            const float a1 = 2 * k + 1 <= lane ? __uint_as_float(v[2 * k + 1]) : 0.f;
-                            w[k] = pack_bf16(a0, a1);
-                        }
+                    for (int k = 0; k < 16; ++k) {
+                        const float a0 = 2 * k <= lim ? __uint_as_float(v[2 * k]) : 0.f;
+                        const float a1 = 2 * k + 1 <= lim ? __uint_as_float(v[2 * k + 1]) : 0.f;
+                        w[k] = pack_bf16(a0, a1);
                     }
                 }
-                tmem_st16(ra + 16u * cc, w);
+                tmem_st16(ra + 16u * (uint32_t)cc, w);
             }
             tmem_st_wait();
             tc_fence_before();
@@ -629,15 +654,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t sa = tbase + lane_off + kColS;
                 uint32_t zr;
                 tmem_ld1(sa + 64, zr);
-#pragma unroll
+#pragma unroll 1
                 for (int hh = 0; hh < 2; ++hh) {
                     uint32_t v[32];
-                    tmem_ld32(sa + 32u * hh, v);
+                    tmem_ld32(sa + 32u * (uint32_t)hh, v);
                     tmem_ld_wait();
                     if (f != 1.f) {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
-                        tmem_st32(sa + 32u * hh, v);
+                        tmem_st32(sa + 32u * (uint32_t)hh, v);
                     }
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
@@ -676,15 +701,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool failed = false;
         // This CTA's part of the head's ring: [slot][rank][chunk][row] x 16 bytes.
         uint8_t* ring = CS > 1 ? p.ring + (size_t)bh * kRing * CS * kXChunks * kTile * 16 : nullptr;
-        // The partial rows of tile tp are complete: each lane's stores are released, then every
-        // CTA that finalises rows of this warp is signalled.
-        auto publish = [&](int tp) {
-            fence_acq_rel_cluster();
-            __syncwarp();
-            if (lane == 0)
-                for (int o = 0; o < CS; ++o)
-                    if (warp_feeds(q, o, RP)) mbar_arrive_cluster(mapa(smem_u32(&bar_rfull[tp % kRing]), o));
-        };
         for (int tt = 0; tt < T; ++tt) {
             const int slot = tt % kRing, use = tt / kRing;
             const int i_tok = tt * kTile + r;
@@ -703,43 +719,59 @@ __global__ void __launch_bounds__(kThreads, 1)
             // features. Alone, the bf16 output row; in a cluster, fp16 times a power-of-two scale per
             // half row (so that any bf16 value range survives), the partial row for its owner.
             const uint32_t na = tbase + lane_off + kColNum;
-            uint32_t v[32], d0, d1;
-            tmem_ld32(na + 32, v);
-            tmem_ld1(na + 64, d0);
-            tmem_ld1(na + 65, d1);
-            tmem_ld_wait();
-            // the previous tile's partial rows (stored an iteration ago) go to their owners first,
-            // so that the release does not wait for this tile's stores
-            if (CS > 1 && tt > 0) publish(tt - 1);
-            const float den_own = __uint_as_float(d0) + __uint_as_float(d1);
-            // y = num / den; a den below 2^-64 (keys far below the stabiliser) is scaled by 2^64 first,
-            // so that 1 / den stays finite
-            const bool tiny = den_own < 0x1p-64f;
-            const float inv_own = den_own > 0.f ? 1.f / (tiny ? den_own * 0x1p64f : den_own) : 0.f;
-            // one half row (32 values in v) -> four 16-byte chunks at chunk c0; returns its scale
-            auto put_half = [&](int c0) -> float {
-                uint32_t w[16];
-                float sc = 1.f, pw = 1.f;
+            float den_own = 0.f, inv_own = 0.f, big = 1.f, e_own = 0.f, sc0 = 1.f, sc1 = 1.f;
+#pragma unroll 1
+            for (int h = 1; h >= 0; --h) {
+                uint32_t v[32];
+                tmem_ld32(na + 32u * (uint32_t)h, v);
+                if (h == 1) {
+                    uint32_t d0, d1;
+                    tmem_ld1(na + 64, d0);
+                    tmem_ld1(na + 65, d1);
+                    tmem_ld_wait();
+                    den_own = __uint_as_float(d0) + __uint_as_float(d1);
+                    // y = num / den; a den below 2^-64 (keys far below the stabiliser) is scaled by
+                    // 2^64 first (num with it), so that 1 / den stays finite
+                    big = den_own < 0x1p-64f ? 0x1p64f : 1.f;
+                    inv_own = den_own > 0.f ? 1.f / (den_own * big) : 0.f;
+                } else {
+                    // the row's exponent offset: read before NUM is released, which lets the Q and
+                    // K teams move on to the tiles that reuse these slots
+                    if (exp_kind && CS > 1) {
+                        failed |= !mbar_wait(&bar_cq[tt & 1], (tt >> 1) & 1, &abort_flag);
+                        failed |= !mbar_wait(&bar_beta[tt & 3], (tt >> 2) & 1, &abort_flag);
+                        e_own = sCq[(tt & 1) * 128 + r] + sBeta[tt & 3];
+                    }
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar_numfree);  // NUM may take the next tile's inter MMA
+                    if (warp == kOWarp0 && lane == 0) SCAN_TRACE(tt, 16);
+                }
+                // half row h: alone, the bf16 output; in a cluster, fp16 times a power-of-two scale 2^ex
+                // with max |y| 2^-ex in [2^14, 2^15) (from the IEEE exponent field, clamped so that
+                // all factors stay finite), so that fp16 keeps 11 bits of any bf16 value range
+                float pw = 1.f;
                 if (CS > 1) {
                     float mx = 0.f;
 #pragma unroll
                     for (int k = 0; k < 32; ++k) mx = fmaxf(mx, fabsf(__uint_as_float(v[k])));
-                    mx = (tiny ? mx * 0x1p64f : mx) * inv_own;
-                    // 2^ex with mx 2^-ex in [2^14, 2^15) (from the IEEE exponent field; clamped so
-                    // that all factors stay finite): fp16 keeps 11 bits of every value of the half
+                    mx = mx * big * inv_own;
                     const int ex = mx > 0.f ? max(-60, min(113, (int)((__float_as_uint(mx) >> 23) & 0xFFu) - 127 - 14)) : 0;
-                    sc = __uint_as_float((uint32_t)(ex + 127) << 23);
+                    const float scl = __uint_as_float((uint32_t)(ex + 127) << 23);
                     pw = __uint_as_float((uint32_t)(127 - ex) << 23);
+                    if (h) sc1 = scl;
+                    else sc0 = scl;
                 }
-                const float f = inv_own * pw;
-                auto yv = [&](uint32_t x) { return tiny ? (__uint_as_float(x) * 0x1p64f) * inv_own * pw : __uint_as_float(x) * f; };
-                if (CS == 1) {
+                uint32_t w[16];
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) w[k] = pack_bf16(yv(v[2 * k]), yv(v[2 * k + 1]));
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        __half2 h2 = __floats2half2_rn(yv(v[2 * k]), yv(v[2 * k + 1]));
+                for (int k = 0; k < 16; ++k) {
+                    const float y0 = __uint_as_float(v[2 * k]) * big * inv_own * pw;
+                    const float y1 = __uint_as_float(v[2 * k + 1]) * big * inv_own * pw;
+                    if (CS == 1) {
+                        w[k] = pack_bf16(y0, y1);
+                    } else {
+                        __half2 h2 = __floats2half2_rn(y0, y1);
                         w[k] = *reinterpret_cast<uint32_t*>(&h2);
                     }
                 }
@@ -747,39 +779,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const uint4 o = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-                        if (CS == 1) yrow[c0 + c] = o;
-                        else __stcg(reinterpret_cast<uint4*>(rec + (c0 + c) * kTile * 16), o);
+                        if (CS == 1) yrow[4 * h + c] = o;
+                        else __stcg(reinterpret_cast<uint4*>(rec + (4 * h + c) * kTile * 16), o);
                     }
                 }
-                return sc;
-            };
-            const float sc1 = put_half(4);
-            tmem_ld32(na, v);
-            // the row's exponent offset: read before NUM is released, which lets the Q and K teams
-            // move on to the tiles that reuse these slots
-            float e_own = 0.f;
-            if (exp_kind && CS > 1) {
-                failed |= !mbar_wait(&bar_cq[tt & 1], (tt >> 1) & 1, &abort_flag);
-                failed |= !mbar_wait(&bar_beta[tt & 3], (tt >> 2) & 1, &abort_flag);
-                e_own = sCq[(tt & 1) * 128 + r] + sBeta[tt & 3];
             }
-            tmem_ld_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar_numfree);  // NUM may take the next tile's inter MMA
-            if (warp == kOWarp0 && lane == 0) SCAN_TRACE(tt, 16);
-            const float sc0 = put_half(0);
             if (CS > 1) {
                 // the row's log-weight: log2(den) plus its exponent offset (-inf: no weight)
                 const float l_own = den_own > 0.f ? log2_pos(den_own) + e_own : -INFINITY;
                 __stcg(reinterpret_cast<uint4*>(rec + 8 * kTile * 16),
                        make_uint4(__float_as_uint(l_own), __float_as_uint(sc0), __float_as_uint(sc1), 0u));
+                // the warp's partial rows of this tile are stored (released at CTA scope; the
+                // full-signal warp releases them to the cluster)
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_ostore[slot]);
             }
             if (warp == kOWarp0 && lane == 0) SCAN_TRACE(tt, 18);
         }
-        if (CS > 1 && T > 0) publish(T - 1);
         (void)failed;
-    } else {
+    } else if (warp < kSWarp0) {
         // ---------------- X team: 4 warps (cluster only) ----------------
         // The rows [rank RP, rank RP + rows) of each tile from the CS partial rows in the ring: a
         // row's result is sum_g w_g y_g / sum_g w_g with w_g = 2^(l_g - max l), l_g = log2(den_g) + e_g
@@ -790,71 +808,60 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint8_t* ring = p.ring + (size_t)bh * kRing * CS * kXChunks * kTile * 16;
             const int row0 = rank * RP, rows = min(RP, kTile - row0);
             bool failed = false;
-            // one pass: 32 rows, four threads per row with two 16-byte chunks each; returns whether
-            // the thread has output (two chunks in out, for the row at dst)
-            auto combine_pass = [&](int tc, int item, uint4 (&out)[2], uint4*& dst) -> bool {
+            // One tile: passes of 32 rows, four threads per row with two 16-byte chunks each.
+            auto combine = [&](int tc) {
                 constexpr int NC = kMaxCluster;  // partials past CS carry no weight
                 const int slot = tc % kRing;
-                const int row = row0 + item / 4, c0 = (item % 4) * 2;
-                const int tok = tc * kTile + row;
-                if (!(item < rows * 4 && tok < p.n)) return false;
-                uint4 meta[NC], yv[NC][2];
-#pragma unroll
-                for (int g = 0; g < NC; ++g) {
-                    if (g >= CS) {  // log-weight -inf
-                        meta[g] = make_uint4(0xFF800000u, 0u, 0u, 0u);
-                        yv[g][0] = yv[g][1] = make_uint4(0u, 0u, 0u, 0u);
-                        continue;
-                    }
-                    const uint8_t* rec = ring + ((size_t)(slot * CS + g) * kXChunks) * kTile * 16 + row * 16;
-                    meta[g] = __ldcg(reinterpret_cast<const uint4*>(rec + 8 * kTile * 16));
-#pragma unroll
-                    for (int k = 0; k < 2; ++k) yv[g][k] = __ldcg(reinterpret_cast<const uint4*>(rec + (c0 + k) * kTile * 16));
-                }
-                float L = -INFINITY;
-#pragma unroll
-                for (int g = 0; g < NC; ++g) L = fmaxf(L, __uint_as_float(meta[g].x));
-                float ws[NC], wsum = 0.f;
-#pragma unroll
-                for (int g = 0; g < NC; ++g) {
-                    const float w = L > -INFINITY ? ex2(__uint_as_float(meta[g].x) - L) : 0.f;  // the largest is 1
-                    wsum += w;
-                    ws[g] = w * __uint_as_float(c0 < 4 ? meta[g].y : meta[g].z);
-                }
-                const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                for (int item = xt; item < rows * 4; item += 32 * kXWarps) {
+                    const int row = row0 + item / 4, c0 = (item % 4) * 2;
+                    const int tok = tc * kTile + row;
+                    if (tok >= p.n) continue;
+                    uint4 meta[NC], yv[NC][2];
 #pragma unroll
                     for (int g = 0; g < NC; ++g) {
-                        const uint32_t hw[4] = {yv[g][k].x, yv[g][k].y, yv[g][k].z, yv[g][k].w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 y2 = __half22float2(*reinterpret_cast<const __half2*>(&hw[e]));
-                            acc[2 * e] = fmaf(ws[g], y2.x, acc[2 * e]);
-                            acc[2 * e + 1] = fmaf(ws[g], y2.y, acc[2 * e + 1]);
+                        if (g >= CS) {  // log-weight -inf
+                            meta[g] = make_uint4(0xFF800000u, 0u, 0u, 0u);
+                            yv[g][0] = yv[g][1] = make_uint4(0u, 0u, 0u, 0u);
+                            continue;
                         }
+                        const uint8_t* rec = ring + ((size_t)(slot * CS + g) * kXChunks) * kTile * 16 + row * 16;
+                        meta[g] = __ldcg(reinterpret_cast<const uint4*>(rec + 8 * kTile * 16));
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) yv[g][k] = __ldcg(reinterpret_cast<const uint4*>(rec + (c0 + k) * kTile * 16));
                     }
-                    out[k] = make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
-                                        pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
+                    float L = -INFINITY;
+#pragma unroll
+                    for (int g = 0; g < NC; ++g) L = fmaxf(L, __uint_as_float(meta[g].x));
+                    float ws[NC], wsum = 0.f;
+#pragma unroll
+                    for (int g = 0; g < NC; ++g) {
+                        const float w = L > -INFINITY ? ex2(__uint_as_float(meta[g].x) - L) : 0.f;  // the largest is 1
+                        wsum += w;
+                        ws[g] = w * __uint_as_float(c0 < 4 ? meta[g].y : meta[g].z);
+                    }
+                    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+                    uint4* dst = reinterpret_cast<uint4*>(p.Y + ((size_t)bh * p.n + tok) * kD + 8 * c0);
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int g = 0; g < NC; ++g) {
+                            const uint32_t hw[4] = {yv[g][k].x, yv[g][k].y, yv[g][k].z, yv[g][k].w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 y2 = __half22float2(*reinterpret_cast<const __half2*>(&hw[e]));
+                                acc[2 * e] = fmaf(ws[g], y2.x, acc[2 * e]);
+                                acc[2 * e + 1] = fmaf(ws[g], y2.y, acc[2 * e + 1]);
+                            }
+                        }
+                        dst[k] = make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
+                                            pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
+                    }
                 }
-                dst = reinterpret_cast<uint4*>(p.Y + ((size_t)bh * p.n + tok) * kD + 8 * c0);
-                return true;
-            };
-            // rows <= 64: at most two passes
-            auto combine = [&](int tc) {
-                uint4 o0[2], o1[2];
-                uint4 *d0 = nullptr, *d1 = nullptr;
-                const bool h0 = combine_pass(tc, xt, o0, d0);
-                const bool h1 = rows * 4 > 32 * kXWarps && combine_pass(tc, xt + 32 * kXWarps, o1, d1);
-                // every thread of the team has consumed its loads: the slot is free for its writers'
-                // next use. The outputs are stored after the release, which then has no stores of
-                // this tile to wait for.
-                named_bar(4, 32 * kXWarps);
-                if (xt == 0)
-                    for (int o = 0; o < CS; ++o) mbar_arrive_cluster(mapa(smem_u32(&bar_rfree[tc % kRing]), o));
-                if (h0) { d0[0] = o0[0]; d0[1] = o0[1]; }
-                if (h1) { d1[0] = o1[0]; d1[1] = o1[1]; }
+                // the warp has consumed its loads of the slot (the free-signal warp passes that on)
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_xread[slot]);
             };
             for (int tc = 0; tc < T; ++tc) {
                 failed |= !mbar_wait_cluster(&bar_rfull[tc % kRing], (tc / kRing) & 1, &abort_flag);
@@ -864,9 +871,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             (void)failed;
         }
+    } else {
+        // ---------------- signal warps (cluster only) ----------------
+        // Warp kSWarp0 releases each tile's partial rows of this CTA to every CTA of the cluster
+        // once the O team has stored them; warp kSWarp0 + 1 tells every CTA that this CTA's X
+        // team has read their rows of a slot. Each holds the one cluster-scope fence of its tile
+        // (the teams themselves only arrive on local barriers), and the remote arrives are relaxed.
+        if (CS > 1 && lane == 0) {
+            const bool full_side = warp == kSWarp0;
+            uint64_t* local = full_side ? bar_ostore : bar_xread;
+            uint64_t* remote = full_side ? bar_rfull : bar_rfree;
+            bool failed = false;
+            for (int t = 0; t < T && !failed; ++t) {
+                failed |= !mbar_wait(&local[t % kRing], (t / kRing) & 1, &abort_flag);
+                fence_acq_rel_cluster();
+                for (int o = 0; o < CS; ++o) mbar_arrive_relaxed_cluster(mapa(smem_u32(&remote[t % kRing]), o));
+            }
+        }
     }
     tc_fence_before();
     __syncthreads();
+#ifdef FAVOR_SCAN_TRACE
+    if (threadIdx.x == 0 && blockIdx.x < 2048) {
+        g_scan_cta_time[blockIdx.x][2] = clock64();
+        g_scan_cta_time[blockIdx.x][3] = globaltimer();
+    }
+#endif
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tbase, 512);
