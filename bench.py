@@ -700,6 +700,8 @@ def main(argv=None):
                     help="time the on-device Omega builder at the workload's m and d instead of the full call")
     ap.add_argument("--n", type=int, default=None,
                     help="override the sequence length (smaller cases for profiler captures; not a bench line)")
+    ap.add_argument("--H", type=int, default=None,
+                    help="override the heads per batch entry (smaller cases for profiler captures; not a bench line)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -709,6 +711,8 @@ def main(argv=None):
     w = si.get_workload(args.workload)
     if args.n is not None:
         w = w.with_(n=args.n, name=f"{w.name}@n={args.n}")
+    if args.H is not None:
+        w = w.with_(H=args.H, name=f"{w.name}@H={args.H}")
     if args.impl == "reference":
         return run_reference(args, w)
     if args.decode:

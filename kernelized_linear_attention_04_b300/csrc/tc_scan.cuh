@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             if (leader) {
                 const uint32_t dcol = tbase + kColR0 + 128u * (uint32_t)(t & 1);
-#pragma unroll 1
+#pragma unroll
                 for (int ks = 0; ks < kD / 16; ++ks)
                     mma_ss(dcol, sdesc_add(d_k, 32u * ks), sdesc_add(d_om, 32u * ks), id_p, ks > 0);
                 mma_commit(&bar_pk[t & 1]);
@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             if (leader) {
                 const uint32_t dcol = tbase + kColR0 + 128u * (uint32_t)b;
-#pragma unroll 1
+#pragma unroll
                 for (int ks = 0; ks < kD / 16; ++ks)
                     mma_ss(dcol, sdesc_add(d_q, 32u * ks), sdesc_add(d_om, 32u * ks), id_p, ks > 0);
                 mma_commit(&bar_pq[b]);
@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             SCAN_TRACE(t, 0);
             tc_fence_after();
             if (leader) {
-#pragma unroll 1
+#pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
                     mma_ts(R, pq + 8u * ks, sdesc_add(d_pk_sc[b], (ks >> 2) * 16384u + (ks & 3) * 32u), id_sc, ks > 0);
                 mma_commit(&bar_sc);
@@ -409,10 +409,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             SCAN_TRACE(t, 1);
             tc_fence_after();
             if (leader) {
-#pragma unroll 1
+#pragma unroll
                 for (int ks = 0; ks < 8; ++ks) mma_ts(num, pq + 8u * ks, sdesc_add(d_snap, 2048u * ks), id_o, ks > 0);
                 if (hilo) {
-#pragma unroll 1
+#pragma unroll
                     for (int ks = 0; ks < 8; ++ks) mma_ts(num, pq + 8u * ks, sdesc_add(d_slo, 2048u * ks), id_lo, 1u);
                 }
             }
@@ -426,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = TIMED_WAIT(7, mbar_wait(&bar_vfull[b], u & 1, &abort_flag)))) break;
             tc_fence_after();
             if (leader) {
-#pragma unroll 1
+#pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
                     mma_ss(tbase + kColS, sdesc_add(d_pk_st[b], 2048u * ks), sdesc_add(d_v[b], 2048u * ks), id_st,
                            (t > 0 || ks > 0) ? 1u : 0u);
@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             SCAN_TRACE(t, 4);
             tc_fence_after();
             if (leader) {
-#pragma unroll 1
+#pragma unroll
                 for (int ks = 0; ks < 8; ++ks) mma_ts(num, R + 8u * ks, sdesc_add(d_v[b], 2048u * ks), id_o, 1u);
                 mma_commit(&bar_num);
                 mma_commit(&bar_vfree[b]);
