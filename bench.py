@@ -689,6 +689,77 @@ def run_omega(args, w):
     print(json.dumps(line))
 
 
+# ------------------------------------------------------------------------------------------------
+# FAVOR+ against exact softmax attention: wall clock and divergence over n and m ("Linear
+# Attention and the Performer", *Exercise*: the (1, 8, n, 64) shape against the exact operator;
+# the "Performer" paper note's checklist: n large enough, wall clock, m, the comparator).
+# Context, not a bench line: one JSON object per point on stdout.
+# ------------------------------------------------------------------------------------------------
+
+SWEEP_N = (256, 1024, 4096, 16384, 65536)
+SWEEP_M = (64, 128, 256, 512)  # the library's range (m <= 512)
+
+
+def run_sweep(args):
+    import torch
+
+    import kernelized_linear_attention_04_b300 as favor
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    ns = [int(x) for x in args.sweep_n.split(",")] if args.sweep_n else list(SWEEP_N)
+    ms = [int(x) for x in args.sweep_m.split(",")] if args.sweep_m else list(SWEEP_M)
+
+    def to_dev(a):
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if a.dtype == np.uint16 else torch.from_numpy(a)
+        return t.to(dev)
+
+    def timed(fn, reps):
+        for _ in range(3):
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        torch.cuda.synchronize()
+        for a, b in evs:
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return float(np.median([a.elapsed_time(b) for a, b in evs]))
+
+    for causal in (False, True):
+        for n in ns:
+            base = si.Workload("sweep", 1, 8, n, 64, ms[0], "bf16", causal, kind="exp", seed=101 + n, omega_seed=7)
+            full = si.full_inputs(base)
+            Q, K, V = (to_dev(full[k]) for k in ("Q", "K", "V"))
+            del full
+            reps = max(3, min(20, int(2e9 / (4.0 * n * n * 64 * 8))))
+            Ye = favor.favor_softmax_attn(Q, K, V, causal=causal)
+            t_exact = timed(lambda: favor.favor_softmax_attn(Q, K, V, causal=causal, out=Ye), reps)
+            ye = Ye.float()
+            for m in ms:
+                w = base.with_(m=m)
+                om, _ = si.omega_for(w)
+                Om = to_dev(om)
+                op = "causal" if causal else "noncausal"
+                ws = torch.empty(max(favor.workspace_bytes(op, 1, 8, n, 64, m, torch.bfloat16, kind="exp"), 1),
+                                 dtype=torch.uint8, device=dev)
+                call = (lambda: favor.favor_attn_causal(Q, K, V, Om, kind="exp", out=Yf, workspace=ws)) if causal else \
+                       (lambda: favor.favor_attn_noncausal(Q, K, V, Om, kind="exp", out=Yf, workspace=ws))
+                Yf = torch.empty_like(Q)
+                call()
+                t_favor = timed(call, max(reps, 10))
+                diff = Yf.float() - ye
+                print(json.dumps({
+                    "sweep": "favor_vs_exact", "form": op, "B": 1, "H": 8, "n": n, "d": 64, "m": m,
+                    "features": "exp", "dtype": "bf16", "favor_ms": t_favor, "exact_ms": t_exact,
+                    "exact_over_favor": t_exact / t_favor,
+                    "rel_l2": float(diff.norm() / ye.norm()), "max_abs": float(diff.abs().max()),
+                    "timing": "CUDA events, median, L2 warm", "data": "synthetic iid N(0, 1)"}), flush=True)
+            del Q, K, V, Ye
+            torch.cuda.empty_cache()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -705,6 +776,10 @@ def main(argv=None):
                     help="override the sequence length (smaller cases for profiler captures; not a bench line)")
     ap.add_argument("--H", type=int, default=None,
                     help="override the heads per batch entry (smaller cases for profiler captures; not a bench line)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="FAVOR+ (exp features) against the exact softmax kernel over n and m: time and divergence")
+    ap.add_argument("--sweep-n", default=None, help="comma-separated sequence lengths for --sweep")
+    ap.add_argument("--sweep-m", default=None, help="comma-separated feature counts for --sweep")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -716,6 +791,8 @@ def main(argv=None):
         w = w.with_(n=args.n, name=f"{w.name}@n={args.n}")
     if args.H is not None:
         w = w.with_(H=args.H, name=f"{w.name}@H={args.H}")
+    if args.sweep:
+        return run_sweep(args)
     if args.impl == "reference":
         return run_reference(args, w)
     if args.decode:

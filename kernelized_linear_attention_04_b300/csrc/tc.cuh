@@ -78,9 +78,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 // Waits for phase `parity` of `bar` to complete. Returns false (after flagging the error and the
 // CTA abort word) if it does not within kWaitLimitNs, or if another role of the CTA already gave up.
-// The first test is inline; the polling loop is one out-of-line copy for all call sites, which keeps
-// the many-role kernels' instruction footprint small.
-__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
     const uint64_t t0 = globaltimer();
     const uint64_t tlim = g_favor_test_wait_ns;
     const uint64_t limit = tlim ? tlim : kWaitLimitNs;
@@ -97,7 +95,16 @@ __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, vola
 }
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
-    return mbar_wait_slow(bar, parity, abort_flag);
+    return mbar_wait_poll(bar, parity, abort_flag);
+}
+// The same wait with the polling loop out of line (one copy for all call sites): for kernels with
+// many warp roles, whose instruction footprint matters more than a call on the slow path.
+__device__ __noinline__ bool mbar_wait_poll_ool(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    return mbar_wait_poll(bar, parity, abort_flag);
+}
+__device__ __forceinline__ bool mbar_wait_lean(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_poll_ool(bar, parity, abort_flag);
 }
 
 // Like mbar_wait, with acquire at cluster scope: for barriers that peers of the cluster arrive on
@@ -113,7 +120,7 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
         : "memory");
     return ok != 0;
 }
-__device__ __noinline__ bool mbar_wait_cluster_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait_cluster_poll(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
     const uint64_t t0 = globaltimer();
     const uint64_t tlim = g_favor_test_wait_ns;
     const uint64_t limit = tlim ? tlim : kWaitLimitNs;
@@ -130,7 +137,14 @@ __device__ __noinline__ bool mbar_wait_cluster_slow(uint64_t* bar, uint32_t pari
 }
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
-    return mbar_wait_cluster_slow(bar, parity, abort_flag);
+    return mbar_wait_cluster_poll(bar, parity, abort_flag);
+}
+__device__ __noinline__ bool mbar_wait_cluster_poll_ool(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    return mbar_wait_cluster_poll(bar, parity, abort_flag);
+}
+__device__ __forceinline__ bool mbar_wait_cluster_lean(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    return mbar_wait_cluster_poll_ool(bar, parity, abort_flag);
 }
 
 // Orders this thread's earlier memory accesses before its later ones for all threads of the cluster.

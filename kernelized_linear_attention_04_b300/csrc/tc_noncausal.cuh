@@ -438,6 +438,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
                 const int u = t * UPT + g;
                 if ((u & 1) != tm) continue;
                 const bool real_feat = f0 + g * 128 + r < p.m;
+                float umu = -INFINITY;  // the unit's largest exponent (counted for real features only)
                 const int s = u % kStateSlots;
                 failed |= !mbar_wait(&bar_ufull[s], (u / kStateSlots) & 1, &abort_flag);
                 __syncwarp();
@@ -459,15 +460,15 @@ __global__ void __launch_bounds__(kStateThreads, 1)
                         const float4 c4 = *reinterpret_cast<const float4*>(cc + i);
                         float f[4];
                         if (p.kind == kKindExp) {
-                            f[0] = ex2(fmaf(__uint_as_float(vv[i + 0]), A2, -c4.x));
-                            f[1] = ex2(fmaf(__uint_as_float(vv[i + 1]), A2, -c4.y));
-                            f[2] = ex2(fmaf(__uint_as_float(vv[i + 2]), A2, -c4.z));
-                            f[3] = ex2(fmaf(__uint_as_float(vv[i + 3]), A2, -c4.w));
-                            if (real_feat)
-                                umax = fmaxf(fmaxf(umax, fmaxf(fmaf(__uint_as_float(vv[i + 0]), A2, -c4.x),
-                                                               fmaf(__uint_as_float(vv[i + 1]), A2, -c4.y))),
-                                             fmaxf(fmaf(__uint_as_float(vv[i + 2]), A2, -c4.z),
-                                                   fmaf(__uint_as_float(vv[i + 3]), A2, -c4.w)));
+                            const float e0 = fmaf(__uint_as_float(vv[i + 0]), A2, -c4.x);
+                            const float e1 = fmaf(__uint_as_float(vv[i + 1]), A2, -c4.y);
+                            const float e2 = fmaf(__uint_as_float(vv[i + 2]), A2, -c4.z);
+                            const float e3 = fmaf(__uint_as_float(vv[i + 3]), A2, -c4.w);
+                            f[0] = ex2(e0);
+                            f[1] = ex2(e1);
+                            f[2] = ex2(e2);
+                            f[3] = ex2(e3);
+                            umu = fmaxf(umu, fmaxf(fmaxf(e0, e1), fmaxf(e2, e3)));
                         } else {
                             f[0] = c4.x == 0.f ? phi_plain(__uint_as_float(vv[i + 0]) * p.scale, p.kind, 1.f, p.relu_eps_s) : 0.f;
                             f[1] = c4.y == 0.f ? phi_plain(__uint_as_float(vv[i + 1]) * p.scale, p.kind, 1.f, p.relu_eps_s) : 0.f;
@@ -489,6 +490,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar_phi[s]);
+                if (real_feat) umax = fmaxf(umax, umu);
             }
             if (p.kind == kKindExp) {  // for the key constant two tiles on (nats, absolute)
                 umax = warp_max(umax);

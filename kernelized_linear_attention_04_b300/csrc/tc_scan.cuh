@@ -304,27 +304,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int b = t & 1, u = t >> 1;
                 if (t + kPrefetch < T) prefetch(t + kPrefetch);
                 // K(t) once the K team has taken the norms of K(t-1) and P_K(t-1) has read it
-                if (t > 0 && !mbar_wait(&bar_kfree, (t - 1) & 1, &abort_flag)) break;
+                if (t > 0 && !mbar_wait_lean(&bar_kfree, (t - 1) & 1, &abort_flag)) break;
                 mbar_arrive_expect_tx(&bar_kfull, kTileBytes);
                 tma_load_3d(sK, &mK, &bar_kfull, 0, t * kTile, bh);
                 kl = t + 1;
                 // Q(t) once P_Q(t-1) has read Q(t-1)
-                if (t > 0 && !mbar_wait(&bar_qfree, (t - 1) & 1, &abort_flag)) break;
+                if (t > 0 && !mbar_wait_lean(&bar_qfree, (t - 1) & 1, &abort_flag)) break;
                 mbar_arrive_expect_tx(&bar_qfull, kTileBytes);
                 tma_load_3d(sQ, &mQ, &bar_qfull, 0, t * kTile, bh);
                 ql = t + 1;
                 // V(t) once the intra MMA of tile t-2 (the last reader of buffer b) is done
-                if (t > 1 && !mbar_wait(&bar_vfree[b], (u & 1) ^ 1, &abort_flag)) break;
+                if (t > 1 && !mbar_wait_lean(&bar_vfree[b], (u & 1) ^ 1, &abort_flag)) break;
                 mbar_arrive_expect_tx(&bar_vfull[b], kTileBytes);
                 tma_load_3d(sV + b * kTileBytes, &mV, &bar_vfull[b], 0, t * kTile, bh);
                 vl = t + 1;
             }
             // Drain the loads in flight before the CTA may exit.
             volatile int never = 0;
-            mbar_wait(&bar_om, 0, &never);
-            if (kl > 0) mbar_wait(&bar_kfull, (kl - 1) & 1, &never);
-            if (ql > 0) mbar_wait(&bar_qfull, (ql - 1) & 1, &never);
-            for (int t = vl - 2 < 0 ? 0 : vl - 2; t < vl; ++t) mbar_wait(&bar_vfull[t & 1], (t >> 1) & 1, &never);
+            mbar_wait_lean(&bar_om, 0, &never);
+            if (kl > 0) mbar_wait_lean(&bar_kfull, (kl - 1) & 1, &never);
+            if (ql > 0) mbar_wait_lean(&bar_qfull, (ql - 1) & 1, &never);
+            for (int t = vl - 2 < 0 ? 0 : vl - 2; t < vl; ++t) mbar_wait_lean(&bar_vfull[t & 1], (t >> 1) & 1, &never);
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer: the whole warp waits, one elected lane issues ----------------
@@ -350,11 +350,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #ifdef FAVOR_SCAN_TRACE
         unsigned long long wacc[10] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
 #endif
-        bool ok = mbar_wait(&bar_om, 0, &abort_flag);
+        bool ok = mbar_wait_lean(&bar_om, 0, &abort_flag);
         tc_fence_after();
         // P_K(t) into region t & 1 (once K(t) is loaded)
         auto issue_pk = [&](int t) -> bool {
-            if (!TIMED_WAIT(0, mbar_wait(&bar_kfull, t & 1, &abort_flag))) return false;
+            if (!TIMED_WAIT(0, mbar_wait_lean(&bar_kfull, t & 1, &abort_flag))) return false;
             tc_fence_after();
             if (leader) {
                 const uint32_t dcol = tbase + kColR0 + 128u * (uint32_t)(t & 1);
@@ -369,8 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P_Q(t) into region t & 1, once Q(t) is loaded and the K team has read P_K(t)
         auto issue_pq = [&](int t) -> bool {
             const int b = t & 1;
-            if (!TIMED_WAIT(1, mbar_wait(&bar_qfull, t & 1, &abort_flag))) return false;
-            if (!TIMED_WAIT(2, mbar_wait(&bar_pkfree[b], (t >> 1) & 1, &abort_flag))) return false;
+            if (!TIMED_WAIT(1, mbar_wait_lean(&bar_qfull, t & 1, &abort_flag))) return false;
+            if (!TIMED_WAIT(2, mbar_wait_lean(&bar_pkfree[b], (t >> 1) & 1, &abort_flag))) return false;
             tc_fence_after();
             if (leader) {
                 const uint32_t dcol = tbase + kColR0 + 128u * (uint32_t)b;
@@ -391,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t num = tbase + kColNum;
             // scores: SC = phi(Q_t) phi(K_t)^T (K = 128 features, two K atoms of phi(K))
             SCAN_TRACE(t, 20);
-            ok = TIMED_WAIT(3, mbar_wait(&bar_phq, t & 1, &abort_flag)) && TIMED_WAIT(4, mbar_wait(&bar_phk[b], u & 1, &abort_flag));
+            ok = TIMED_WAIT(3, mbar_wait_lean(&bar_phq, t & 1, &abort_flag)) && TIMED_WAIT(4, mbar_wait_lean(&bar_phk[b], u & 1, &abort_flag));
             if (!ok) break;
             SCAN_TRACE(t, 0);
             tc_fence_after();
@@ -404,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             // inter: NUM = phi(Q_t) [S_<t | z_<t] (K = 128 features), plus phi(Q_t) S_lo
             SCAN_TRACE(t, 21);
-            ok = TIMED_WAIT(5, mbar_wait(&bar_snap, t & 1, &abort_flag)) && TIMED_WAIT(6, mbar_wait(&bar_numfree, (t & 1) ^ 1, &abort_flag));
+            ok = TIMED_WAIT(5, mbar_wait_lean(&bar_snap, t & 1, &abort_flag)) && TIMED_WAIT(6, mbar_wait_lean(&bar_numfree, (t & 1) ^ 1, &abort_flag));
             if (!ok) break;
             SCAN_TRACE(t, 1);
             tc_fence_after();
@@ -423,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             SCAN_TRACE(t, 2);
             // state: [S | z] += phi(K_t)^T [V_t | 1] (K = 128 tokens; phi(K) read MN-major, its
             // second 64-feature region LBO bytes on; the ones are the second N region of B)
-            if (!(ok = TIMED_WAIT(7, mbar_wait(&bar_vfull[b], u & 1, &abort_flag)))) break;
+            if (!(ok = TIMED_WAIT(7, mbar_wait_lean(&bar_vfull[b], u & 1, &abort_flag)))) break;
             tc_fence_after();
             if (leader) {
 #pragma unroll
@@ -437,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             SCAN_TRACE(t, 3);
             // intra: NUM += A~ [V_t | 1] (K = 128 keys, A~ packed in place of the scores)
             SCAN_TRACE(t, 22);
-            if (!(ok = TIMED_WAIT(8, mbar_wait(&bar_atil, t & 1, &abort_flag)))) break;
+            if (!(ok = TIMED_WAIT(8, mbar_wait_lean(&bar_atil, t & 1, &abort_flag)))) break;
             SCAN_TRACE(t, 4);
             tc_fence_after();
             if (leader) {
@@ -459,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (leader) mma_commit(&bar_drain);
         __syncwarp();
         volatile int never = 0;
-        mbar_wait(&bar_drain, 0, &never);
+        mbar_wait_lean(&bar_drain, 0, &never);
     } else if (warp < kKWarp0) {
         // ---------------- Q team: 8 warps ----------------
         const int qw = warp - kQWarp0;
@@ -470,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool failed = false;
         for (int t = 0; t < T; ++t) {
             const int b = t & 1, u = t >> 1;
-            failed |= !mbar_wait(&bar_pq[b], u & 1, &abort_flag);
+            failed |= !mbar_wait_lean(&bar_pq[b], u & 1, &abort_flag);
             if (warp == kQWarp0 && lane == 0) SCAN_TRACE(t, 6);
             __syncwarp();
             tc_fence_after();
@@ -527,11 +527,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool valid = t * kTile + r < p.n;
             float kn = 0.f;  // |k^_r|^2 / 2 in binary orders of magnitude
             if (exp_kind) {
-                failed |= !mbar_wait(&bar_kfull, t & 1, &abort_flag);
+                failed |= !mbar_wait_lean(&bar_kfull, t & 1, &abort_flag);
                 __syncwarp();
                 kn = 0.5f * s2 * tile_row_sqnorm<64>(sK, r) * kLog2e;
             }
-            failed |= !mbar_wait(&bar_pk[b], u & 1, &abort_flag);
+            failed |= !mbar_wait_lean(&bar_pk[b], u & 1, &abort_flag);
             if (warp == kKWarp0 && lane == 0) SCAN_TRACE(t, 8);
             __syncwarp();
             tc_fence_after();
@@ -570,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // phi(K_t) into buffer b once the MMAs of tile t-2 have read it
             if (t >= 2) {
-                failed |= !mbar_wait(&bar_phkfree[b], (u & 1) ^ 1, &abort_flag);
+                failed |= !mbar_wait_lean(&bar_phkfree[b], (u & 1) ^ 1, &abort_flag);
                 __syncwarp();
             }
             uint8_t* dst = sPK + b * kPhiBytes;
@@ -609,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0 && !withhold) mbar_arrive(&bar_snap);
         for (int t = 0; t < T; ++t) {
-            failed |= !mbar_wait(&bar_sc, t & 1, &abort_flag);
+            failed |= !mbar_wait_lean(&bar_sc, t & 1, &abort_flag);
             if (warp == kAWarp0 && lane == 0) SCAN_TRACE(t, 11);
             __syncwarp();
             tc_fence_after();
@@ -645,8 +645,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- the state image S_<t+1 once state(t) is done (rescaled if the key stabiliser rose)
             if (t + 1 < T) {
                 const int t1 = t + 1;
-                failed |= !mbar_wait(&bar_st, t & 1, &abort_flag);
-                failed |= !mbar_wait(&bar_beta[t1 & 3], (t1 >> 2) & 1, &abort_flag);
+                failed |= !mbar_wait_lean(&bar_st, t & 1, &abort_flag);
+                failed |= !mbar_wait_lean(&bar_beta[t1 & 3], (t1 >> 2) & 1, &abort_flag);
                 if (warp == kAWarp0 && lane == 0) SCAN_TRACE(t, 13);
                 __syncwarp();
                 tc_fence_after();
@@ -709,9 +709,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint4* yrow = reinterpret_cast<uint4*>(p.Y + ((size_t)bh * p.n + i_tok) * kD);
             const bool store = CS > 1 || i_tok < p.n;
             // the slot's previous tile has been read by every CTA of the cluster
-            if (CS > 1 && use > 0) failed |= !mbar_wait_cluster(&bar_rfree[slot], (use - 1) & 1, &abort_flag);
+            if (CS > 1 && use > 0) failed |= !mbar_wait_cluster_lean(&bar_rfree[slot], (use - 1) & 1, &abort_flag);
             if (warp == kOWarp0 && lane == 0) SCAN_TRACE(tt, 23);
-            failed |= !mbar_wait(&bar_num, tt & 1, &abort_flag);
+            failed |= !mbar_wait_lean(&bar_num, tt & 1, &abort_flag);
             if (warp == kOWarp0 && lane == 0) SCAN_TRACE(tt, 15);
             __syncwarp();
             tc_fence_after();
@@ -738,8 +738,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // the row's exponent offset: read before NUM is released, which lets the Q and
                     // K teams move on to the tiles that reuse these slots
                     if (exp_kind && CS > 1) {
-                        failed |= !mbar_wait(&bar_cq[tt & 1], (tt >> 1) & 1, &abort_flag);
-                        failed |= !mbar_wait(&bar_beta[tt & 3], (tt >> 2) & 1, &abort_flag);
+                        failed |= !mbar_wait_lean(&bar_cq[tt & 1], (tt >> 1) & 1, &abort_flag);
+                        failed |= !mbar_wait_lean(&bar_beta[tt & 3], (tt >> 2) & 1, &abort_flag);
                         e_own = sCq[(tt & 1) * 128 + r] + sBeta[tt & 3];
                     }
                     tmem_ld_wait();
@@ -864,7 +864,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(&bar_xread[slot]);
             };
             for (int tc = 0; tc < T; ++tc) {
-                failed |= !mbar_wait_cluster(&bar_rfull[tc % kRing], (tc / kRing) & 1, &abort_flag);
+                failed |= !mbar_wait_cluster_lean(&bar_rfull[tc % kRing], (tc / kRing) & 1, &abort_flag);
                 if (warp == kXWarp0 && lane == 0) SCAN_TRACE(tc, 17);
                 combine(tc);
                 if (warp == kXWarp0 && lane == 0) SCAN_TRACE(tc, 25);
@@ -883,7 +883,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint64_t* remote = full_side ? bar_rfull : bar_rfree;
             bool failed = false;
             for (int t = 0; t < T && !failed; ++t) {
-                failed |= !mbar_wait(&local[t % kRing], (t / kRing) & 1, &abort_flag);
+                failed |= !mbar_wait_lean(&local[t % kRing], (t / kRing) & 1, &abort_flag);
                 fence_acq_rel_cluster();
                 for (int o = 0; o < CS; ++o) mbar_arrive_relaxed_cluster(mapa(smem_u32(&remote[t % kRing]), o));
             }

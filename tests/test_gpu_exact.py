@@ -55,3 +55,33 @@ def test_exact_attention_rejects_unsupported(favor):
     x = torch.zeros(1, 1, 8, 128, device="cuda", dtype=torch.bfloat16)
     with pytest.raises(favor.FavorError):
         favor.favor_softmax_attn(x, x, x)
+
+
+def test_sweep_against_exact_attention(favor):
+    """bench.py --sweep: one JSON object per (form, n, m) with both wall clocks and the divergence of
+    FAVOR+ from the exact kernel; the divergence at n = 256 agrees with the same comparison made
+    by the oracle in fp64 on the same seeded inputs (up to the bf16 rounding of both GPU outputs,
+    amplified by the small norm of the exact output of diffuse attention)."""
+    import json
+    import os
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--sweep", "--sweep-n", "256,1024",
+                          "--sweep-m", "64,128"], capture_output=True, text=True, timeout=600, check=True).stdout
+    pts = [json.loads(line) for line in out.splitlines() if line.startswith("{")]
+    assert len(pts) == 8
+    assert {(p["form"], p["n"], p["m"]) for p in pts} == {(f, n, m) for f in ("noncausal", "causal")
+                                                          for n in (256, 1024) for m in (64, 128)}
+    for p in pts:
+        assert p["favor_ms"] > 0 and p["exact_ms"] > 0 and np.isfinite(p["rel_l2"]) and p["rel_l2"] > 0
+    p = next(p for p in pts if p["form"] == "noncausal" and p["n"] == 256 and p["m"] == 64)
+    w = si.Workload("sweep", 1, 8, 256, 64, 64, "bf16", False, kind="exp", seed=101 + 256, omega_seed=7)
+    full = si.full_inputs(w)
+    q, k, v = (si.to_f64(full[t]) for t in ("Q", "K", "V"))
+    _, om64 = si.omega_for(w)
+    yf = oracle.attn_noncausal(q, k, v, om64, kind="exp")
+    ye = oracle.softmax_attention(q, k, v)
+    ref = np.linalg.norm(yf - ye) / np.linalg.norm(ye)
+    assert abs(p["rel_l2"] - ref) <= 0.3 * ref, (p["rel_l2"], ref)
