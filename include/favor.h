@@ -55,7 +55,8 @@ typedef enum {
     FAVOR_ERR_MISALIGNED = 3,   /* a pointer is not 16-byte aligned (workspace: 256-byte)          */
     FAVOR_ERR_WORKSPACE = 4,    /* ws_bytes smaller than favor_workspace_bytes(...)                */
     FAVOR_ERR_CUDA = 5,         /* a CUDA runtime/driver call or kernel launch failed              */
-    FAVOR_ERR_TIMEOUT = 6       /* a device-side bounded wait gave up (reported after the fact)    */
+    FAVOR_ERR_TIMEOUT = 6,      /* a device-side bounded wait gave up (reported after the fact)    */
+    FAVOR_ERR_BOUNDS = 7        /* debug builds only: a device-side index check failed             */
 } favor_status_t;
 
 typedef enum { FAVOR_F32 = 0, FAVOR_BF16 = 1 } favor_dtype_t;
@@ -144,7 +145,9 @@ favor_status_t favor_attn_causal(const void* Q, const void* K, const void* V, co
  * FAVOR_OP_NONCAUSAL) exceeds it are rejected with FAVOR_ERR_WORKSPACE before anything runs.
  *
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress, with that
- * device current) and caches it; make that first call outside any CUDA stream capture. The call
+ * device current) and caches it with the current context; make that first call outside any CUDA
+ * stream capture. After a device reset (or any re-creation of the context) the next call looks the
+ * address up again, so that call too must be outside stream capture. The call
  * allocates nothing and frees nothing. All calls share the one array: two calls that may overlap
  * on the GPU (different streams, or several host threads) race on it and give undefined results,
  * so serialise them. The array keeps the last call's contents; nothing in it needs to start at
@@ -215,7 +218,8 @@ favor_status_t favor_softmax_attn(const void* Q, const void* K, const void* V, v
 const char* favor_status_string(favor_status_t status);
 
 /* Synchronises `stream`, then reads and clears the device error word of the current device.
- * Returns FAVOR_OK, FAVOR_ERR_TIMEOUT (a bounded device wait gave up) or FAVOR_ERR_CUDA. */
+ * Returns FAVOR_OK, FAVOR_ERR_TIMEOUT (a bounded device wait gave up), FAVOR_ERR_BOUNDS (a debug
+ * build's device-side index check failed; takes precedence) or FAVOR_ERR_CUDA. */
 favor_status_t favor_last_device_error(void* stream);
 
 /* FAVOR_ABI_VERSION of the loaded library. */

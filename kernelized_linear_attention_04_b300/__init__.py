@@ -36,7 +36,7 @@ _KINDS = {"exp": 0, "relu": 1, "elu": 2}
 _STABS = {"none": 0, "row": 1, "head": 2}
 _OPS = {"features": 0, "noncausal": 1, "causal": 2}
 _STATUS = {0: "FAVOR_OK", 1: "FAVOR_ERR_INVALID_ARG", 2: "FAVOR_ERR_UNSUPPORTED", 3: "FAVOR_ERR_MISALIGNED",
-           4: "FAVOR_ERR_WORKSPACE", 5: "FAVOR_ERR_CUDA", 6: "FAVOR_ERR_TIMEOUT"}
+           4: "FAVOR_ERR_WORKSPACE", 5: "FAVOR_ERR_CUDA", 6: "FAVOR_ERR_TIMEOUT", 7: "FAVOR_ERR_BOUNDS"}
 KERNEL_COUNT = 11
 # Size of the library's fixed scratch array used by favor_attn_noncausal_noalloc.
 NOALLOC_SCRATCH_BYTES = 16 << 20

@@ -16,9 +16,25 @@ constexpr int kStabHead = 2;
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Device error word: set (never trapped on) by a kernel whose bounded wait gave up.
+// Device error word: set (never trapped on) by a kernel whose bounded wait gave up, or, in a debug
+// build, whose bounds check failed.
 constexpr unsigned kDevErrTimeout = 1u;
+constexpr unsigned kDevErrBounds = 2u;
 __device__ unsigned int g_favor_error;
+
+// Debug builds (-DFAVOR_DEBUG, the stand-in for a memory checker) test the index of every
+// computed-address access to global memory, shared memory and tensor memory against its buffer:
+// a failed check records kDevErrBounds in the device error word and the guarded access is skipped.
+// Release builds compile the checks away (the guard is the constant true).
+#ifdef FAVOR_DEBUG
+__device__ __forceinline__ bool favor_in_bounds(bool ok) {
+    if (!ok) atomicOr(&g_favor_error, kDevErrBounds);
+    return ok;
+}
+#define FAVOR_IN_BOUNDS(cond) (::favor::favor_in_bounds(static_cast<bool>(cond)))
+#else
+#define FAVOR_IN_BOUNDS(cond) true
+#endif
 
 // Test hook, 0 (off) unless a caller arms it through favor_test_set_wait_limit: while it holds a
 // nonzero value, every bounded wait gives up after that many nanoseconds instead of its normal limit,

@@ -499,26 +499,54 @@ __device__ const Eye<uint16_t, 128> g_eye_bf16_128 = make_eye<uint16_t, 128>(0x3
 __device__ const Eye<float, 64> g_eye_f32_64 = make_eye<float, 64>(1.f);
 __device__ const Eye<float, 128> g_eye_f32_128 = make_eye<float, 128>(1.f);
 
-std::mutex g_eye_mu;
-void* g_eye_addr[64][4] = {};
-
-// Device address of the identity of head size d in dtype dt on the current device (looked up once
-// per device); nullptr on failure.
-const void* eye_ptr(int d, favor_dtype_t dt) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    const int k = (dt == FAVOR_BF16 ? 0 : 2) + (d == 128 ? 1 : 0);
-    std::lock_guard<std::mutex> g(g_eye_mu);
-    if (!g_eye_addr[dev][k]) {
+// Device addresses of the library's __device__ arrays, cached per (device, slot) together with the
+// context they were looked up in: after a device reset (or any teardown of the primary context) the
+// current context differs and the address is looked up again instead of being reused stale.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CUcontext current_context() {
+    static CtxGetCurrentFn fn = [] {
         void* p = nullptr;
-        cudaError_t e = k == 0 ? cudaGetSymbolAddress(&p, g_eye_bf16_64)
-                        : k == 1 ? cudaGetSymbolAddress(&p, g_eye_bf16_128)
-                        : k == 2 ? cudaGetSymbolAddress(&p, g_eye_f32_64)
-                                 : cudaGetSymbolAddress(&p, g_eye_f32_128);
-        if (e != cudaSuccess) return nullptr;
-        g_eye_addr[dev][k] = p;
+        cudaDriverEntryPointQueryResult q;
+        return cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+                       q == cudaDriverEntryPointSuccess
+                   ? reinterpret_cast<CtxGetCurrentFn>(p)
+                   : nullptr;
+    }();
+    CUcontext c = nullptr;
+    if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+    return c;
+}
+struct SymbolCache {
+    CUcontext ctx;
+    void* addr;
+};
+constexpr int kSymDevices = 64, kSymSlots = 5;  // slots 0-3: identities; 4: the no-alloc scratch
+std::mutex g_sym_mu;
+SymbolCache g_sym[kSymDevices][kSymSlots] = {};
+template <typename Sym>
+void* symbol_address(const Sym& symbol, int slot) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kSymDevices) return nullptr;
+    const CUcontext ctx = current_context();
+    std::lock_guard<std::mutex> g(g_sym_mu);
+    SymbolCache& e = g_sym[dev][slot];
+    if (!e.addr || e.ctx != ctx) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess || !p) return nullptr;
+        e.addr = p;
+        e.ctx = ctx;
     }
-    return g_eye_addr[dev][k];
+    return e.addr;
+}
+
+// Device address of the identity of head size d in dtype dt on the current device (cached per device
+// and context); nullptr on failure.
+const void* eye_ptr(int d, favor_dtype_t dt) {
+    const int k = (dt == FAVOR_BF16 ? 0 : 2) + (d == 128 ? 1 : 0);
+    return k == 0   ? symbol_address(g_eye_bf16_64, 0)
+           : k == 1 ? symbol_address(g_eye_bf16_128, 1)
+           : k == 2 ? symbol_address(g_eye_f32_64, 2)
+                    : symbol_address(g_eye_f32_128, 3);
 }
 
 favor_status_t check_ws(void* ws, size_t ws_bytes, size_t need) {
@@ -547,6 +575,7 @@ const char* favor_status_string(favor_status_t st) {
         case FAVOR_ERR_WORKSPACE: return "FAVOR_ERR_WORKSPACE: workspace smaller than favor_workspace_bytes()";
         case FAVOR_ERR_CUDA: return "FAVOR_ERR_CUDA: CUDA call or kernel launch failed";
         case FAVOR_ERR_TIMEOUT: return "FAVOR_ERR_TIMEOUT: a device-side bounded wait gave up";
+        case FAVOR_ERR_BOUNDS: return "FAVOR_ERR_BOUNDS: a device-side index check of a debug build failed";
     }
     return "unknown favor_status_t";
 }
@@ -758,21 +787,11 @@ namespace {
 // cudaGetSymbolAddress returns for the current device.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[FAVOR_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void* g_noalloc_addr[kMaxDevices] = {};
-
-// Device address of g_noalloc_scratch on the current device, looked up once per device.
+// Device address of g_noalloc_scratch on the current device (cached per device and context).
 favor_status_t noalloc_scratch(void** out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FAVOR_ERR_CUDA;
-    std::lock_guard<std::mutex> g(g_noalloc_mu);
-    if (!g_noalloc_addr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return FAVOR_ERR_CUDA;
-        g_noalloc_addr[dev] = p;
-    }
-    *out = g_noalloc_addr[dev];
+    void* p = symbol_address(g_noalloc_scratch, 4);
+    if (!p) return FAVOR_ERR_CUDA;
+    *out = p;
     return FAVOR_OK;
 }
 
@@ -802,7 +821,7 @@ favor_status_t favor_last_device_error(void* stream) {
     if (v == 0) return FAVOR_OK;
     unsigned zero = 0;
     if (cudaMemcpyToSymbol(g_favor_error, &zero, sizeof(zero)) != cudaSuccess) return FAVOR_ERR_CUDA;
-    return FAVOR_ERR_TIMEOUT;
+    return (v & kDevErrBounds) ? FAVOR_ERR_BOUNDS : FAVOR_ERR_TIMEOUT;
 }
 
 favor_status_t favor_softmax_attn(const void* Q, const void* K, const void* V, void* Y, int B, int H, int n, int d,

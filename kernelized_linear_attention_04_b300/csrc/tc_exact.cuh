@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         lb[h * 128 + r] = l;
         named_bar(1, 32 * kSoftWarps);
         const float inv = 1.f / (lb[r] + lb[128 + r]);
-        if (i_tok < p.n) {
+        if (i_tok < p.n && FAVOR_IN_BOUNDS(bh < (int)gridDim.y && 32 * h + 32 <= kD)) {
             uint4* dst = reinterpret_cast<uint4*>(p.Y + ((size_t)bh * p.n + i_tok) * kD + 32 * h);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {

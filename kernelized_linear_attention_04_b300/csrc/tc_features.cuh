@@ -226,7 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     o[i] = exp_kind ? ex2(fmaf(a, A2, -stab_r - lsm)) : phi_plain(a * p.scale, p.kind, inv_sqrt_m, p.relu_eps);
                 }
                 const int f0 = cg * Wf + c0;
-                if (valid) {
+                // (features past m, in the padding of the last group, are skipped by the guards below)
+                if (valid && FAVOR_IN_BOUNDS(bh < (int)gridDim.y && row < p.n)) {
                     float* dst = p.Phi + ((size_t)bh * p.n + row) * p.m + f0;
                     if (f0 + 32 <= p.m && (p.m & 3) == 0) {
 #pragma unroll

@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         failed |= !mbar_wait(&bar_s, 0, &abort_flag);
         __syncwarp();
         tc_fence_after();
-        if (tm < G) {
+        if (tm < G && FAVOR_IN_BOUNDS(bh * T + rank < (int)gridDim.x && tm * 128 + r < MP)) {
             const int feat = tm * 128 + r;
             uint32_t v[32];
             tmem_ld32(tbase + lane_off + 64 * tm + 32 * cg, v);
@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld16(tbase + lane_off + 16 * cg4, nv);
         tmem_ld2(tbase + lane_off + kD, d0, d1);
         tmem_ld_wait();
-        if (r < nvalid) {
+        if (r < nvalid && FAVOR_IN_BOUNDS(j0 + r < p.n && bh * T + rank < (int)gridDim.x && 16 * cg4 + 16 <= kD)) {
             const float inv = 1.f / (__uint_as_float(d0) + __uint_as_float(d1));
             uint4* dst = reinterpret_cast<uint4*>(p.Y + ((size_t)bh * p.n + j0 + r) * kD + 16 * cg4);
 #pragma unroll

@@ -621,6 +621,7 @@ __global__ void __launch_bounds__(128) nc_combine(const float* __restrict__ pS, 
                          pack_bf16(acc[6], acc[7]));
     const int a = ch / 8, c = ch % 8;
     uint8_t* img = Simg + (size_t)bh * m_pad * D * 2 + (size_t)a * m_pad * 128;
+    if (!FAVOR_IN_BOUNDS(bh < (int)gridDim.y && row < m_pad && a < D / 64)) return;
     *reinterpret_cast<uint4*>(img + row * 128 + ((c ^ (row & 7)) << 4)) = o;
     if (ch == 0) zout[(size_t)bh * m_pad + row] = zs;
 }
@@ -933,7 +934,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(&bar_ufree[s]);
             // Each thread stores whole 32-byte sectors of its own row (rows past n are not written).
             const int row = (t0 + t) * kTile + r;
-            if (row < p.n) {
+            if (row < p.n && FAVOR_IN_BOUNDS(bh < (int)gridDim.y && (cg + 1) * kC <= D)) {
                 uint4* dst = reinterpret_cast<uint4*>(p.Y + ((size_t)bh * p.n + row) * D + cg * kC);
 #pragma unroll
                 for (int cc = 0; cc < kC / 8; ++cc) {

@@ -189,6 +189,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int bh = blockIdx.x / CS;
+    // extents for the debug build's bounds checks: output rows, one head's ring
+    [[maybe_unused]] const size_t y_rows = (size_t)(gridDim.x / CS) * p.n;
+    [[maybe_unused]] const size_t ring_head = (size_t)kRing * CS * kXChunks * kTile * 16;
     const int T = (p.n + kTile - 1) / kTile;
     constexpr bool exp_kind = KIND == kKindExp;
     constexpr bool hilo = exp_kind;     // state image with its rounding remainder
@@ -589,6 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 features16(v, w, 32 * cc < fv, ck);
 #pragma unroll
                 for (int k4 = 0; k4 < 4; ++k4)
+                    if (FAVOR_IN_BOUNDS(dst - sPK + (cc >> 1) * 16384 + sw128_offset(r, (cc & 1) * 4 + k4) + 16 <= 2 * kPhiBytes))
                     *reinterpret_cast<uint4*>(dst + (cc >> 1) * 16384 + sw128_offset(r, (cc & 1) * 4 + k4)) =
                         make_uint4(w[4 * k4] & keep, w[4 * k4 + 1] & keep, w[4 * k4 + 2] & keep, w[4 * k4 + 3] & keep);
             }
@@ -667,11 +671,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const uint4 o = pack8_hi(v + 8 * c);
-                        *reinterpret_cast<uint4*>(sSnap + sw128_offset(r, 4 * hh + c)) = o;
+                        if (FAVOR_IN_BOUNDS(sw128_offset(r, 4 * hh + c) + 16 <= kTileBytes))
+                            *reinterpret_cast<uint4*>(sSnap + sw128_offset(r, 4 * hh + c)) = o;
                         if (hilo) {
                             const uint4 ol = make_uint4(lo_pair(v[8 * c + 0], v[8 * c + 1], o.x), lo_pair(v[8 * c + 2], v[8 * c + 3], o.y),
                                                         lo_pair(v[8 * c + 4], v[8 * c + 5], o.z), lo_pair(v[8 * c + 6], v[8 * c + 7], o.w));
-                            *reinterpret_cast<uint4*>(sSlo + sw128_offset(r, 4 * hh + c)) = ol;
+                            if (FAVOR_IN_BOUNDS(sw128_offset(r, 4 * hh + c) + 16 <= kTileBytes))
+                                *reinterpret_cast<uint4*>(sSlo + sw128_offset(r, 4 * hh + c)) = ol;
                         }
                     }
                 }
@@ -779,14 +785,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const uint4 o = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-                        if (CS == 1) yrow[4 * h + c] = o;
-                        else __stcg(reinterpret_cast<uint4*>(rec + (4 * h + c) * kTile * 16), o);
+                        if (CS == 1) {
+                            if (FAVOR_IN_BOUNDS((size_t)bh * p.n + i_tok < y_rows)) yrow[4 * h + c] = o;
+                        } else if (FAVOR_IN_BOUNDS((size_t)(rec - ring) + (4 * h + c) * kTile * 16 + 16 <= ring_head)) {
+                            __stcg(reinterpret_cast<uint4*>(rec + (4 * h + c) * kTile * 16), o);
+                        }
                     }
                 }
             }
             if (CS > 1) {
                 // the row's log-weight: log2(den) plus its exponent offset (-inf: no weight)
                 const float l_own = den_own > 0.f ? log2_pos(den_own) + e_own : -INFINITY;
+                if (FAVOR_IN_BOUNDS((size_t)(rec - ring) + 8 * kTile * 16 + 16 <= ring_head))
                 __stcg(reinterpret_cast<uint4*>(rec + 8 * kTile * 16),
                        make_uint4(__float_as_uint(l_own), __float_as_uint(sc0), __float_as_uint(sc1), 0u));
                 // the warp's partial rows of this tile are stored (released at CTA scope; the
@@ -826,6 +836,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             continue;
                         }
                         const uint8_t* rec = ring + ((size_t)(slot * CS + g) * kXChunks) * kTile * 16 + row * 16;
+                        if (!FAVOR_IN_BOUNDS((size_t)(rec - ring) + 8 * kTile * 16 + 16 <= ring_head)) {
+                            meta[g] = make_uint4(0xFF800000u, 0u, 0u, 0u);
+                            yv[g][0] = yv[g][1] = make_uint4(0u, 0u, 0u, 0u);
+                            continue;
+                        }
                         meta[g] = __ldcg(reinterpret_cast<const uint4*>(rec + 8 * kTile * 16));
 #pragma unroll
                         for (int k = 0; k < 2; ++k) yv[g][k] = __ldcg(reinterpret_cast<const uint4*>(rec + (c0 + k) * kTile * 16));
@@ -855,6 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 acc[2 * e + 1] = fmaf(ws[g], y2.y, acc[2 * e + 1]);
                             }
                         }
+                        if (FAVOR_IN_BOUNDS((size_t)bh * p.n + tok < y_rows && c0 + k < 8))
                         dst[k] = make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
                                             pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
                     }

@@ -34,7 +34,7 @@ def test_library_loads_and_exports_every_declared_symbol():
 def test_status_strings_and_kernel_names():
     import kernelized_linear_attention_04_b300 as favor
 
-    for code in range(7):
+    for code in range(8):
         assert favor.lib.favor_status_string(code).decode().startswith("FAVOR_")
     assert favor.KERNEL_NAMES[0] == "features"
     assert favor.KERNEL_NAMES[-1] == "exact"

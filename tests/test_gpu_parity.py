@@ -155,6 +155,7 @@ def test_features_small_cases(favor, dtype, kind, stab, n, d, m):
     w = si.Workload("case", 2, 2, n, d, m, dtype, False, kind=kind, seed=9 + n, omega_seed=3 + d)
     Q, _, _, Om, om64 = device_inputs(w)
     P = favor.favor_features(Q, Om, kind=kind, relu_eps=w.relu_eps, stab=stab)
+    assert favor.last_device_error() == 0
     ref = oracle.features(f64(Q), om64, kind=kind, relu_eps=w.relu_eps, stab=stab)
     assert_close_features(P.cpu().numpy(), ref, m, f"{dtype} {kind} {stab} n={n}")
 
