@@ -180,8 +180,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* sCq = reinterpret_cast<float*>(smem + kOffCq);
     float* sMx = reinterpret_cast<float*>(smem + kOffMx);
     __shared__ uint64_t bar_om, bar_kfull, bar_kfree, bar_qfull, bar_qfree, bar_vfull[2], bar_vfree[2];
-    __shared__ uint64_t bar_pk[2], bar_pkfree[2], bar_pq[2], bar_phq, bar_phk[2], bar_phkfree[2];
-    __shared__ uint64_t bar_sc, bar_atil, bar_st, bar_snap, bar_num, bar_numfree, bar_beta[4], bar_cq[2];
+    __shared__ uint64_t bar_pk[2], bar_pkfree[2], bar_pq[2], bar_scr[2], bar_phkfree[2];
+    __shared__ uint64_t bar_sc, bar_atil, bar_st, bar_inter, bar_num, bar_beta[4], bar_cq[2];
     __shared__ uint64_t bar_drain, bar_rfull[kRing], bar_rfree[kRing], bar_ostore[kRing], bar_xread[kRing];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
@@ -234,18 +234,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bar_pk[b], 1);
             mbar_init(&bar_pkfree[b], kKWarps);
             mbar_init(&bar_pq[b], 1);
-            mbar_init(&bar_phk[b], kKWarps);
+            // the scores of tile t may start: phi(Q_t) packed (Q team) and phi(K_t) stored (K team)
+            mbar_init(&bar_scr[b], kQWarps + kKWarps);
             mbar_init(&bar_phkfree[b], 1);
             mbar_init(&bar_cq[b], kQWarps / 2);
         }
         for (int b = 0; b < 4; ++b) mbar_init(&bar_beta[b], 1);
-        mbar_init(&bar_phq, kQWarps);
         mbar_init(&bar_sc, 1);
         mbar_init(&bar_atil, kAWarps);
         mbar_init(&bar_st, 1);
-        mbar_init(&bar_snap, kAWarps);
+        // the inter MMA of tile t may start: the state image of S_<t (A team) and NUM drained (O team)
+        mbar_init(&bar_inter, kAWarps + kOWarps);
         mbar_init(&bar_num, 1);
-        mbar_init(&bar_numfree, kOWarps);
         mbar_init(&bar_drain, 1);
         for (int i = 0; i < kRing; ++i) {
             // a slot's partial rows of this CTA's rows: one arrive per feeding warp of every CTA
@@ -394,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t num = tbase + kColNum;
             // scores: SC = phi(Q_t) phi(K_t)^T (K = 128 features, two K atoms of phi(K))
             SCAN_TRACE(t, 20);
-            ok = TIMED_WAIT(3, mbar_wait_lean(&bar_phq, t & 1, &abort_flag)) && TIMED_WAIT(4, mbar_wait_lean(&bar_phk[b], u & 1, &abort_flag));
+            ok = TIMED_WAIT(3, mbar_wait_lean(&bar_scr[b], u & 1, &abort_flag));
             if (!ok) break;
             SCAN_TRACE(t, 0);
             tc_fence_after();
@@ -407,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             // inter: NUM = phi(Q_t) [S_<t | z_<t] (K = 128 features), plus phi(Q_t) S_lo
             SCAN_TRACE(t, 21);
-            ok = TIMED_WAIT(5, mbar_wait_lean(&bar_snap, t & 1, &abort_flag)) && TIMED_WAIT(6, mbar_wait_lean(&bar_numfree, (t & 1) ^ 1, &abort_flag));
+            ok = TIMED_WAIT(5, mbar_wait_lean(&bar_inter, t & 1, &abort_flag));
             if (!ok) break;
             SCAN_TRACE(t, 1);
             tc_fence_after();
@@ -512,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar_phq);
+            if (lane == 0) mbar_arrive(&bar_scr[b]);
             if (warp == kQWarp0 && lane == 0) SCAN_TRACE(t, 7);
         }
         (void)failed;
@@ -598,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar_phk[b]);
+            if (lane == 0) mbar_arrive(&bar_scr[b]);
             if (warp == kKWarp0 && lane == 0) SCAN_TRACE(t, 10);
         }
         (void)failed;
@@ -611,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool withhold = g_favor_test_wait_ns != 0;  // test hook: never publish the first state image
         // the state image before tile 0 (zero) is in place
         __syncwarp();
-        if (lane == 0 && !withhold) mbar_arrive(&bar_snap);
+        if (lane == 0 && !withhold) mbar_arrive(&bar_inter);
         for (int t = 0; t < T; ++t) {
             failed |= !mbar_wait_lean(&bar_sc, t & 1, &abort_flag);
             if (warp == kAWarp0 && lane == 0) SCAN_TRACE(t, 11);
@@ -694,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_async_smem();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bar_snap);
+                if (lane == 0) mbar_arrive(&bar_inter);
                 if (warp == kAWarp0 && lane == 0) SCAN_TRACE(t, 14);
             }
         }
@@ -707,6 +707,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool failed = false;
         // This CTA's part of the head's ring: [slot][rank][chunk][row] x 16 bytes.
         uint8_t* ring = CS > 1 ? p.ring + (size_t)bh * kRing * CS * kXChunks * kTile * 16 : nullptr;
+        // NUM is free for the first tile's inter MMA
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_inter);
         for (int tt = 0; tt < T; ++tt) {
             const int slot = tt % kRing, use = tt / kRing;
             const int i_tok = tt * kTile + r;
@@ -751,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_wait();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&bar_numfree);  // NUM may take the next tile's inter MMA
+                    if (lane == 0) mbar_arrive(&bar_inter);  // NUM may take the next tile's inter MMA
                     if (warp == kOWarp0 && lane == 0) SCAN_TRACE(tt, 16);
                 }
                 // half row h: alone, the bf16 output; in a cluster, fp16 times a power-of-two scale 2^ex
