@@ -119,12 +119,16 @@ favor_status_t favor_attn_noncausal(const void* Q, const void* K, const void* V,
  * Computed as a chunked scan: per chunk, an intra-chunk lower-triangular block plus the carried
  * prefix state. chunk: 0 (implementation default), 64 or 128; the result does not depend on it
  * beyond rounding. bf16 with d = 64 and m <= 512 runs a tensor-core scan, one CTA per 128-feature
- * group and a thread-block cluster of ceil(m / 128) CTAs per head, which carries the state every
- * 128 tokens and masks j <= i inside each 128-token tile (two 64-token chunks give exactly that
- * sum); other inputs run on CUDA cores in 16-token steps. Shapes and dtypes as above. Workspace
- * (favor_workspace_bytes): 0 bytes for m <= 128; for m > 128 the CTAs of a head exchange their
- * partial output rows through it (B*H * 4 * ceil(m/128) * 18432 bytes; its contents on entry
- * do not matter).
+ * group and a group of CS = ceil(m / 128) CTAs per head (a persistent grid of at most one CTA per
+ * SM, each group taking heads in turn; launched cooperatively when CS > 1), which carries the state
+ * every 128 tokens and masks j <= i inside each 128-token tile (two 64-token chunks give exactly
+ * that sum); other inputs run on CUDA cores in 16-token steps. Shapes and dtypes as above.
+ * Workspace (favor_workspace_bytes): 0 bytes for m <= 128; for m > 128 the CTAs of a group count
+ * and exchange their partial output rows through it: for G = min(B*H, 160 / CS) groups, 64 bytes
+ * of counters each (the whole rounded up to 256 bytes), then G * 4 * CS * 18432 bytes. Its
+ * contents on entry do not matter (the counters are cleared on the stream before the launch). The
+ * scan takes every SM of the device: a kernel running beside it on another stream delays its
+ * start.
  */
 favor_status_t favor_attn_causal(const void* Q, const void* K, const void* V, const void* Omega, void* Y,
                                  int B, int H, int n, int d, int m, int chunk, favor_dtype_t dt,

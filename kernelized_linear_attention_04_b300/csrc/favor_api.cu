@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -403,30 +404,49 @@ favor_status_t tc_noncausal(const void* Q, const void* K, const void* V, const v
     return lerr == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;
 }
 
+// SMs of the current device (cached per device ordinal; 0 on failure).
+int sm_count() {
+    constexpr int kDevices = 64;
+    static std::atomic<int> cache[kDevices] = {};
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevices) return 0;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v == 0 && cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) cache[dev].store(v);
+    return v;
+}
+
+// The causal scan as a persistent grid: G groups of cs CTAs (one per SM at most), group g taking
+// the heads g, g + G, ...; with cs > 1 the groups' CTAs signal each other through counters in the
+// workspace, so the launch is cooperative (all CTAs resident together) and the counters are
+// cleared first.
 favor_status_t tc_causal(const void* Q, const void* K, const void* V, const void* Om, void* Y, int B, int H, int n,
                          int m, int kind, float eps, void* ws, cudaStream_t s) {
     const int BH = B * H;
     const int cs = m_padded(m) / 128;
+    const int sms = sm_count();
+    if (sms < cs) return FAVOR_ERR_CUDA;
+    const int G = std::min(tcs::ScanWs::max_groups((size_t)BH, cs), sms / cs);
     CUtensorMap mQ, mK, mV, mOm;
     if (!tma::encode_bf16_3d(&mQ, Q, 64, n, BH, 64, tcs::kTile) || !tma::encode_bf16_3d(&mK, K, 64, n, BH, 64, tcs::kTile) ||
         !tma::encode_bf16_3d(&mV, V, 64, n, BH, 64, tcs::kTile) || !tma::encode_bf16_2d(&mOm, Om, 64, m, 64, 128))
         return FAVOR_ERR_CUDA;
     uint8_t* wsb = static_cast<uint8_t*>(ws);
+    uint32_t* flags = cs > 1 ? reinterpret_cast<uint32_t*>(wsb) : nullptr;
+    uint8_t* ring = cs > 1 ? wsb + tcs::ScanWs::flag_bytes((size_t)BH, cs) : nullptr;
     tcs::ScanParams sp{n, m, kind, eps * std::sqrt((float)m), feat_scale(64, kind), static_cast<__nv_bfloat16*>(Y),
-                       cs > 1 ? wsb : nullptr};
+                       BH, cs, ring, flags};
     const size_t smem = tcs::ScanSmem::bytes();
     auto kern = kind == kKindExp ? tcs::causal_scan<kKindExp> : kind == kKindRelu ? tcs::causal_scan<kKindRelu> : tcs::causal_scan<kKindElu>;
     FAVOR_TRY(set_smem(kern, smem));
+    if (cs > 1 && cudaMemsetAsync(flags, 0, (size_t)G * tcs::kFlagWords * 4, s) != cudaSuccess) return FAVOR_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = cs > 1 ? 1 : 0;
     cfg.stream = s;
-    cfg.gridDim = dim3(BH * cs, 1, 1);
+    cfg.gridDim = dim3(G * cs, 1, 1);
     cfg.blockDim = dim3(tcs::kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cudaError_t lerr = cudaSuccess;

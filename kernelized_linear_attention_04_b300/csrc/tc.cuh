@@ -82,6 +82,7 @@ __device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, v
     const uint64_t t0 = globaltimer();
     const uint64_t tlim = g_favor_test_wait_ns;
     const uint64_t limit = tlim ? tlim : kWaitLimitNs;
+    if (*abort_flag) return false;  // another role gave up: no wait runs to its limit after that
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 255u) != 0) continue;
@@ -149,6 +150,39 @@ __device__ __forceinline__ bool mbar_wait_cluster_lean(uint64_t* bar, uint32_t p
 
 // Orders this thread's earlier memory accesses before its later ones for all threads of the cluster.
 __device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
+// Counters in global memory between the CTAs of one launch (they must all be resident together:
+// a cooperative launch). The writer fences, then adds: its earlier writes, and those it has
+// acquired from its own CTA, are visible to a reader whose acquiring load sees the sum.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ void counter_add_relaxed(uint32_t* a, uint32_t v) {
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* a) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+    return v;
+}
+// Waits until the counter *a reaches `target` (modulo 2^32), bounded like mbar_wait.
+__device__ __noinline__ bool counter_wait_poll(const uint32_t* a, uint32_t target, volatile int* abort_flag) {
+    const uint64_t t0 = globaltimer();
+    const uint64_t tlim = g_favor_test_wait_ns;
+    const uint64_t limit = tlim ? tlim : kWaitLimitNs;
+    for (uint32_t it = 0;; ++it) {
+        if ((int32_t)(ld_acquire_gpu(a) - target) >= 0) return true;
+        if ((it & 15u) != 0) continue;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > limit) {
+            atomicOr(&g_favor_error, kDevErrTimeout);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+__device__ __forceinline__ bool counter_wait(const uint32_t* a, uint32_t target, volatile int* abort_flag) {
+    if ((int32_t)(ld_acquire_gpu(a) - target) >= 0) return true;
+    return counter_wait_poll(a, target, abort_flag);
+}
 
 // ---------------------------------------------------------------------------------------------
 // Thread-block clusters: rank, distributed shared memory, remote arrivals, cluster barrier

@@ -1,18 +1,25 @@
 // Tensor-core (tcgen05 + TMA + TMEM) causal FAVOR+ scan, bf16 in / fp32 accumulate, d = 64,
 // m <= 512.
 //
-// One thread-block cluster of CS = ceil(m / 128) CTAs walks the 128-token tiles of one head in
-// order; CTA `rank` owns the features [128 rank, 128 rank + 128). Per tile t (query rows i, keys j
-// of the tile) each CTA forms, over its own features,
+// A group of CS = ceil(m / 128) CTAs walks the 128-token tiles of one head in order; CTA `rank`
+// of the group owns the features [128 rank, 128 rank + 128). Per tile t (query rows i, keys j of
+// the tile) each CTA forms, over its own features,
 //   num_i = phi(q_i) S_<t + sum_{j <= i} (phi(q_i) . phi(k_j)) v_j
 //   den_i = phi(q_i) z_<t + sum_{j <= i}  phi(q_i) . phi(k_j)
 // and then S_<t+1 = S_<t + Phi(K_t)^T V_t, z_<t+1 = z_<t + Phi(K_t)^T 1 ("Performer for vision",
 // *How It Works*, Step 2: prefix sums; the state is carried every 128 tokens and keys are masked
 // by j <= i inside the tile, which for two 64-token chunks is exactly their chunked prefix sum).
-// The CTAs of a cluster then combine their partial results row by row: each writes its partial
-// rows of tile t into a ring of kRing tiles in global memory (L2-resident) and signals the rows'
-// owners through their mbarriers a tile later; a separate warp team of each CTA combines the rows
-// it finalises, so that neither the tensor-core pipeline nor the NUM drain waits on a peer.
+// The CTAs of a group then combine their partial results row by row: each writes its partial rows
+// of tile t into a ring of kRing tiles in global memory (L2-resident) and counts them into the
+// group's counters; a separate warp team of each CTA combines the rows it finalises once every
+// CTA's rows are counted in, so that neither the tensor-core pipeline nor the NUM drain waits on
+// a peer.
+//
+// The grid is persistent: G groups (at most one CTA per SM, all resident together, launched
+// cooperatively when CS > 1), group g taking the heads g, g + G, g + 2G, ... one after another.
+// The groups need no common GPC, as thread-block clusters would (four-CTA clusters leave SMs of
+// every GPC idle). Within a CTA the tiles of all its heads form one sequence (index gt) that
+// drives every buffer and barrier phase; at a head's first tile the state restarts from zero.
 //
 // Every contraction runs on the tensor cores, with the A operand in TMEM wherever it is produced
 // there:
@@ -38,9 +45,9 @@
 //                and, read transposed, the state's A operand); the running key stabiliser.
 //   warps 14-17  A team: SC -> A~ (masked by j <= i, bf16) in place; then the bf16 image of
 //                [S | z] after the state update (rescaled first if the key stabiliser rose).
-//   warps 18-21  O team: NUM -> y (alone: the output; in a cluster: the partial rows, to the ring).
-//   warps 22-25  X team (cluster only): the rows this CTA finalises, from the ring's partials.
-//   warps 26-27  signal warps (cluster only): release a tile's stored partial rows to the cluster,
+//   warps 18-21  O team: NUM -> y (alone: the output; in a group: the partial rows, to the ring).
+//   warps 22-25  X team (CS > 1 only): the rows this CTA finalises, from the ring's partials.
+//   warps 26-27  signal warps (CS > 1 only): release a tile's stored partial rows to the group,
 //                and report the slots the X team has read.
 //
 // Stabilisers (exp family; Y does not depend on them, both cancel between num and den):
@@ -49,7 +56,7 @@
 //   keys: a running constant per CTA, the exact largest exponent w_r . k^_j - |k^_j|^2/2 seen so
 //   far over the CTA's features and the head's keys, raised (and the state rescaled) only when a
 //   tile exceeds it by more than kSlackHi binary orders of magnitude;
-//   across the cluster, each CTA's partial row y_g = num_g / den_g carries the log-weight
+//   across the group, each CTA's partial row y_g = num_g / den_g carries the log-weight
 //   l_g = log2(den_g) + c_i + beta; the owner of the row weights the partials by 2^(l_g - max l).
 // The common factor 1/sqrt(m) is dropped. The generalized-ReLU and elu + 1 families have no
 // stabiliser.
@@ -69,7 +76,7 @@ using tcnc::tile_row_sqnorm;
 
 constexpr int kTile = 128;
 constexpr int kD = 64;
-constexpr int kMaxCluster = 4;                    // m <= 512
+constexpr int kMaxCluster = 4;                    // m <= 512: CTAs per group
 constexpr int kQWarp0 = 2, kQWarps = 8;
 constexpr int kKWarp0 = kQWarp0 + kQWarps, kKWarps = 4;
 constexpr int kAWarp0 = kKWarp0 + kKWarps, kAWarps = 4;
@@ -83,6 +90,8 @@ constexpr int kPrefetch = 3;                        // tiles of K, Q, V prefetch
 constexpr int kRing = 4;                            // tiles of partial rows in flight per head
 constexpr int kXChunks = 9;                         // 16-byte chunks of a partial row: 8 of y (fp16), log-weight and scales
 constexpr float kSlackHi = 16.f;                    // key stabiliser rises once exceeded by 2^16
+constexpr int kMaxCtas = 160;                       // persistent grid bound (at least a device's SMs)
+constexpr int kFlagWords = 16;                      // per group: kRing full and kRing free counters, padded
 
 // Timeline of one CTA for profiling builds (compiled with -DFAVOR_SCAN_TRACE): the SM clock at
 // named points of each role, for the first kTraceTiles tiles of CTA 0. Off in the library.
@@ -132,16 +141,23 @@ struct ScanParams {
     float relu_eps_s;  // relu_eps * sqrt(m): the features are scaled by sqrt(m) (a common factor)
     float scale;       // d^-1/4 (1 for elu + 1)
     __nv_bfloat16* Y;
-    uint8_t* ring;     // cluster > 1: per head kRing x CS x kXChunks x 128 rows x 16 bytes (ScanWs)
+    int bh;            // heads (B * H)
+    int cs;            // CTAs per group, ceil(m / 128)
+    uint8_t* ring;     // cs > 1: per group kRing x cs x kXChunks x 128 rows x 16 bytes (ScanWs)
+    uint32_t* flags;   // cs > 1: per group kFlagWords counters, zero at launch (ScanWs)
 };
 
 struct ScanSmem {
     static size_t bytes() { return 1024 + kOffEnd; }
 };
 
-// Workspace of the scan: the ring of partial rows (only for a cluster).
+// Workspace of the scan (only for cs > 1): the groups' counters, then their rings of partial rows.
+// Sized for the largest grid any device may get, min(BH, kMaxCtas / cs) groups.
 struct ScanWs {
-    static size_t bytes(size_t BH, int cs) { return cs > 1 ? BH * kRing * cs * kXChunks * kTile * 16 : 0; }
+    static int max_groups(size_t BH, int cs) { return (int)(BH < (size_t)(kMaxCtas / cs) ? BH : (size_t)(kMaxCtas / cs)); }
+    static size_t flag_bytes(size_t BH, int cs) { return ((size_t)max_groups(BH, cs) * kFlagWords * 4 + 255) & ~size_t(255); }
+    __host__ __device__ static size_t ring_bytes(int cs) { return (size_t)kRing * cs * kXChunks * kTile * 16; }
+    static size_t bytes(size_t BH, int cs) { return cs > 1 ? flag_bytes(BH, cs) + max_groups(BH, cs) * ring_bytes(cs) : 0; }
 };
 
 // bf16 image of 8 fp32 values as one 16-byte chunk, and (lo) the bf16 rounding of what the first
@@ -164,9 +180,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mOm, ScanParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];  // aligned to 1024 by hand below
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int CS = (int)cluster_size();
-    const int rank = (int)cluster_rank();
-    const int RP = (kTile + CS - 1) / CS;  // rows finalised by each CTA of the cluster
+    const int CS = p.cs;
+    const int G = (int)gridDim.x / CS;  // groups
+    const int grp = (int)blockIdx.x / CS, rank = (int)blockIdx.x % CS;
+    const int RP = (kTile + CS - 1) / CS;  // rows finalised by each CTA of the group
     const int feat0 = rank * 128;
     uint8_t* sOm = smem + kOffOm;
     uint8_t* sQ = smem + kOffQ;
@@ -188,11 +205,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ float sBeta[4], sF[4], sKmx[4];
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int bh = blockIdx.x / CS;
-    // extents for the debug build's bounds checks: output rows, one head's ring
-    [[maybe_unused]] const size_t y_rows = (size_t)(gridDim.x / CS) * p.n;
-    [[maybe_unused]] const size_t ring_head = (size_t)kRing * CS * kXChunks * kTile * 16;
+    // extents for the debug build's bounds checks: output rows, one group's ring
+    [[maybe_unused]] const size_t y_rows = (size_t)p.bh * p.n;
+    [[maybe_unused]] const size_t ring_head = ScanWs::ring_bytes(CS);
     const int T = (p.n + kTile - 1) / kTile;
+    // This CTA's tiles: those of its group's heads grp, grp + G, ..., one sequence gt in [0, GT).
+    // Roles that need a tile's head and place in it follow them with seq_next.
+    const int GT = (p.bh - grp + G - 1) / G * T;
+    auto seq_next = [&](int& hd, int& tl) {
+        if (++tl == T) {
+            tl = 0;
+            hd += G;
+        }
+    };
+    // the group's ring and counters (full: [0, kRing), free: [kRing, 2 kRing))
+    uint8_t* const ring_grp = CS > 1 ? p.ring + (size_t)grp * ScanWs::ring_bytes(CS) : nullptr;
+    uint32_t* const flags = CS > 1 ? p.flags + (size_t)grp * kFlagWords : nullptr;
     constexpr bool exp_kind = KIND == kKindExp;
     constexpr bool hilo = exp_kind;     // state image with its rounding remainder
     const float A2 = p.scale * kLog2e;  // projections -> exponents in binary orders of magnitude
@@ -248,10 +276,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bar_num, 1);
         mbar_init(&bar_drain, 1);
         for (int i = 0; i < kRing; ++i) {
-            // a slot's partial rows of this CTA's rows: one arrive per feeding warp of every CTA
-            mbar_init(&bar_rfull[i], CS);
-            // this CTA's slot has been read by every CTA of the cluster
-            mbar_init(&bar_rfree[i], CS);
+            // every CTA of the group has stored its partial rows of the slot's tile / read them
+            mbar_init(&bar_rfull[i], 1);
+            mbar_init(&bar_rfree[i], 1);
             // this CTA's partial rows of a slot are stored / its X team has read a slot
             mbar_init(&bar_ostore[i], kOWarps);
             mbar_init(&bar_xread[i], kXWarps);
@@ -271,7 +298,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_async_smem();
     if (warp == 1) tmem_alloc(&tmem_base, 512);
     __syncthreads();
-    cluster_sync();  // every CTA's barriers are initialised before any remote arrive
     tc_fence_after();
 #ifdef FAVOR_SCAN_TRACE
     if (threadIdx.x == 0 && blockIdx.x < 2048) {
@@ -297,30 +323,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             // K, Q and V of the tiles kPrefetch ahead go to L2 first: the loads below have only
             // about one tile of lead (single K and Q buffers), less than a device-memory round
             // trip under load
-            auto prefetch = [&](int t) {
-                tma_prefetch_3d(&mK, 0, t * kTile, bh);
-                tma_prefetch_3d(&mQ, 0, t * kTile, bh);
-                tma_prefetch_3d(&mV, 0, t * kTile, bh);
+            int ph = grp, pt = 0;  // the next tile to prefetch
+            auto prefetch_next = [&]() {
+                tma_prefetch_3d(&mK, 0, pt * kTile, ph);
+                tma_prefetch_3d(&mQ, 0, pt * kTile, ph);
+                tma_prefetch_3d(&mV, 0, pt * kTile, ph);
+                seq_next(ph, pt);
             };
-            for (int t = 1; t < kPrefetch && t < T; ++t) prefetch(t);
-            for (int t = 0; t < T; ++t) {
-                const int b = t & 1, u = t >> 1;
-                if (t + kPrefetch < T) prefetch(t + kPrefetch);
-                // K(t) once the K team has taken the norms of K(t-1) and P_K(t-1) has read it
-                if (t > 0 && !mbar_wait_lean(&bar_kfree, (t - 1) & 1, &abort_flag)) break;
+            seq_next(ph, pt);  // tile 0 is loaded at once
+            for (int gt = 1; gt < kPrefetch && gt < GT; ++gt) prefetch_next();
+            for (int gt = 0, hb = grp, tl = 0; gt < GT; ++gt, seq_next(hb, tl)) {
+                const int b = gt & 1, u = gt >> 1;
+                const int row = tl * kTile;
+                if (gt + kPrefetch < GT) prefetch_next();  // tile gt + kPrefetch
+                // K(gt) once the K team has taken the norms of K(gt-1) and P_K(gt-1) has read it
+                if (gt > 0 && !mbar_wait_lean(&bar_kfree, (gt - 1) & 1, &abort_flag)) break;
                 mbar_arrive_expect_tx(&bar_kfull, kTileBytes);
-                tma_load_3d(sK, &mK, &bar_kfull, 0, t * kTile, bh);
-                kl = t + 1;
-                // Q(t) once P_Q(t-1) has read Q(t-1)
-                if (t > 0 && !mbar_wait_lean(&bar_qfree, (t - 1) & 1, &abort_flag)) break;
+                tma_load_3d(sK, &mK, &bar_kfull, 0, row, hb);
+                kl = gt + 1;
+                // Q(gt) once P_Q(gt-1) has read Q(gt-1)
+                if (gt > 0 && !mbar_wait_lean(&bar_qfree, (gt - 1) & 1, &abort_flag)) break;
                 mbar_arrive_expect_tx(&bar_qfull, kTileBytes);
-                tma_load_3d(sQ, &mQ, &bar_qfull, 0, t * kTile, bh);
-                ql = t + 1;
-                // V(t) once the intra MMA of tile t-2 (the last reader of buffer b) is done
-                if (t > 1 && !mbar_wait_lean(&bar_vfree[b], (u & 1) ^ 1, &abort_flag)) break;
+                tma_load_3d(sQ, &mQ, &bar_qfull, 0, row, hb);
+                ql = gt + 1;
+                // V(gt) once the intra MMA of tile gt-2 (the last reader of buffer b) is done
+                if (gt > 1 && !mbar_wait_lean(&bar_vfree[b], (u & 1) ^ 1, &abort_flag)) break;
                 mbar_arrive_expect_tx(&bar_vfull[b], kTileBytes);
-                tma_load_3d(sV + b * kTileBytes, &mV, &bar_vfull[b], 0, t * kTile, bh);
-                vl = t + 1;
+                tma_load_3d(sV + b * kTileBytes, &mV, &bar_vfull[b], 0, row, hb);
+                vl = gt + 1;
             }
             // Drain the loads in flight before the CTA may exit.
             volatile int never = 0;
@@ -386,9 +416,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             return true;
         };
-        if (ok && T > 0) ok = issue_pk(0) && issue_pq(0) && (T < 2 || issue_pk(1));
-        for (int t = 0; t < T && ok; ++t) {
+        // t: this CTA's tile sequence over its heads (phases and buffers); the state restarts at
+        // each head's first tile
+        if (ok && GT > 0) ok = issue_pk(0) && issue_pq(0) && (GT < 2 || issue_pk(1));
+        for (int t = 0, hd = grp, tl = 0; t < GT && ok; ++t, seq_next(hd, tl)) {
             const int b = t & 1, u = t >> 1;
+            const bool head_start = tl == 0;
             const uint32_t R = tbase + kColR0 + 128u * (uint32_t)b;
             const uint32_t pq = tbase + kColPQ;
             const uint32_t num = tbase + kColNum;
@@ -405,13 +438,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&bar_sc);
             }
             __syncwarp();
-            // inter: NUM = phi(Q_t) [S_<t | z_<t] (K = 128 features), plus phi(Q_t) S_lo
+            // inter: NUM = phi(Q_t) [S_<t | z_<t] (K = 128 features), plus phi(Q_t) S_lo; none at a
+            // head's first tile (S_<0 = 0), whose intra MMA starts NUM. Waited for all the same: NUM
+            // must have been drained.
             SCAN_TRACE(t, 21);
             ok = TIMED_WAIT(5, mbar_wait_lean(&bar_inter, t & 1, &abort_flag));
             if (!ok) break;
             SCAN_TRACE(t, 1);
             tc_fence_after();
-            if (leader) {
+            if (leader && !head_start) {
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) mma_ts(num, pq + 8u * ks, sdesc_add(d_snap, 2048u * ks), id_o, ks > 0);
                 if (hilo) {
@@ -422,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             // the next tile's query projection (phi(Q_t) has been read by now, in MMA order), so
             // that phi(Q_{t+1}) is formed while this tile's state and intra MMAs run
-            if (t + 1 < T && !(ok = issue_pq(t + 1))) break;
+            if (t + 1 < GT && !(ok = issue_pq(t + 1))) break;
             SCAN_TRACE(t, 2);
             // state: [S | z] += phi(K_t)^T [V_t | 1] (K = 128 tokens; phi(K) read MN-major, its
             // second 64-feature region LBO bytes on; the ones are the second N region of B)
@@ -432,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
                     mma_ss(tbase + kColS, sdesc_add(d_pk_st[b], 2048u * ks), sdesc_add(d_v[b], 2048u * ks), id_st,
-                           (t > 0 || ks > 0) ? 1u : 0u);
+                           (!head_start || ks > 0) ? 1u : 0u);
                 mma_commit(&bar_st);
                 mma_commit(&bar_phkfree[b]);
             }
@@ -445,12 +480,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             if (leader) {
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) mma_ts(num, R + 8u * ks, sdesc_add(d_v[b], 2048u * ks), id_o, 1u);
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_ts(num, R + 8u * ks, sdesc_add(d_v[b], 2048u * ks), id_o, (!head_start || ks > 0) ? 1u : 0u);
                 mma_commit(&bar_num);
                 mma_commit(&bar_vfree[b]);
             }
             __syncwarp();
-            if (t + 2 < T && !(ok = issue_pk(t + 2))) break;
+            if (t + 2 < GT && !(ok = issue_pk(t + 2))) break;
             SCAN_TRACE(t, 5);
         }
 #ifdef FAVOR_SCAN_TRACE
@@ -471,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         const int fv = min(64, max(0, p.m - feat0 - 64 * h));  // real features among this warp's 64
         bool failed = false;
-        for (int t = 0; t < T; ++t) {
+        for (int t = 0; t < GT; ++t) {  // the CTA's tile sequence
             const int b = t & 1, u = t >> 1;
             failed |= !mbar_wait_lean(&bar_pq[b], u & 1, &abort_flag);
             if (warp == kQWarp0 && lane == 0) SCAN_TRACE(t, 6);
@@ -525,9 +561,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float s2 = p.scale * p.scale;
         float beta = -INFINITY;  // running key stabiliser, binary orders of magnitude
         bool failed = false;
-        for (int t = 0; t < T; ++t) {
+        for (int t = 0, hd = grp, tl = 0; t < GT; ++t, seq_next(hd, tl)) {  // the CTA's tile sequence
             const int b = t & 1, u = t >> 1;
-            const bool valid = t * kTile + r < p.n;
+            const bool valid = tl * kTile + r < p.n;
+            if (tl == 0) beta = -INFINITY;  // a new head
             float kn = 0.f;  // |k^_r|^2 / 2 in binary orders of magnitude
             if (exp_kind) {
                 failed |= !mbar_wait_lean(&bar_kfull, t & 1, &abort_flag);
@@ -612,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the state image before tile 0 (zero) is in place
         __syncwarp();
         if (lane == 0 && !withhold) mbar_arrive(&bar_inter);
-        for (int t = 0; t < T; ++t) {
+        for (int t = 0; t < GT; ++t) {  // the CTA's tile sequence
             failed |= !mbar_wait_lean(&bar_sc, t & 1, &abort_flag);
             if (warp == kAWarp0 && lane == 0) SCAN_TRACE(t, 11);
             __syncwarp();
@@ -646,8 +683,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_atil);
             if (warp == kAWarp0 && lane == 0) SCAN_TRACE(t, 12);
-            // ---- the state image S_<t+1 once state(t) is done (rescaled if the key stabiliser rose)
-            if (t + 1 < T) {
+            // ---- the state image S_<t+1 once state(t) is done (rescaled if the key stabiliser rose;
+            // unused if tile t + 1 starts a head, whose inter MMA is skipped)
+            if (t + 1 < GT) {
                 const int t1 = t + 1;
                 failed |= !mbar_wait_lean(&bar_st, t & 1, &abort_flag);
                 failed |= !mbar_wait_lean(&bar_beta[t1 & 3], (t1 >> 2) & 1, &abort_flag);
@@ -705,27 +743,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = q * 32 + lane;  // query row of NUM
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         bool failed = false;
-        // This CTA's part of the head's ring: [slot][rank][chunk][row] x 16 bytes.
-        uint8_t* ring = CS > 1 ? p.ring + (size_t)bh * kRing * CS * kXChunks * kTile * 16 : nullptr;
+        // The group's ring: [slot][rank][chunk][row] x 16 bytes.
+        uint8_t* ring = ring_grp;
         // NUM is free for the first tile's inter MMA
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_inter);
-        for (int tt = 0; tt < T; ++tt) {
+        for (int tt = 0, bh = grp, tl = 0; tt < GT; ++tt, seq_next(bh, tl)) {  // the CTA's tile sequence
             const int slot = tt % kRing, use = tt / kRing;
-            const int i_tok = tt * kTile + r;
+            const int i_tok = tl * kTile + r;
             // where this row's results go: the output row (alone), or its partial record in the ring
             uint8_t* rec = CS > 1 ? ring + ((size_t)(slot * CS + rank) * kXChunks) * kTile * 16 + r * 16 : nullptr;
             uint4* yrow = reinterpret_cast<uint4*>(p.Y + ((size_t)bh * p.n + i_tok) * kD);
             const bool store = CS > 1 || i_tok < p.n;
-            // the slot's previous tile has been read by every CTA of the cluster
-            if (CS > 1 && use > 0) failed |= !mbar_wait_cluster_lean(&bar_rfree[slot], (use - 1) & 1, &abort_flag);
+            // the slot's previous tile has been read by every CTA of the group
+            if (CS > 1 && use > 0) failed |= !mbar_wait_lean(&bar_rfree[slot], (use - 1) & 1, &abort_flag);
             if (warp == kOWarp0 && lane == 0) SCAN_TRACE(tt, 23);
             failed |= !mbar_wait_lean(&bar_num, tt & 1, &abort_flag);
             if (warp == kOWarp0 && lane == 0) SCAN_TRACE(tt, 15);
             __syncwarp();
             tc_fence_after();
             // NUM in two halves (the second with the denominator first); y = num / den of this CTA's
-            // features. Alone, the bf16 output row; in a cluster, fp16 times a power-of-two scale per
+            // features. Alone, the bf16 output row; in a group, fp16 times a power-of-two scale per
             // half row (so that any bf16 value range survives), the partial row for its owner.
             const uint32_t na = tbase + lane_off + kColNum;
             float den_own = 0.f, inv_own = 0.f, big = 1.f, e_own = 0.f, sc0 = 1.f, sc1 = 1.f;
@@ -757,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) mbar_arrive(&bar_inter);  // NUM may take the next tile's inter MMA
                     if (warp == kOWarp0 && lane == 0) SCAN_TRACE(tt, 16);
                 }
-                // half row h: alone, the bf16 output; in a cluster, fp16 times a power-of-two scale 2^ex
+                // half row h: alone, the bf16 output; in a group, fp16 times a power-of-two scale 2^ex
                 // with max |y| 2^-ex in [2^14, 2^15) (from the IEEE exponent field, clamped so that
                 // all factors stay finite), so that fp16 keeps 11 bits of any bf16 value range
                 float pw = 1.f;
@@ -803,7 +841,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __stcg(reinterpret_cast<uint4*>(rec + 8 * kTile * 16),
                        make_uint4(__float_as_uint(l_own), __float_as_uint(sc0), __float_as_uint(sc1), 0u));
                 // the warp's partial rows of this tile are stored (released at CTA scope; the
-                // full-signal warp releases them to the cluster)
+                // full-signal warp releases them to the group)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar_ostore[slot]);
             }
@@ -811,24 +849,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         (void)failed;
     } else if (warp < kSWarp0) {
-        // ---------------- X team: 4 warps (cluster only) ----------------
+        // ---------------- X team: 4 warps (groups of CS > 1 only) ----------------
         // The rows [rank RP, rank RP + rows) of each tile from the CS partial rows in the ring: a
         // row's result is sum_g w_g y_g / sum_g w_g with w_g = 2^(l_g - max l), l_g = log2(den_g) + e_g
         // (y_g = num_g / den_g as stored, times its power-of-two scale). TPR threads per row, each
         // taking 8 / TPR consecutive 16-byte chunks of it.
         if (CS > 1) {
             const int xt = threadIdx.x - 32 * kXWarp0;
-            const uint8_t* ring = p.ring + (size_t)bh * kRing * CS * kXChunks * kTile * 16;
+            const uint8_t* ring = ring_grp;
             const int row0 = rank * RP, rows = min(RP, kTile - row0);
             bool failed = false;
             // One tile: passes of 32 rows, four threads per row with two 16-byte chunks each.
-            auto combine = [&](int tc) {
+            auto combine = [&](int tc, int bh, int t) {  // tile t of head bh, the sequence's tile tc
                 constexpr int NC = kMaxCluster;  // partials past CS carry no weight
                 const int slot = tc % kRing;
 #pragma unroll 1
                 for (int item = xt; item < rows * 4; item += 32 * kXWarps) {
                     const int row = row0 + item / 4, c0 = (item % 4) * 2;
-                    const int tok = tc * kTile + row;
+                    const int tok = t * kTile + row;
                     if (tok >= p.n) continue;
                     uint4 meta[NC], yv[NC][2];
 #pragma unroll
@@ -882,29 +920,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar_xread[slot]);
             };
-            for (int tc = 0; tc < T; ++tc) {
-                failed |= !mbar_wait_cluster_lean(&bar_rfull[tc % kRing], (tc / kRing) & 1, &abort_flag);
+            for (int tc = 0, hd = grp, tl = 0; tc < GT; ++tc, seq_next(hd, tl)) {  // the CTA's tile sequence
+                // every CTA of the group has stored its partial rows of tile tc
+                failed |= !mbar_wait_lean(&bar_rfull[tc % kRing], (tc / kRing) & 1, &abort_flag);
                 if (warp == kXWarp0 && lane == 0) SCAN_TRACE(tc, 17);
-                combine(tc);
+                combine(tc, hd, tl);
                 if (warp == kXWarp0 && lane == 0) SCAN_TRACE(tc, 25);
             }
             (void)failed;
         }
     } else {
-        // ---------------- signal warps (cluster only) ----------------
-        // Warp kSWarp0 releases each tile's partial rows of this CTA to every CTA of the cluster
-        // once the O team has stored them; warp kSWarp0 + 1 tells every CTA that this CTA's X
-        // team has read their rows of a slot. Each holds the one cluster-scope fence of its tile
-        // (the teams themselves only arrive on local barriers), and the remote arrives are relaxed.
+        // ---------------- signal warps (groups of CS > 1 only) ----------------
+        // The group's counters, kept off the teams' paths (a load from L2 per tile would sit in the
+        // O team's loop). Warp kSWarp0, per tile: once the O team has stored this CTA's partial
+        // rows, counts them into the slot's full counter; once the counter shows every CTA's rows,
+        // lets the X team combine them. Warp kSWarp0 + 1, per tile: once the X team has read the
+        // slot, counts that into its free counter; once every CTA has read it, lets the O team
+        // store the tile kRing later into it. Each holds the one GPU-scope fence of its tile (the
+        // teams only arrive on local barriers), and the adds are relaxed.
         if (CS > 1 && lane == 0) {
             const bool full_side = warp == kSWarp0;
             uint64_t* local = full_side ? bar_ostore : bar_xread;
-            uint64_t* remote = full_side ? bar_rfull : bar_rfree;
+            uint64_t* ready = full_side ? bar_rfull : bar_rfree;
+            uint32_t* counter = flags + (full_side ? 0 : kRing);
             bool failed = false;
-            for (int t = 0; t < T && !failed; ++t) {
-                failed |= !mbar_wait_lean(&local[t % kRing], (t / kRing) & 1, &abort_flag);
-                fence_acq_rel_cluster();
-                for (int o = 0; o < CS; ++o) mbar_arrive_relaxed_cluster(mapa(smem_u32(&remote[t % kRing]), o));
+            for (int t = 0; t < GT && !failed; ++t) {
+                const int slot = t % kRing, use = t / kRing;
+                failed |= !mbar_wait_lean(&local[slot], use & 1, &abort_flag);
+                fence_acq_rel_gpu();
+                counter_add_relaxed(&counter[slot], 1u);
+                if (!full_side && t + kRing >= GT) continue;  // no later tile takes the slot
+                failed |= !counter_wait(&counter[slot], (uint32_t)(CS * (use + 1)), &abort_flag);
+                mbar_arrive(&ready[slot]);
             }
         }
     }
@@ -920,7 +967,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tbase, 512);
     }
-    cluster_sync();  // the cluster's CTAs leave together
 }
 
 }  // namespace tcs

@@ -73,11 +73,13 @@ def test_workspace_sizes_per_path():
     # longer sequences run the three-kernel path, whose workspace does not grow with n beyond the splits
     assert favor.workspace_bytes("noncausal", 1, 8, 4096, 64, 256, bf) > 0
     # the tensor-core causal scans keep the state in TMEM; with more than 128 features the CTAs of a
-    # head combine their partial rows through a ring of 4 tiles x CS CTAs x 9 x 128 rows x 16 bytes
+    # group combine their partial rows through a ring of 4 tiles x CS CTAs x 9 x 128 rows x 16 bytes,
+    # after 16 u32 counters per group (256-byte piece), for min(B*H, 160 // CS) groups
     for m in (64, 128):
         assert favor.workspace_bytes("causal", 4, 16, 8192, 64, m, bf) == 0
-    for m, cs in ((192, 2), (256, 2), (384, 3), (512, 4)):
-        assert favor.workspace_bytes("causal", 4, 16, 8192, 64, m, bf) == 64 * 4 * cs * 9 * 128 * 16
+    for BH, m, cs in ((64, 192, 2), (64, 256, 2), (64, 384, 3), (64, 512, 4), (256, 512, 4), (7, 384, 3)):
+        groups = min(BH, 160 // cs)
+        assert favor.workspace_bytes("causal", 1, BH, 8192, 64, m, bf) == up(groups * 64) + groups * 4 * cs * 9 * 128 * 16
     # streaming decode state: fp32 S [BH][m][d], z [BH][m], stabilisers [BH][m/64], block partials
     # [BH][m/64][d+2], u32 counter [BH]; 256-byte pieces
     up = lambda b: (b + 255) // 256 * 256
