@@ -436,7 +436,8 @@ favor_status_t tc_causal(const void* Q, const void* K, const void* V, const void
     tcs::ScanParams sp{n, m, kind, eps * std::sqrt((float)m), feat_scale(64, kind), static_cast<__nv_bfloat16*>(Y),
                        BH, cs, ring, flags};
     const size_t smem = tcs::ScanSmem::bytes();
-    auto kern = kind == kKindExp ? tcs::causal_scan<kKindExp> : kind == kKindRelu ? tcs::causal_scan<kKindRelu> : tcs::causal_scan<kKindElu>;
+    auto kern = cs > 1 ? (kind == kKindExp ? tcs::causal_scan<kKindExp, true> : kind == kKindRelu ? tcs::causal_scan<kKindRelu, true> : tcs::causal_scan<kKindElu, true>)
+                       : (kind == kKindExp ? tcs::causal_scan<kKindExp, false> : kind == kKindRelu ? tcs::causal_scan<kKindRelu, false> : tcs::causal_scan<kKindElu, false>);
     FAVOR_TRY(set_smem(kern, smem));
     if (cs > 1 && cudaMemsetAsync(flags, 0, (size_t)G * tcs::kFlagWords * 4, s) != cudaSuccess) return FAVOR_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};

@@ -172,15 +172,51 @@ __device__ __forceinline__ uint32_t lo_pair(uint32_t x0, uint32_t x1, uint32_t h
     return pack_bf16(__uint_as_float(x0) - __uint_as_float(hw << 16), __uint_as_float(x1) - __uint_as_float(hw & 0xFFFF0000u));
 }
 
+// The CTA's abort word: set by the role whose wait gave up; every later wait of the CTA then gives
+// up at once.
+__shared__ int s_abort;
+// The scan's waits: the phase test inline, the bounded polling out of line with the fewest
+// arguments (the kernel's instruction footprint sets its speed: every wait site counts).
+__device__ __noinline__ bool scan_wait_slow(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer();
+    const uint64_t tlim = g_favor_test_wait_ns;
+    const uint64_t limit = tlim ? tlim : kWaitLimitNs;
+    volatile int* abort_flag = &s_abort;
+    if (*abort_flag) return false;
+    for (uint32_t it = 1;; ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if ((it & 255u) != 0) continue;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > limit) {
+            atomicOr(&g_favor_error, kDevErrTimeout);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+__device__ __forceinline__ bool scan_wait(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return scan_wait_slow(smem_u32(bar), parity);
+}
+
 // KIND: the feature family (kKindExp, kKindRelu, kKindElu), fixed per instance so that each
-// instance carries only its own feature map and stabiliser code.
-template <int KIND>
+// instance carries only its own feature map and stabiliser code. GROUPED: CS > 1 (the ring, the
+// X team and the signal warps); without it, CS = 1 and the O team writes the output rows.
+template <int KIND, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1)
     causal_scan(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                 const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mOm, ScanParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];  // aligned to 1024 by hand below
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int CS = p.cs;
+    const int CS = GROUPED ? p.cs : 1;
     const int G = (int)gridDim.x / CS;  // groups
     const int grp = (int)blockIdx.x / CS, rank = (int)blockIdx.x % CS;
     const int RP = (kTile + CS - 1) / CS;  // rows finalised by each CTA of the group
@@ -201,7 +237,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ uint64_t bar_sc, bar_atil, bar_st, bar_inter, bar_num, bar_beta[4], bar_cq[2];
     __shared__ uint64_t bar_drain, bar_rfull[kRing], bar_rfree[kRing], bar_ostore[kRing], bar_xread[kRing];
     __shared__ uint32_t tmem_base;
-    __shared__ int abort_flag;
     __shared__ float sBeta[4], sF[4], sKmx[4];
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -219,8 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     };
     // the group's ring and counters (full: [0, kRing), free: [kRing, 2 kRing))
-    uint8_t* const ring_grp = CS > 1 ? p.ring + (size_t)grp * ScanWs::ring_bytes(CS) : nullptr;
-    uint32_t* const flags = CS > 1 ? p.flags + (size_t)grp * kFlagWords : nullptr;
+    uint8_t* const ring_grp = GROUPED ? p.ring + (size_t)grp * ScanWs::ring_bytes(CS) : nullptr;
+    uint32_t* const flags = GROUPED ? p.flags + (size_t)grp * kFlagWords : nullptr;
     constexpr bool exp_kind = KIND == kKindExp;
     constexpr bool hilo = exp_kind;     // state image with its rounding remainder
     const float A2 = p.scale * kLog2e;  // projections -> exponents in binary orders of magnitude
@@ -250,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     if (threadIdx.x == 0) {
-        abort_flag = 0;
+        s_abort = 0;
         mbar_init(&bar_om, 1);
         mbar_init(&bar_kfull, 1);
         mbar_init(&bar_kfree, kKWarps);
@@ -323,31 +358,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             // K, Q and V of the tiles kPrefetch ahead go to L2 first: the loads below have only
             // about one tile of lead (single K and Q buffers), less than a device-memory round
             // trip under load
-            int ph = grp, pt = 0;  // the next tile to prefetch
-            auto prefetch_next = [&]() {
-                tma_prefetch_3d(&mK, 0, pt * kTile, ph);
-                tma_prefetch_3d(&mQ, 0, pt * kTile, ph);
-                tma_prefetch_3d(&mV, 0, pt * kTile, ph);
-                seq_next(ph, pt);
-            };
-            seq_next(ph, pt);  // tile 0 is loaded at once
-            for (int gt = 1; gt < kPrefetch && gt < GT; ++gt) prefetch_next();
+            int pf = 1, ph = grp, pt = 0;  // the next tile to prefetch (tile 0 is loaded at once)
+            seq_next(ph, pt);
             for (int gt = 0, hb = grp, tl = 0; gt < GT; ++gt, seq_next(hb, tl)) {
                 const int b = gt & 1, u = gt >> 1;
                 const int row = tl * kTile;
-                if (gt + kPrefetch < GT) prefetch_next();  // tile gt + kPrefetch
+                for (; pf <= gt + kPrefetch && pf < GT; ++pf, seq_next(ph, pt)) {  // up to tile gt + kPrefetch
+                    tma_prefetch_3d(&mK, 0, pt * kTile, ph);
+                    tma_prefetch_3d(&mQ, 0, pt * kTile, ph);
+                    tma_prefetch_3d(&mV, 0, pt * kTile, ph);
+                }
                 // K(gt) once the K team has taken the norms of K(gt-1) and P_K(gt-1) has read it
-                if (gt > 0 && !mbar_wait_lean(&bar_kfree, (gt - 1) & 1, &abort_flag)) break;
+                if (gt > 0 && !scan_wait(&bar_kfree, (gt - 1) & 1)) break;
                 mbar_arrive_expect_tx(&bar_kfull, kTileBytes);
                 tma_load_3d(sK, &mK, &bar_kfull, 0, row, hb);
                 kl = gt + 1;
                 // Q(gt) once P_Q(gt-1) has read Q(gt-1)
-                if (gt > 0 && !mbar_wait_lean(&bar_qfree, (gt - 1) & 1, &abort_flag)) break;
+                if (gt > 0 && !scan_wait(&bar_qfree, (gt - 1) & 1)) break;
                 mbar_arrive_expect_tx(&bar_qfull, kTileBytes);
                 tma_load_3d(sQ, &mQ, &bar_qfull, 0, row, hb);
                 ql = gt + 1;
                 // V(gt) once the intra MMA of tile gt-2 (the last reader of buffer b) is done
-                if (gt > 1 && !mbar_wait_lean(&bar_vfree[b], (u & 1) ^ 1, &abort_flag)) break;
+                if (gt > 1 && !scan_wait(&bar_vfree[b], (u & 1) ^ 1)) break;
                 mbar_arrive_expect_tx(&bar_vfull[b], kTileBytes);
                 tma_load_3d(sV + b * kTileBytes, &mV, &bar_vfull[b], 0, row, hb);
                 vl = gt + 1;
@@ -383,11 +415,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #ifdef FAVOR_SCAN_TRACE
         unsigned long long wacc[10] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
 #endif
-        bool ok = mbar_wait_lean(&bar_om, 0, &abort_flag);
+        bool ok = scan_wait(&bar_om, 0);
         tc_fence_after();
         // P_K(t) into region t & 1 (once K(t) is loaded)
         auto issue_pk = [&](int t) -> bool {
-            if (!TIMED_WAIT(0, mbar_wait_lean(&bar_kfull, t & 1, &abort_flag))) return false;
+            if (!TIMED_WAIT(0, scan_wait(&bar_kfull, t & 1))) return false;
             tc_fence_after();
             if (leader) {
                 const uint32_t dcol = tbase + kColR0 + 128u * (uint32_t)(t & 1);
@@ -402,8 +434,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P_Q(t) into region t & 1, once Q(t) is loaded and the K team has read P_K(t)
         auto issue_pq = [&](int t) -> bool {
             const int b = t & 1;
-            if (!TIMED_WAIT(1, mbar_wait_lean(&bar_qfull, t & 1, &abort_flag))) return false;
-            if (!TIMED_WAIT(2, mbar_wait_lean(&bar_pkfree[b], (t >> 1) & 1, &abort_flag))) return false;
+            if (!TIMED_WAIT(1, scan_wait(&bar_qfull, t & 1))) return false;
+            if (!TIMED_WAIT(2, scan_wait(&bar_pkfree[b], (t >> 1) & 1))) return false;
             tc_fence_after();
             if (leader) {
                 const uint32_t dcol = tbase + kColR0 + 128u * (uint32_t)b;
@@ -417,77 +449,82 @@ __global__ void __launch_bounds__(kThreads, 1)
             return true;
         };
         // t: this CTA's tile sequence over its heads (phases and buffers); the state restarts at
-        // each head's first tile
-        if (ok && GT > 0) ok = issue_pk(0) && issue_pq(0) && (GT < 2 || issue_pk(1));
-        for (int t = 0, hd = grp, tl = 0; t < GT && ok; ++t, seq_next(hd, tl)) {
+        // each head's first tile. Iterations -2 and -1 issue only the first projections (P_K(0);
+        // P_Q(0), P_K(1)), so that each stage has one copy of its code.
+        for (int t = -2, tl = 0; t < GT && ok; ++t) {
             const int b = t & 1, u = t >> 1;
             const bool head_start = tl == 0;
             const uint32_t R = tbase + kColR0 + 128u * (uint32_t)b;
             const uint32_t pq = tbase + kColPQ;
             const uint32_t num = tbase + kColNum;
-            // scores: SC = phi(Q_t) phi(K_t)^T (K = 128 features, two K atoms of phi(K))
-            SCAN_TRACE(t, 20);
-            ok = TIMED_WAIT(3, mbar_wait_lean(&bar_scr[b], u & 1, &abort_flag));
-            if (!ok) break;
-            SCAN_TRACE(t, 0);
-            tc_fence_after();
-            if (leader) {
+            if (t >= 0) {
+                // scores: SC = phi(Q_t) phi(K_t)^T (K = 128 features, two K atoms of phi(K))
+                SCAN_TRACE(t, 20);
+                ok = TIMED_WAIT(3, scan_wait(&bar_scr[b], u & 1));
+                if (!ok) break;
+                SCAN_TRACE(t, 0);
+                tc_fence_after();
+                if (leader) {
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_ts(R, pq + 8u * ks, sdesc_add(d_pk_sc[b], (ks >> 2) * 16384u + (ks & 3) * 32u), id_sc, ks > 0);
-                mma_commit(&bar_sc);
-            }
-            __syncwarp();
-            // inter: NUM = phi(Q_t) [S_<t | z_<t] (K = 128 features), plus phi(Q_t) S_lo; none at a
-            // head's first tile (S_<0 = 0), whose intra MMA starts NUM. Waited for all the same: NUM
-            // must have been drained.
-            SCAN_TRACE(t, 21);
-            ok = TIMED_WAIT(5, mbar_wait_lean(&bar_inter, t & 1, &abort_flag));
-            if (!ok) break;
-            SCAN_TRACE(t, 1);
-            tc_fence_after();
-            if (leader && !head_start) {
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) mma_ts(num, pq + 8u * ks, sdesc_add(d_snap, 2048u * ks), id_o, ks > 0);
-                if (hilo) {
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) mma_ts(num, pq + 8u * ks, sdesc_add(d_slo, 2048u * ks), id_lo, 1u);
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_ts(R, pq + 8u * ks, sdesc_add(d_pk_sc[b], (ks >> 2) * 16384u + (ks & 3) * 32u), id_sc, ks > 0);
+                    mma_commit(&bar_sc);
                 }
+                __syncwarp();
+                // inter: NUM = phi(Q_t) [S_<t | z_<t] (K = 128 features), plus phi(Q_t) S_lo; none at
+                // a head's first tile (S_<0 = 0), whose intra MMA starts NUM. Waited for all the
+                // same: NUM must have been drained.
+                SCAN_TRACE(t, 21);
+                ok = TIMED_WAIT(5, scan_wait(&bar_inter, t & 1));
+                if (!ok) break;
+                SCAN_TRACE(t, 1);
+                tc_fence_after();
+                if (leader && !head_start) {
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) mma_ts(num, pq + 8u * ks, sdesc_add(d_snap, 2048u * ks), id_o, ks > 0);
+                    if (hilo) {
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks) mma_ts(num, pq + 8u * ks, sdesc_add(d_slo, 2048u * ks), id_lo, 1u);
+                    }
+                }
+                __syncwarp();
             }
-            __syncwarp();
             // the next tile's query projection (phi(Q_t) has been read by now, in MMA order), so
             // that phi(Q_{t+1}) is formed while this tile's state and intra MMAs run
-            if (t + 1 < GT && !(ok = issue_pq(t + 1))) break;
-            SCAN_TRACE(t, 2);
-            // state: [S | z] += phi(K_t)^T [V_t | 1] (K = 128 tokens; phi(K) read MN-major, its
-            // second 64-feature region LBO bytes on; the ones are the second N region of B)
-            if (!(ok = TIMED_WAIT(7, mbar_wait_lean(&bar_vfull[b], u & 1, &abort_flag)))) break;
-            tc_fence_after();
-            if (leader) {
+            if (t >= -1 && t + 1 < GT && !(ok = issue_pq(t + 1))) break;
+            if (t >= 0) {
+                SCAN_TRACE(t, 2);
+                // state: [S | z] += phi(K_t)^T [V_t | 1] (K = 128 tokens; phi(K) read MN-major, its
+                // second 64-feature region LBO bytes on; the ones are the second N region of B)
+                if (!(ok = TIMED_WAIT(7, scan_wait(&bar_vfull[b], u & 1)))) break;
+                tc_fence_after();
+                if (leader) {
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_ss(tbase + kColS, sdesc_add(d_pk_st[b], 2048u * ks), sdesc_add(d_v[b], 2048u * ks), id_st,
-                           (!head_start || ks > 0) ? 1u : 0u);
-                mma_commit(&bar_st);
-                mma_commit(&bar_phkfree[b]);
-            }
-            __syncwarp();
-            SCAN_TRACE(t, 3);
-            // intra: NUM += A~ [V_t | 1] (K = 128 keys, A~ packed in place of the scores)
-            SCAN_TRACE(t, 22);
-            if (!(ok = TIMED_WAIT(8, mbar_wait_lean(&bar_atil, t & 1, &abort_flag)))) break;
-            SCAN_TRACE(t, 4);
-            tc_fence_after();
-            if (leader) {
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_ss(tbase + kColS, sdesc_add(d_pk_st[b], 2048u * ks), sdesc_add(d_v[b], 2048u * ks), id_st,
+                               (!head_start || ks > 0) ? 1u : 0u);
+                    mma_commit(&bar_st);
+                    mma_commit(&bar_phkfree[b]);
+                }
+                __syncwarp();
+                SCAN_TRACE(t, 3);
+                // intra: NUM += A~ [V_t | 1] (K = 128 keys, A~ packed in place of the scores)
+                SCAN_TRACE(t, 22);
+                if (!(ok = TIMED_WAIT(8, scan_wait(&bar_atil, t & 1)))) break;
+                SCAN_TRACE(t, 4);
+                tc_fence_after();
+                if (leader) {
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_ts(num, R + 8u * ks, sdesc_add(d_v[b], 2048u * ks), id_o, (!head_start || ks > 0) ? 1u : 0u);
-                mma_commit(&bar_num);
-                mma_commit(&bar_vfree[b]);
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_ts(num, R + 8u * ks, sdesc_add(d_v[b], 2048u * ks), id_o, (!head_start || ks > 0) ? 1u : 0u);
+                    mma_commit(&bar_num);
+                    mma_commit(&bar_vfree[b]);
+                }
+                __syncwarp();
+                if (++tl == T) tl = 0;
             }
-            __syncwarp();
             if (t + 2 < GT && !(ok = issue_pk(t + 2))) break;
-            SCAN_TRACE(t, 5);
+            if (t >= 0) SCAN_TRACE(t, 5);
         }
 #ifdef FAVOR_SCAN_TRACE
         if (lane == 0 && blockIdx.x < 2048)
@@ -509,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool failed = false;
         for (int t = 0; t < GT; ++t) {  // the CTA's tile sequence
             const int b = t & 1, u = t >> 1;
-            failed |= !mbar_wait_lean(&bar_pq[b], u & 1, &abort_flag);
+            failed |= !scan_wait(&bar_pq[b], u & 1);
             if (warp == kQWarp0 && lane == 0) SCAN_TRACE(t, 6);
             __syncwarp();
             tc_fence_after();
@@ -567,11 +604,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (tl == 0) beta = -INFINITY;  // a new head
             float kn = 0.f;  // |k^_r|^2 / 2 in binary orders of magnitude
             if (exp_kind) {
-                failed |= !mbar_wait_lean(&bar_kfull, t & 1, &abort_flag);
+                failed |= !scan_wait(&bar_kfull, t & 1);
                 __syncwarp();
                 kn = 0.5f * s2 * tile_row_sqnorm<64>(sK, r) * kLog2e;
             }
-            failed |= !mbar_wait_lean(&bar_pk[b], u & 1, &abort_flag);
+            failed |= !scan_wait(&bar_pk[b], u & 1);
             if (warp == kKWarp0 && lane == 0) SCAN_TRACE(t, 8);
             __syncwarp();
             tc_fence_after();
@@ -610,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // phi(K_t) into buffer b once the MMAs of tile t-2 have read it
             if (t >= 2) {
-                failed |= !mbar_wait_lean(&bar_phkfree[b], (u & 1) ^ 1, &abort_flag);
+                failed |= !scan_wait(&bar_phkfree[b], (u & 1) ^ 1);
                 __syncwarp();
             }
             uint8_t* dst = sPK + b * kPhiBytes;
@@ -650,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0 && !withhold) mbar_arrive(&bar_inter);
         for (int t = 0; t < GT; ++t) {  // the CTA's tile sequence
-            failed |= !mbar_wait_lean(&bar_sc, t & 1, &abort_flag);
+            failed |= !scan_wait(&bar_sc, t & 1);
             if (warp == kAWarp0 && lane == 0) SCAN_TRACE(t, 11);
             __syncwarp();
             tc_fence_after();
@@ -687,8 +724,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // unused if tile t + 1 starts a head, whose inter MMA is skipped)
             if (t + 1 < GT) {
                 const int t1 = t + 1;
-                failed |= !mbar_wait_lean(&bar_st, t & 1, &abort_flag);
-                failed |= !mbar_wait_lean(&bar_beta[t1 & 3], (t1 >> 2) & 1, &abort_flag);
+                failed |= !scan_wait(&bar_st, t & 1);
+                failed |= !scan_wait(&bar_beta[t1 & 3], (t1 >> 2) & 1);
                 if (warp == kAWarp0 && lane == 0) SCAN_TRACE(t, 13);
                 __syncwarp();
                 tc_fence_after();
@@ -752,13 +789,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int slot = tt % kRing, use = tt / kRing;
             const int i_tok = tl * kTile + r;
             // where this row's results go: the output row (alone), or its partial record in the ring
-            uint8_t* rec = CS > 1 ? ring + ((size_t)(slot * CS + rank) * kXChunks) * kTile * 16 + r * 16 : nullptr;
+            uint8_t* rec = GROUPED ? ring + ((size_t)(slot * CS + rank) * kXChunks) * kTile * 16 + r * 16 : nullptr;
             uint4* yrow = reinterpret_cast<uint4*>(p.Y + ((size_t)bh * p.n + i_tok) * kD);
-            const bool store = CS > 1 || i_tok < p.n;
+            const bool store = GROUPED || i_tok < p.n;
             // the slot's previous tile has been read by every CTA of the group
-            if (CS > 1 && use > 0) failed |= !mbar_wait_lean(&bar_rfree[slot], (use - 1) & 1, &abort_flag);
+            if (GROUPED && use > 0) failed |= !scan_wait(&bar_rfree[slot], (use - 1) & 1);
             if (warp == kOWarp0 && lane == 0) SCAN_TRACE(tt, 23);
-            failed |= !mbar_wait_lean(&bar_num, tt & 1, &abort_flag);
+            failed |= !scan_wait(&bar_num, tt & 1);
             if (warp == kOWarp0 && lane == 0) SCAN_TRACE(tt, 15);
             __syncwarp();
             tc_fence_after();
@@ -784,9 +821,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     // the row's exponent offset: read before NUM is released, which lets the Q and
                     // K teams move on to the tiles that reuse these slots
-                    if (exp_kind && CS > 1) {
-                        failed |= !mbar_wait_lean(&bar_cq[tt & 1], (tt >> 1) & 1, &abort_flag);
-                        failed |= !mbar_wait_lean(&bar_beta[tt & 3], (tt >> 2) & 1, &abort_flag);
+                    if (exp_kind && GROUPED) {
+                        failed |= !scan_wait(&bar_cq[tt & 1], (tt >> 1) & 1);
+                        failed |= !scan_wait(&bar_beta[tt & 3], (tt >> 2) & 1);
                         e_own = sCq[(tt & 1) * 128 + r] + sBeta[tt & 3];
                     }
                     tmem_ld_wait();
@@ -799,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // with max |y| 2^-ex in [2^14, 2^15) (from the IEEE exponent field, clamped so that
                 // all factors stay finite), so that fp16 keeps 11 bits of any bf16 value range
                 float pw = 1.f;
-                if (CS > 1) {
+                if (GROUPED) {
                     float mx = 0.f;
 #pragma unroll
                     for (int k = 0; k < 32; ++k) mx = fmaxf(mx, fabsf(__uint_as_float(v[k])));
@@ -815,7 +852,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < 16; ++k) {
                     const float y0 = __uint_as_float(v[2 * k]) * big * inv_own * pw;
                     const float y1 = __uint_as_float(v[2 * k + 1]) * big * inv_own * pw;
-                    if (CS == 1) {
+                    if (!GROUPED) {
                         w[k] = pack_bf16(y0, y1);
                     } else {
                         __half2 h2 = __floats2half2_rn(y0, y1);
@@ -826,7 +863,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const uint4 o = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-                        if (CS == 1) {
+                        if (!GROUPED) {
                             if (FAVOR_IN_BOUNDS((size_t)bh * p.n + i_tok < y_rows)) yrow[4 * h + c] = o;
                         } else if (FAVOR_IN_BOUNDS((size_t)(rec - ring) + (4 * h + c) * kTile * 16 + 16 <= ring_head)) {
                             __stcg(reinterpret_cast<uint4*>(rec + (4 * h + c) * kTile * 16), o);
@@ -834,7 +871,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (CS > 1) {
+            if (GROUPED) {
                 // the row's log-weight: log2(den) plus its exponent offset (-inf: no weight)
                 const float l_own = den_own > 0.f ? log2_pos(den_own) + e_own : -INFINITY;
                 if (FAVOR_IN_BOUNDS((size_t)(rec - ring) + 8 * kTile * 16 + 16 <= ring_head))
@@ -854,7 +891,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // row's result is sum_g w_g y_g / sum_g w_g with w_g = 2^(l_g - max l), l_g = log2(den_g) + e_g
         // (y_g = num_g / den_g as stored, times its power-of-two scale). TPR threads per row, each
         // taking 8 / TPR consecutive 16-byte chunks of it.
-        if (CS > 1) {
+        if (GROUPED) {
             const int xt = threadIdx.x - 32 * kXWarp0;
             const uint8_t* ring = ring_grp;
             const int row0 = rank * RP, rows = min(RP, kTile - row0);
@@ -922,7 +959,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             for (int tc = 0, hd = grp, tl = 0; tc < GT; ++tc, seq_next(hd, tl)) {  // the CTA's tile sequence
                 // every CTA of the group has stored its partial rows of tile tc
-                failed |= !mbar_wait_lean(&bar_rfull[tc % kRing], (tc / kRing) & 1, &abort_flag);
+                failed |= !scan_wait(&bar_rfull[tc % kRing], (tc / kRing) & 1);
                 if (warp == kXWarp0 && lane == 0) SCAN_TRACE(tc, 17);
                 combine(tc, hd, tl);
                 if (warp == kXWarp0 && lane == 0) SCAN_TRACE(tc, 25);
@@ -938,7 +975,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // slot, counts that into its free counter; once every CTA has read it, lets the O team
         // store the tile kRing later into it. Each holds the one GPU-scope fence of its tile (the
         // teams only arrive on local barriers), and the adds are relaxed.
-        if (CS > 1 && lane == 0) {
+        if (GROUPED && lane == 0) {
             const bool full_side = warp == kSWarp0;
             uint64_t* local = full_side ? bar_ostore : bar_xread;
             uint64_t* ready = full_side ? bar_rfull : bar_rfree;
@@ -946,11 +983,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool failed = false;
             for (int t = 0; t < GT && !failed; ++t) {
                 const int slot = t % kRing, use = t / kRing;
-                failed |= !mbar_wait_lean(&local[slot], use & 1, &abort_flag);
+                failed |= !scan_wait(&local[slot], use & 1);
                 fence_acq_rel_gpu();
                 counter_add_relaxed(&counter[slot], 1u);
                 if (!full_side && t + kRing >= GT) continue;  // no later tile takes the slot
-                failed |= !counter_wait(&counter[slot], (uint32_t)(CS * (use + 1)), &abort_flag);
+                failed |= !counter_wait(&counter[slot], (uint32_t)(CS * (use + 1)), &s_abort);
                 mbar_arrive(&ready[slot]);
             }
         }
