@@ -172,39 +172,19 @@ __device__ __forceinline__ uint32_t lo_pair(uint32_t x0, uint32_t x1, uint32_t h
     return pack_bf16(__uint_as_float(x0) - __uint_as_float(hw << 16), __uint_as_float(x1) - __uint_as_float(hw & 0xFFFF0000u));
 }
 
-// The CTA's abort word: set by the role whose wait gave up; every later wait of the CTA then gives
-// up at once.
+// The CTA's abort word. The scan's waits spin inline on their phase and give up once it is set:
+// the kernel's instruction footprint sets its speed, and a call to a bounded slow path at each
+// wait site costs more code than the wait. The bound comes from the CTA's watchdog lane instead,
+// which sets the word (and the timeout error) once no role has made progress for the wait limit;
+// the waits that run after a role's last beat (the drains, the group counters) keep a bound of
+// their own.
 __shared__ int s_abort;
-// The scan's waits: the phase test inline, the bounded polling out of line with the fewest
-// arguments (the kernel's instruction footprint sets its speed: every wait site counts).
-__device__ __noinline__ bool scan_wait_slow(uint32_t bar, uint32_t parity) {
-    const uint64_t t0 = globaltimer();
-    const uint64_t tlim = g_favor_test_wait_ns;
-    const uint64_t limit = tlim ? tlim : kWaitLimitNs;
-    volatile int* abort_flag = &s_abort;
-    if (*abort_flag) return false;
-    for (uint32_t it = 1;; ++it) {
-        uint32_t ok;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(bar), "r"(parity)
-            : "memory");
-        if (ok) return true;
-        if ((it & 255u) != 0) continue;
-        if (*abort_flag) return false;
-        if (globaltimer() - t0 > limit) {
-            atomicOr(&g_favor_error, kDevErrTimeout);
-            *abort_flag = 1;
-            return false;
-        }
-    }
-}
+__shared__ uint32_t s_beat[3];  // progress: the MMA warp's, the O team's and the X team's tiles
+__shared__ uint32_t s_done;     // warps (but the watchdog's) past the end of their role
 __device__ __forceinline__ bool scan_wait(uint64_t* bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    return scan_wait_slow(smem_u32(bar), parity);
+    while (!mbar_try_wait(bar, parity))
+        if (*reinterpret_cast<volatile int*>(&s_abort)) return false;
+    return true;
 }
 
 // KIND: the feature family (kKindExp, kKindRelu, kKindElu), fixed per instance so that each
@@ -286,6 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         s_abort = 0;
+        s_done = 0;
+        s_beat[0] = s_beat[1] = s_beat[2] = 0;
         mbar_init(&bar_om, 1);
         mbar_init(&bar_kfull, 1);
         mbar_init(&bar_kfree, kKWarps);
@@ -384,12 +366,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(sV + b * kTileBytes, &mV, &bar_vfull[b], 0, row, hb);
                 vl = gt + 1;
             }
-            // Drain the loads in flight before the CTA may exit.
+            // Drain the loads in flight before the CTA may exit (whether or not it gave up): Omega,
+            // the last K and Q, the last two V (one wait site, cold code).
             volatile int never = 0;
-            mbar_wait_lean(&bar_om, 0, &never);
-            if (kl > 0) mbar_wait_lean(&bar_kfull, (kl - 1) & 1, &never);
-            if (ql > 0) mbar_wait_lean(&bar_qfull, (ql - 1) & 1, &never);
-            for (int t = vl - 2 < 0 ? 0 : vl - 2; t < vl; ++t) mbar_wait_lean(&bar_vfull[t & 1], (t >> 1) & 1, &never);
+#pragma unroll 1
+            for (int i = 0; i < 5; ++i) {
+                const int t = i == 1 ? kl - 1 : i == 2 ? ql - 1 : vl - 5 + i;
+                if (i > 0 && t < 0) continue;
+                uint64_t* bar = i == 0 ? &bar_om : i == 1 ? &bar_kfull : i == 2 ? &bar_qfull : &bar_vfull[t & 1];
+                mbar_wait_lean(bar, i == 0 ? 0u : i <= 2 ? (uint32_t)(t & 1) : (uint32_t)((t >> 1) & 1), &never);
+            }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer: the whole warp waits, one elected lane issues ----------------
@@ -522,6 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
                 if (++tl == T) tl = 0;
+                if (lane == 0) *reinterpret_cast<volatile uint32_t*>(&s_beat[0]) = (uint32_t)t + 1u;
             }
             if (t + 2 < GT && !(ok = issue_pk(t + 2))) break;
             if (t >= 0) SCAN_TRACE(t, 5);
@@ -639,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 beta = 0.f;
             }
-            if (r == 0) {
+            if (exp_kind && r == 0) {  // the other families keep no stabiliser
                 sBeta[t & 3] = beta;
                 sF[t & 3] = f;
                 mbar_arrive(&bar_beta[t & 3]);
@@ -725,11 +712,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (t + 1 < GT) {
                 const int t1 = t + 1;
                 failed |= !scan_wait(&bar_st, t & 1);
-                failed |= !scan_wait(&bar_beta[t1 & 3], (t1 >> 2) & 1);
+                if (exp_kind) failed |= !scan_wait(&bar_beta[t1 & 3], (t1 >> 2) & 1);
                 if (warp == kAWarp0 && lane == 0) SCAN_TRACE(t, 13);
                 __syncwarp();
                 tc_fence_after();
-                const float f = sF[t1 & 3];
+                const float f = exp_kind ? sF[t1 & 3] : 1.f;
                 const uint32_t sa = tbase + lane_off + kColS;
                 uint32_t zr;
                 tmem_ld1(sa + 64, zr);
@@ -882,7 +869,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar_ostore[slot]);
             }
-            if (warp == kOWarp0 && lane == 0) SCAN_TRACE(tt, 18);
+            if (warp == kOWarp0 && lane == 0) {
+                *reinterpret_cast<volatile uint32_t*>(&s_beat[1]) = (uint32_t)tt + 1u;
+                SCAN_TRACE(tt, 18);
+            }
         }
         (void)failed;
     } else if (warp < kSWarp0) {
@@ -962,6 +952,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 failed |= !scan_wait(&bar_rfull[tc % kRing], (tc / kRing) & 1);
                 if (warp == kXWarp0 && lane == 0) SCAN_TRACE(tc, 17);
                 combine(tc, hd, tl);
+                if (warp == kXWarp0 && lane == 0) *reinterpret_cast<volatile uint32_t*>(&s_beat[2]) = (uint32_t)tc + 1u;
                 if (warp == kXWarp0 && lane == 0) SCAN_TRACE(tc, 25);
             }
             (void)failed;
@@ -990,8 +981,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 failed |= !counter_wait(&counter[slot], (uint32_t)(CS * (use + 1)), &s_abort);
                 mbar_arrive(&ready[slot]);
             }
+        } else if (warp == kSWarp0 + 1 && lane == 31) {
+            // ---- the watchdog: until every other warp has left its role, watch the progress beats;
+            // if none moves for the wait limit, set the abort word (all spinning waits give up)
+            const uint64_t tlim = g_favor_test_wait_ns;
+            const uint64_t limit = tlim ? tlim : kWaitLimitNs;
+            volatile uint32_t* beat = s_beat;
+            volatile uint32_t* done = &s_done;
+            volatile int* abort_word = &s_abort;
+            uint32_t last = beat[0] + beat[1] + beat[2];
+            uint64_t t0 = globaltimer();
+            while (*done < (uint32_t)(kThreads / 32 - 1)) {
+                __nanosleep(1000);
+                const uint32_t now_beat = beat[0] + beat[1] + beat[2];
+                const uint64_t now = globaltimer();
+                if (now_beat != last) {
+                    last = now_beat;
+                    t0 = now;
+                } else if (now - t0 > limit && !*abort_word) {
+                    atomicOr(&g_favor_error, kDevErrTimeout);
+                    *abort_word = 1;
+                }
+            }
         }
     }
+    // this warp's role has ended (the watchdog's warp is not counted: it waits for the others)
+    if (lane == 0 && warp != kSWarp0 + 1) atomicAdd(&s_done, 1u);
     tc_fence_before();
     __syncthreads();
 #ifdef FAVOR_SCAN_TRACE
