@@ -436,8 +436,15 @@ favor_status_t tc_causal(const void* Q, const void* K, const void* V, const void
     tcs::ScanParams sp{n, m, kind, eps * std::sqrt((float)m), feat_scale(64, kind), static_cast<__nv_bfloat16*>(Y),
                        BH, cs, ring, flags};
     const size_t smem = tcs::ScanSmem::bytes();
-    auto kern = cs > 1 ? (kind == kKindExp ? tcs::causal_scan<kKindExp, true> : kind == kKindRelu ? tcs::causal_scan<kKindRelu, true> : tcs::causal_scan<kKindElu, true>)
-                       : (kind == kKindExp ? tcs::causal_scan<kKindExp, false> : kind == kKindRelu ? tcs::causal_scan<kKindRelu, false> : tcs::causal_scan<kKindElu, false>);
+    using ScanKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, tcs::ScanParams);
+    // the instance for 4 CTAs per group reads CS from the parameters (CSX = 0)
+    static const ScanKernel kScan[3][4] = {
+        {tcs::causal_scan<kKindExp, 1>, tcs::causal_scan<kKindExp, 2>, tcs::causal_scan<kKindExp, 3>, tcs::causal_scan<kKindExp, 0>},
+        {tcs::causal_scan<kKindRelu, 1>, tcs::causal_scan<kKindRelu, 2>, tcs::causal_scan<kKindRelu, 3>, tcs::causal_scan<kKindRelu, 0>},
+        {tcs::causal_scan<kKindElu, 1>, tcs::causal_scan<kKindElu, 2>, tcs::causal_scan<kKindElu, 3>, tcs::causal_scan<kKindElu, 0>}};
+    const int ki = kind == kKindExp ? 0 : kind == kKindRelu ? 1 : 2;
+    if (cs < 1 || cs > tcs::kMaxCluster) return FAVOR_ERR_UNSUPPORTED;
+    const ScanKernel kern = kScan[ki][cs - 1];
     FAVOR_TRY(set_smem(kern, smem));
     if (cs > 1 && cudaMemsetAsync(flags, 0, (size_t)G * tcs::kFlagWords * 4, s) != cudaSuccess) return FAVOR_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};

@@ -188,15 +188,18 @@ __device__ __forceinline__ bool scan_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // KIND: the feature family (kKindExp, kKindRelu, kKindElu), fixed per instance so that each
-// instance carries only its own feature map and stabiliser code. GROUPED: CS > 1 (the ring, the
-// X team and the signal warps); without it, CS = 1 and the O team writes the output rows.
-template <int KIND, bool GROUPED>
+// instance carries only its own feature map and stabiliser code. CSX: the CTAs of a group, CS =
+// ceil(m / 128), fixed per instance (1, 2, 3: the combine unrolled over exactly CS partials), or
+// 0 for CS read from the parameters (the instance for CS = 4, which runs faster so, measured);
+// with CS > 1 the ring, the X team and the signal warps, with CS = 1 the O team writes the output.
+template <int KIND, int CSX>
 __global__ void __launch_bounds__(kThreads, 1)
     causal_scan(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                 const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mOm, ScanParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];  // aligned to 1024 by hand below
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int CS = GROUPED ? p.cs : 1;
+    constexpr bool GROUPED = CSX != 1;
+    const int CS = CSX > 0 ? CSX : p.cs;
     const int G = (int)gridDim.x / CS;  // groups
     const int grp = (int)blockIdx.x / CS, rank = (int)blockIdx.x % CS;
     const int RP = (kTile + CS - 1) / CS;  // rows finalised by each CTA of the group
@@ -888,7 +891,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool failed = false;
             // One tile: passes of 32 rows, four threads per row with two 16-byte chunks each.
             auto combine = [&](int tc, int bh, int t) {  // tile t of head bh, the sequence's tile tc
-                constexpr int NC = kMaxCluster;  // partials past CS carry no weight
+                constexpr int NC = CSX > 0 ? CSX : kMaxCluster;  // partials past CS carry no weight
                 const int slot = tc % kRing;
 #pragma unroll 1
                 for (int item = xt; item < rows * 4; item += 32 * kXWarps) {
