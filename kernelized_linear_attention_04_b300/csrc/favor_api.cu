@@ -326,7 +326,9 @@ favor_status_t tc_fused(const void* Q, const void* K, const void* V, const void*
     tcfu::FusedParams fp{n,  m,  m_pad, kind, eps * std::sqrt((float)m), feat_scale(64, kind), static_cast<__nv_bfloat16*>(Y),
                          Pp, Zp, Stab};
     const size_t smem = tcfu::FusedSmem::bytes(m_pad);
-    FAVOR_TRY(set_smem(tcfu::nc_fused_small, smem));
+    // one instance per feature family (each carries only its own feature map)
+    auto kfused = kind == kKindExp ? tcfu::nc_fused_small<kKindExp> : kind == kKindRelu ? tcfu::nc_fused_small<kKindRelu> : tcfu::nc_fused_small<kKindElu>;
+    FAVOR_TRY(set_smem(kfused, smem));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(BH * T, 1, 1);
     cfg.blockDim = dim3(tcfu::kThreads, 1, 1);
@@ -340,7 +342,7 @@ favor_status_t tc_fused(const void* Q, const void* K, const void* V, const void*
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t lerr = cudaSuccess;
-    FAVOR_TRY(traced(FAVOR_KERNEL_FUSED, s, [&] { lerr = cudaLaunchKernelEx(&cfg, tcfu::nc_fused_small, mQ, mK, mV, mOm, fp); }));
+    FAVOR_TRY(traced(FAVOR_KERNEL_FUSED, s, [&] { lerr = cudaLaunchKernelEx(&cfg, kfused, mQ, mK, mV, mOm, fp); }));
     return lerr == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA;
 }
 
@@ -365,7 +367,7 @@ favor_status_t tc_noncausal(const void* Q, const void* K, const void* V, const v
 
     tcnc::StateParams sp{n, m, w.m_pad, groups, w.tokens_per_split, kind, eps_s, sc, pS, pz, pst};
     const size_t smem_state = tcnc::StateSmem<D>::bytes(groups);
-    auto kstate = tcnc::nc_state_tc<D>;
+    auto kstate = kind == kKindExp ? tcnc::nc_state_tc<D, kKindExp> : kind == kKindRelu ? tcnc::nc_state_tc<D, kKindRelu> : tcnc::nc_state_tc<D, kKindElu>;
     FAVOR_TRY(set_smem(kstate, smem_state));
     FAVOR_TRY(traced(FAVOR_KERNEL_STATE, s, [&] {
         kstate<<<dim3(w.splits, BH, 1), tcnc::kStateThreads, smem_state, s>>>(mK, mV, mOm, sp);
@@ -391,7 +393,7 @@ favor_status_t tc_noncausal(const void* Q, const void* K, const void* V, const v
     if (lerr != cudaSuccess) return FAVOR_ERR_CUDA;
     tcnc::ReadoutParams rp{n, w.m_pad, m, w.tiles_per_cta, kind, eps_s, sc, img, zf, static_cast<__nv_bfloat16*>(Y)};
     const size_t smem_read = tcnc::ReadoutSmem<D>::bytes(w.m_pad);
-    auto kread = tcnc::nc_readout_tc<D>;
+    auto kread = kind == kKindExp ? tcnc::nc_readout_tc<D, kKindExp> : kind == kKindRelu ? tcnc::nc_readout_tc<D, kKindRelu> : tcnc::nc_readout_tc<D, kKindElu>;
     FAVOR_TRY(set_smem(kread, smem_read));
     cudaLaunchConfig_t rc = {};
     rc.gridDim = dim3(w.chunks, BH, 1);

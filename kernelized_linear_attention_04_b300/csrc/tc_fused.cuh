@@ -63,6 +63,7 @@ struct FusedSmem {
     }
 };
 
+template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     nc_fused_small(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                    const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mOm, FusedParams p) {
@@ -108,7 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
         // the peers' rows of the operand (and of the remainder, exp family) arrive by bulk copies
         // (after the first cluster barrier)
-        mbar_arrive_expect_tx(&bar_img, (uint32_t)(MP - own_rows) * 128 * (p.kind == kKindExp ? 2u : 1u));
+        mbar_arrive_expect_tx(&bar_img, (uint32_t)(MP - own_rows) * 128 * (KIND == kKindExp ? 2u : 1u));
         // the loads start before the TMEM allocation and the CTA barrier
         tma_prefetch_desc(&mQ);
         tma_prefetch_desc(&mK);
@@ -179,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     }
     const float A2 = p.scale * kLog2e;
-    const bool exp_kind = p.kind == kKindExp;
+    const bool exp_kind = KIND == kKindExp;
     const int ew = warp - 1;  // epilogue warp index (warp 0 has -1)
     const int q = warp & 3;
     const int r = q * 32 + lane;
@@ -242,8 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         f0 = ex2(fmaf(a0, A2, -(cj[i] + stab)));
                         f1 = ex2(fmaf(a1, A2, -(cj[i + 1] + stab)));
                     } else {
-                        f0 = cj[i] == 0.f ? phi_plain(a0 * p.scale, p.kind, 1.f, p.relu_eps_s) : 0.f;
-                        f1 = cj[i + 1] == 0.f ? phi_plain(a1 * p.scale, p.kind, 1.f, p.relu_eps_s) : 0.f;
+                        f0 = cj[i] == 0.f ? phi_plain(a0 * p.scale, KIND, 1.f, p.relu_eps_s) : 0.f;
+                        f1 = cj[i + 1] == 0.f ? phi_plain(a1 * p.scale, KIND, 1.f, p.relu_eps_s) : 0.f;
                     }
                     if (!real_feat) f0 = f1 = 0.f;
                     zpart += f0 + f1;
@@ -308,8 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     f0 = ex2(fmaf(__uint_as_float(v[i]), A2, -cst));
                     f1 = ex2(fmaf(__uint_as_float(v[i + 1]), A2, -cst));
                 } else {
-                    f0 = phi_plain(__uint_as_float(v[i]) * p.scale, p.kind, 1.f, p.relu_eps_s);
-                    f1 = phi_plain(__uint_as_float(v[i + 1]) * p.scale, p.kind, 1.f, p.relu_eps_s);
+                    f0 = phi_plain(__uint_as_float(v[i]) * p.scale, KIND, 1.f, p.relu_eps_s);
+                    f1 = phi_plain(__uint_as_float(v[i + 1]) * p.scale, KIND, 1.f, p.relu_eps_s);
                 }
                 pk[i / 2] = pack_bf16(f0, f1);
             }
@@ -426,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint64_t bd = sdesc_sw128(smem_u32(sS + ks * 2048), (uint32_t)MP * 128, 1024);
                     mma_ts(tbase, tbase + 256 + ks * 8, bd, id_n, ks > 0);
                 }
-                if (p.kind == kKindExp) {
+                if (KIND == kKindExp) {
                     constexpr uint32_t id_lo = idesc_bf16(128, kD, false, true);
                     for (int ks = 0; ks < MP / 16; ++ks) {
                         uint64_t bd = sdesc_sw128(smem_u32(sSlo + ks * 2048), 16, 1024);

@@ -122,7 +122,7 @@ constexpr int kStateNormWarps = 2;
 constexpr int kStateEpiWarp0 = 2 + kStateNormWarps;
 constexpr int kStateThreads = 32 * (kStateEpiWarp0 + kStateEpiWarps);
 
-template <int D>
+template <int D, int KIND>
 __global__ void __launch_bounds__(kStateThreads, 1)
     nc_state_tc(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
                 const __grid_constant__ CUtensorMap mOm, StateParams p) {
@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
         const int nt = 32 * kStateNormWarps;
         bool ok = mbar_wait(&bar_om, 0, &abort_flag);
         float W = 0.f;
-        if (p.kind == kKindExp) {
+        if (KIND == kKindExp) {
             float w2 = 0.f;
             for (int row = nw * 32 + lane; row < G * 128; row += nt) {
                 const int g = row >> 7, rr = row & 127;
@@ -332,14 +332,14 @@ __global__ void __launch_bounds__(kStateThreads, 1)
             for (int i = 0; i < 2; ++i) {
                 const int tok = nw * 64 + lane + 32 * i;
                 v2[i] = j0 + t * kTile + tok < j1;
-                const float xn2 = p.kind == kKindExp ? p.scale * p.scale * tile_row_sqnorm<D>(kt, tok) : 0.f;
+                const float xn2 = KIND == kKindExp ? p.scale * p.scale * tile_row_sqnorm<D>(kt, tok) : 0.f;
                 h2[i] = 0.5f * xn2;
                 if (v2[i]) bmax = fmaxf(bmax, W * sqrtf(xn2) - h2[i]);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_kempty[st]);
             float f = 1.f;
-            if (p.kind == kKindExp) {
+            if (KIND == kKindExp) {
                 const float wm = warp_max(bmax);
                 if (lane == 0) sRed[b2][nw] = wm;
                 named_bar(2, nt);
@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 #pragma unroll
             for (int i = 0; i < 2; ++i)
                 sC[b2 * 128 + nw * 64 + lane + 32 * i] =
-                    v2[i] ? (p.kind == kKindExp ? (h2[i] + stab) * kLog2e : 0.f) : INFINITY;
+                    v2[i] ? (KIND == kKindExp ? (h2[i] + stab) * kLog2e : 0.f) : INFINITY;
             if (nw == 0 && lane == 0) {
                 sF[b2] = f;
                 sStabT[b2] = stab;
@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
             if (lane == 0) mbar_arrive(&bar_nfull[b2]);
         }
         if (nw == 0 && lane == 0)
-            p.pstab[((size_t)bh * splits + split) * fslices + fslice] = (p.kind == kKindExp && ok) ? stab : 0.f;
+            p.pstab[((size_t)bh * splits + split) * fslices + fslice] = (KIND == kKindExp && ok) ? stab : 0.f;
     } else {
         // ---------------- epilogue: two teams of 8 warps ----------------
         // Team tm handles the units u = tm (mod 2). Within a team, warp (cg, q) reads TMEM lane
@@ -459,7 +459,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
                     for (int i = 0; i < 32; i += 4) {
                         const float4 c4 = *reinterpret_cast<const float4*>(cc + i);
                         float f[4];
-                        if (p.kind == kKindExp) {
+                        if (KIND == kKindExp) {
                             const float e0 = fmaf(__uint_as_float(vv[i + 0]), A2, -c4.x);
                             const float e1 = fmaf(__uint_as_float(vv[i + 1]), A2, -c4.y);
                             const float e2 = fmaf(__uint_as_float(vv[i + 2]), A2, -c4.z);
@@ -470,10 +470,10 @@ __global__ void __launch_bounds__(kStateThreads, 1)
                             f[3] = ex2(e3);
                             umu = fmaxf(umu, fmaxf(fmaxf(e0, e1), fmaxf(e2, e3)));
                         } else {
-                            f[0] = c4.x == 0.f ? phi_plain(__uint_as_float(vv[i + 0]) * p.scale, p.kind, 1.f, p.relu_eps_s) : 0.f;
-                            f[1] = c4.y == 0.f ? phi_plain(__uint_as_float(vv[i + 1]) * p.scale, p.kind, 1.f, p.relu_eps_s) : 0.f;
-                            f[2] = c4.z == 0.f ? phi_plain(__uint_as_float(vv[i + 2]) * p.scale, p.kind, 1.f, p.relu_eps_s) : 0.f;
-                            f[3] = c4.w == 0.f ? phi_plain(__uint_as_float(vv[i + 3]) * p.scale, p.kind, 1.f, p.relu_eps_s) : 0.f;
+                            f[0] = c4.x == 0.f ? phi_plain(__uint_as_float(vv[i + 0]) * p.scale, KIND, 1.f, p.relu_eps_s) : 0.f;
+                            f[1] = c4.y == 0.f ? phi_plain(__uint_as_float(vv[i + 1]) * p.scale, KIND, 1.f, p.relu_eps_s) : 0.f;
+                            f[2] = c4.z == 0.f ? phi_plain(__uint_as_float(vv[i + 2]) * p.scale, KIND, 1.f, p.relu_eps_s) : 0.f;
+                            f[3] = c4.w == 0.f ? phi_plain(__uint_as_float(vv[i + 3]) * p.scale, KIND, 1.f, p.relu_eps_s) : 0.f;
                         }
                         pk[i / 2] = pack_bf16(f[0], f[1]);
                         pk[i / 2 + 1] = pack_bf16(f[2], f[3]);
@@ -492,7 +492,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
                 if (lane == 0) mbar_arrive(&bar_phi[s]);
                 if (real_feat) umax = fmaxf(umax, umu);
             }
-            if (p.kind == kKindExp) {  // for the key constant two tiles on (nats, absolute)
+            if (KIND == kKindExp) {  // for the key constant two tiles on (nats, absolute)
                 umax = warp_max(umax);
                 if (lane == 0) sUnitMax[t & 3][ew] = umax == -INFINITY ? -INFINITY : umax / kLog2e + stab_t;
             }
@@ -652,7 +652,7 @@ struct ReadoutSmem {
     }
 };
 
-template <int D>
+template <int D, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     nc_readout_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mOm, ReadoutParams p) {
     using SM = ReadoutSmem<D>;
@@ -815,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = q * 32 + lane;  // token row of the tile
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         const float A2 = p.scale * kLog2e;
-        const bool exp_kind = p.kind == kKindExp;
+        const bool exp_kind = KIND == kKindExp;
         bool failed = !mbar_wait(&bar_const, 0, &abort_flag);
         __syncwarp();
         bool have_sz = false;
@@ -829,7 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     f[k] = exp_kind ? ex2(fmaf(__uint_as_float(v[i + k]), A2, -cst))
-                                    : phi_plain(__uint_as_float(v[i + k]) * p.scale, p.kind, 1.f, p.relu_eps_s);
+                                    : phi_plain(__uint_as_float(v[i + k]) * p.scale, KIND, 1.f, p.relu_eps_s);
                 const uint32_t w0 = pack_bf16(f[0], f[1]), w1 = pack_bf16(f[2], f[3]);
                 pk[i / 2] = w0;
                 pk[i / 2 + 1] = w1;
