@@ -544,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float c = 0.f;
             if (exp_kind) {
                 float mx = -INFINITY;
-#pragma unroll
+#pragma unroll 1
                 for (int cc = 0; cc < 2; ++cc) {
                     if (32 * cc < fv) {
                         uint32_t v[32];
@@ -596,7 +596,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (exp_kind) {
                 failed |= !scan_wait(&bar_kfull, t & 1);
                 __syncwarp();
-                kn = 0.5f * s2 * tile_row_sqnorm<64>(sK, r) * kLog2e;
+                float sa = 0.f, sb = 0.f;  // |k_r|^2 over the 8 chunks of the row, one chunk per step
+#pragma unroll 1
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 kv = *reinterpret_cast<const uint4*>(sK + sw128_offset(r, c));
+                    tcnc::sq_acc_bf16x2(kv.x, sa, sb);
+                    tcnc::sq_acc_bf16x2(kv.y, sa, sb);
+                    tcnc::sq_acc_bf16x2(kv.z, sa, sb);
+                    tcnc::sq_acc_bf16x2(kv.w, sa, sb);
+                }
+                kn = 0.5f * s2 * (sa + sb) * kLog2e;
             }
             failed |= !scan_wait(&bar_pk[b], u & 1);
             if (warp == kKWarp0 && lane == 0) SCAN_TRACE(t, 8);
@@ -607,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float f = 1.f;
             if (exp_kind) {
                 float mx = -INFINITY;
-#pragma unroll
+#pragma unroll 1
                 for (int cc = 0; cc < 4; ++cc) {
                     if (32 * cc < fv) {
                         uint32_t v[32];
