@@ -87,6 +87,33 @@ def test_causal_scan_feature_groups(favor, kind, n, m):
     assert_close_attn(f64(Y), ref, "bf16", f"causal {kind} n={n} m={m}")
 
 
+# The scan runs a persistent grid: G = min(heads, SMs // CS) groups of CS = ceil(m / 128) CTAs,
+# group g taking heads g, g + G, ... one after another, the state, the key stabiliser and NUM
+# restarting at each head's first tile. Heads past the first round (and the first and last heads)
+# against the oracle, for every family and group size.
+ROUND_CASES = [("exp", 512, 300), ("relu", 512, 300), ("exp", 384, 130), ("relu", 256, 300),
+               ("exp", 128, 130), ("elu", 64, 200)]
+
+
+@pytest.mark.parametrize("kind,m,n", ROUND_CASES)
+def test_causal_scan_heads_over_rounds(favor, kind, m, n):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    cs = -(-m // 128)
+    groups = sms // cs
+    H = groups + 3  # three groups take a second head
+    w = si.Workload("case", 1, H, n, 64, m, "bf16", True, kind=kind, seed=91 + m, omega_seed=13 + m)
+    Q, K, V, Om, om64 = device_inputs(w)
+    Y = run_attn(favor, w, Q, K, V, Om)
+    assert favor.last_device_error() == 0
+    heads = [0, 1, groups - 1, groups, groups + 1, H - 1]
+    if kind == "elu":  # elu + 1 features of the raw q, k (no Omega)
+        ref = oracle.attn_linear_elu(f64(Q[0, heads]), f64(K[0, heads]), f64(V[0, heads]), causal=True)
+    else:
+        ref = oracle_attn(w, f64(Q[0, heads]), f64(K[0, heads]), f64(V[0, heads]), om64)
+    for i, h in enumerate(heads):
+        assert_close_attn(f64(Y[0, h]), ref[i], "bf16", f"causal {kind} m={m} n={n} head {h} of {H}")
+
+
 NONCAUSAL_PATH_CASES = (
     [("relu", n, d, m) for n in (1025, 1500, 4099) for d in (64, 128) for m in (128, 256)]
     + [("exp", n, 64, 256) for n in (1025, 4096)]

@@ -1,8 +1,9 @@
 """The bounded-wait failure path on the device, exercised without any fault or hang.
 
-Every mbarrier wait in the tensor-core kernels gives up after a time limit, records FAVOR_ERR_TIMEOUT
-in the device error word, tells the CTA's other roles to stop, drains its copies in flight and
-frees its tensor memory. favor_test_set_wait_limit arms a test hook that shortens the limit to a
+Every mbarrier wait in the tensor-core kernels gives up after a time limit (in the causal scan, once
+the CTA's watchdog lane has seen no progress for that long), records FAVOR_ERR_TIMEOUT in the device
+error word, tells the CTA's other roles to stop, drains its copies in flight and frees its tensor
+memory. m = 128 runs the scan's single-CTA instance, m = 512 a group of four CTAs. favor_test_set_wait_limit arms a test hook that shortens the limit to a
 millisecond and makes the causal scan withhold one arrival, so that one wait runs out for sure;
 the test then checks that the status reaches the host and that the next normal call on the same
 device still matches the oracle.
