@@ -728,7 +728,8 @@ def run_sweep(args):
         torch.cuda.synchronize()
         return float(np.median([a.elapsed_time(b) for a, b in evs]))
 
-    for causal in (False, True):
+    forms = {"both": (False, True), "noncausal": (False,), "causal": (True,)}[args.sweep_form]
+    for causal in forms:
         for n in ns:
             base = si.Workload("sweep", 1, 8, n, 64, ms[0], "bf16", causal, kind="exp", seed=101 + n, omega_seed=7)
             full = si.full_inputs(base)
@@ -782,6 +783,8 @@ def main(argv=None):
                     help="FAVOR+ (exp features) against the exact softmax kernel over n and m: time and divergence")
     ap.add_argument("--sweep-n", default=None, help="comma-separated sequence lengths for --sweep")
     ap.add_argument("--sweep-m", default=None, help="comma-separated feature counts for --sweep")
+    ap.add_argument("--sweep-form", default="both", choices=["both", "noncausal", "causal"],
+                    help="the attention forms --sweep covers")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
