@@ -190,7 +190,7 @@ __device__ __forceinline__ bool scan_wait(uint64_t* bar, uint32_t parity) {
 // KIND: the feature family (kKindExp, kKindRelu, kKindElu), fixed per instance so that each
 // instance carries only its own feature map and stabiliser code. CSX: the CTAs of a group, CS =
 // ceil(m / 128), fixed per instance (1, 2, 3: the combine unrolled over exactly CS partials), or
-// 0 for CS read from the parameters (the instance for CS = 4, which runs faster so, measured);
+// 0 for CS read from the parameters (used for CS = 4, where it measured faster than a fixed CS);
 // with CS > 1 the ring, the X team and the signal warps, with CS = 1 the O team writes the output.
 template <int KIND, int CSX>
 __global__ void __launch_bounds__(kThreads, 1)
