@@ -59,7 +59,7 @@ NCU_TRAFFIC: dict[str, dict] = {
     "noncausal_bf16_B1H8n1024d64m256:fused": {"bytes": 3253248, "src": "09c185d466e8dabc"},
     # profiles/causal_scan_relu_bf16_B8H32n32768d64m512.md: a 32-head x 8192-token capture
     # (118,248,960 bytes) scaled by the 32x more tokens of the full launch
-    "causal_relu_bf16_B8H32n32768d64m512:causal": {"bytes": 3783966720, "src": "d90161917cce3966"},
+    "causal_relu_bf16_B8H32n32768d64m512:causal": {"bytes": 3783966720, "src": "4f9a3a0886ca0d83"},
 }
 
 
