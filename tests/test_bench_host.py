@@ -78,6 +78,15 @@ def test_argument_checks():
         os.environ.update(env)
 
 
+def test_sweep_form_choices():
+    # --sweep covers both forms by default; --sweep-form narrows it; anything else is refused
+    out = subprocess.run([sys.executable, "bench.py", "--help"], cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                         capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0 and "--sweep-form {both,noncausal,causal}" in out.stdout
+    with pytest.raises(SystemExit):
+        bench.main(["--sweep", "--sweep-form", "sideways"])
+
+
 def free_port() -> int:
     with socket.socket() as s:
         s.bind(("127.0.0.1", 0))
