@@ -60,6 +60,8 @@ NCU_TRAFFIC: dict[str, dict] = {
     # profiles/causal_scan_relu_bf16_B8H32n32768d64m512.md: a 32-head x 8192-token capture
     # (118,248,960 bytes) scaled by the 32x more tokens of the full launch
     "causal_relu_bf16_B8H32n32768d64m512:causal": {"bytes": 3783966720, "src": "4f9a3a0886ca0d83"},
+    # profiles/causal_scan_exp_bf16_B4H16n8192d64m256.md: the full launch captured
+    "causal_bf16_B4H16n8192d64m256:causal": {"bytes": 250125312, "src": "4f9a3a0886ca0d83"},
 }
 
 
