@@ -77,7 +77,8 @@ def test_workspace_sizes_per_path():
     # after 16 u32 counters per group (256-byte piece), for min(B*H, 160 // CS) groups
     for m in (64, 128):
         assert favor.workspace_bytes("causal", 4, 16, 8192, 64, m, bf) == 0
-    for BH, m, cs in ((64, 192, 2), (64, 256, 2), (64, 384, 3), (64, 512, 4), (256, 512, 4), (7, 384, 3)):
+    for BH, m, cs in ((64, 192, 2), (64, 256, 2), (64, 384, 3), (64, 512, 4), (256, 512, 4), (7, 384, 3),
+                      (1000, 512, 4), (1000, 384, 3), (1000, 256, 2)):
         groups = min(BH, 160 // cs)
         assert favor.workspace_bytes("causal", 1, BH, 8192, 64, m, bf) == up(groups * 64) + groups * 4 * cs * 9 * 128 * 16
     # streaming decode state: fp32 S [BH][m][d], z [BH][m], stabilisers [BH][m/64], block partials
